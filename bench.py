@@ -1,0 +1,507 @@
+"""Benchmark: decode-attention µs per layer-step and effective KV GB/s (% of HBM peak).
+
+One step = one pass of the whole hot path on one layer: on-device encode of the new K and
+V row into the resident store (kvq_append x2), seq_lens += 1, and the split-K fused
+dequant flash-decode (kvq_flash_decode: decode kernel + combine kernel).  The store grows
+by one token per step.  Inputs are resident in HBM when the timed region starts; the L2
+is flushed (a 2 x L2 write) before every timed step, outside its events.
+
+Default workload: 8B-class decode layer, one sequence, 32 query heads on 8 KV heads,
+head_dim 128, kv_len 65536, q8_0 K and V; the sweep adds every codec arm at kv_len 4096,
+16384 and 65536 (kernel-only timings).  `value` is effective KV GB/s: the KV bytes one
+decode reads (kv_len x kv_heads x bytes per token-head of K and V, scales included)
+divided by the step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload layer8b|longctx|ragged|resident] [--codec q8_0/q8_0]
+                    [--kv-len L] [--variant 0|1|2] [--no-sweep]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention µs/layer-step & effective KV GB/s (% of HBM peak) vs kv_len"
+FALLBACK_HBM_GBS = 6800.0
+ROW_BYTES = {"bf16": lambda d: 2 * d, "f16": lambda d: 2 * d, "q8_0": lambda d: d + d // 16,
+             "q4s": lambda d: d // 2 + d // 16}
+
+WORKLOADS = {
+    "layer8b": dict(batch=1, hq=32, hkv=8, d=128, kv_len=65536, dist="normal", scaled=False,
+                    codec="q8_0/q8_0"),
+    "longctx": dict(batch=1, hq=32, hkv=2, d=256, kv_len=204800, dist="normal", scaled=True,
+                    codec="q8_0/q8_0"),
+    "ragged": dict(batch=64, hq=32, hkv=8, d=128, kv_len=None, dist="normal", scaled=False,
+                   codec="q8_0/q8_0"),
+    "resident": dict(batch=1, hq=32, hkv=8, d=128, kv_len=65536, dist="t3", scaled=True,
+                     codec="q8_0/q8_0"),
+}
+
+
+def token_head_bytes(codec_pair: str, d: int) -> int:
+    kc, vc = codec_pair.split("/")
+    return ROW_BYTES[kc](d) + ROW_BYTES[vc](d)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                j = json.load(f)
+            for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if key in j:
+                    return float(j[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "flash_decode_quantized_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_sha: str, workload_key: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == workload_key and parts[1] == kernel_sha:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- device side
+
+def device_rows(torch, gen, n, hkv, d, dist, scales):
+    if dist == "normal":
+        x = torch.randn((n, hkv, d), generator=gen, device="cuda", dtype=torch.float32)
+    else:  # Student-t, 3 degrees of freedom: N / sqrt(chi2_3 / 3)
+        z = torch.randn((n, hkv, d), generator=gen, device="cuda", dtype=torch.float32)
+        c = torch.randn((3, n, hkv, d), generator=gen, device="cuda", dtype=torch.float32)
+        x = z / torch.sqrt((c * c).sum(0) / 3.0)
+    if scales is not None:
+        x = x * scales
+    return x.to(torch.bfloat16)
+
+
+class Layer:
+    """One decode layer's resident stores plus per-step inputs, on the current device."""
+
+    def __init__(self, kvq, torch, wl, codec_pair, seq_lens, capacity_extra, seed, page_size=256):
+        self.kvq, self.torch = kvq, torch
+        self.hq, self.hkv, self.d = wl["hq"], wl["hkv"], wl["d"]
+        self.kc, self.vc = codec_pair.split("/")
+        self.batch = len(seq_lens)
+        self.page_size = page_size
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        ks = vs = None
+        if wl["scaled"]:
+            lo, hi = math.log(0.25), math.log(4.0)
+            ks = torch.exp(torch.rand((self.hkv, self.d), generator=gen, device="cuda") * (hi - lo) + lo)
+            vs = torch.exp(torch.rand((self.hkv, self.d), generator=gen, device="cuda") * (hi - lo) + lo)
+        self.k_scales, self.v_scales, self.dist = ks, vs, wl["dist"]
+        caps = [int(L) + capacity_extra for L in seq_lens]
+        pages = [max(1, -(-c // page_size)) for c in caps]
+        total = int(sum(pages))
+        perm = torch.randperm(total, generator=gen, device="cuda").to(torch.int32)
+        self.max_pages = max(pages)
+        pt = torch.full((self.batch, self.max_pages), -1, dtype=torch.int32, device="cuda")
+        pos = 0
+        for b, n in enumerate(pages):
+            pt[b, :n] = perm[pos:pos + n]
+            pos += n
+        self.page_table = pt
+        self.k_store = kvq.kvq_store_create(self.kc, self.hkv, self.d, page_size, total)
+        self.v_store = kvq.kvq_store_create(self.vc, self.hkv, self.d, page_size, total)
+        self.seq_lens = torch.zeros(self.batch, dtype=torch.int32, device="cuda")
+        for b, L in enumerate(seq_lens):
+            done = 0
+            while done < L:
+                n = min(32768, int(L) - done)
+                seq = torch.tensor([done], dtype=torch.int32, device="cuda")
+                kr = device_rows(torch, gen, n, self.hkv, self.d, self.dist, ks)
+                vr = device_rows(torch, gen, n, self.hkv, self.d, self.dist, vs)
+                kvq.kvq_append(self.k_store, kr[None], seq, pt[b:b + 1].contiguous())
+                kvq.kvq_append(self.v_store, vr[None], seq, pt[b:b + 1].contiguous())
+                done += n
+        self.seq_lens.copy_(torch.tensor(list(seq_lens), dtype=torch.int32))
+        self.host_lens = [int(L) for L in seq_lens]
+        self.q = torch.randn((self.batch, self.hq, self.d), generator=gen, device="cuda").to(torch.bfloat16)
+        self.new_k = device_rows(torch, gen, 1, self.hkv, self.d, self.dist, ks).view(1, 1, self.hkv, self.d).expand(self.batch, 1, self.hkv, self.d).contiguous()
+        self.new_v = device_rows(torch, gen, 1, self.hkv, self.d, self.dist, vs).view(1, 1, self.hkv, self.d).expand(self.batch, 1, self.hkv, self.d).contiguous()
+        self.out = torch.empty((self.batch, self.hq, self.d), dtype=torch.float32, device="cuda")
+        self.hint = max(caps)
+        self.ws = None
+
+    def prepare(self, variant, chunk_tokens=0):
+        n = self.kvq.kvq_decode_workspace_bytes(self.k_store, self.batch, self.hq, self.hint,
+                                                chunk_tokens, variant)
+        self.ws = self.torch.empty(n, dtype=self.torch.uint8, device="cuda")
+        self.variant, self.chunk = variant, chunk_tokens
+
+    def append(self, new_k=None, new_v=None):
+        kvq = self.kvq
+        kvq.kvq_append(self.k_store, self.new_k if new_k is None else new_k, self.seq_lens, self.page_table)
+        kvq.kvq_append(self.v_store, self.new_v if new_v is None else new_v, self.seq_lens, self.page_table)
+        kvq.kvq_seq_lens_add(self.seq_lens, 1)
+        self.host_lens = [L + 1 for L in self.host_lens]
+
+    def decode(self, q=None):
+        return self.kvq.kvq_flash_decode(self.q if q is None else q, self.k_store, self.v_store,
+                                         self.seq_lens, self.page_table, out=self.out,
+                                         max_len_hint=self.hint, workspace=self.ws,
+                                         chunk_tokens=self.chunk, variant=self.variant)
+
+    def kv_bytes(self):
+        return sum(self.host_lens) * self.hkv * token_head_bytes(f"{self.kc}/{self.vc}", self.d)
+
+
+def l2_flusher(torch):
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device="cuda")
+    return lambda: buf.fill_(1.0)
+
+
+def time_decode_only(torch, layer, flush, iters):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for i in range(iters):
+        flush()
+        ev[i][0].record()
+        layer.decode()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_mine(args, rank, world):
+    import torch
+    from flash_decode_quantized_gb300 import kvq
+
+    torch.cuda.set_device(rank % max(1, torch.cuda.device_count()))
+    wl = dict(WORKLOADS[args.workload])
+    codec = args.codec or wl["codec"]
+    if wl["kv_len"] is None:
+        from workloads import ragged_lengths
+        seq_lens = [int(x) for x in ragged_lengths(1234 + rank, wl["batch"])]
+    else:
+        seq_lens = [args.kv_len or wl["kv_len"]] * wl["batch"]
+    extra = args.warmup + args.steps + 64
+    layer = Layer(kvq, torch, wl, codec, seq_lens, extra, seed=1000 + rank)
+    layer.prepare(args.variant, args.chunk_tokens)
+    flush = l2_flusher(torch)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush()
+        layer.append()
+        layer.decode()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    kv_bytes = []
+    launches0 = kvq.kvq_launch_count()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(K):
+            flush()
+            ev[i][0].record()
+            layer.append()
+            ev[i][1].record()
+            layer.decode()
+            ev[i][2].record()
+            kv_bytes.append(layer.kv_bytes())
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    launches = kvq.kvq_launch_count() - launches0
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    ms_per_step = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms_per_step], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    kvb = statistics.mean(kv_bytes)
+    value = world * kvb / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    dec_mean = statistics.mean(dec_ms)
+    achieved = kvb / (dec_mean * 1e-3) / 1e9
+    sha = kernel_sources_sha()
+    key = f"{args.workload}:{codec}:{seq_lens[0] if len(set(seq_lens)) == 1 else 'ragged'}"
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(sha, key),
+                "kernel": "kvq_flash_decode call (decode + combine kernels)",
+                "peak_source": f"{peak_kind} copy bandwidth",
+                "decode_us": round(dec_mean * 1e3, 2),
+                "decode_us_p10_p90": [round(float(np.percentile(dec_ms, 10)) * 1e3, 2),
+                                      round(float(np.percentile(dec_ms, 90)) * 1e3, 2)],
+                "cv": round(statistics.pstdev(dec_ms) / dec_mean, 4)}
+
+    e2e = measure_e2e(torch, kvq, layer, flush, max(3, min(K, 20)))
+    e2e["value"] = round(world * e2e.pop("kvb") / (e2e["ms"] * 1e-3) / 1e9, 1)
+
+    sweep = None
+    if rank == 0 and not args.no_sweep and args.workload == "layer8b":
+        sweep = run_sweep(torch, kvq, args, flush, peak)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_layer_step": round(ms_per_step * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, device-generated bf16 rows encoded on device)",
+        "config": {"workload": f"{args.workload}: B={wl['batch']}, Hq={wl['hq']}, Hkv={wl['hkv']}, "
+                               f"D={wl['d']}, kv_len={seq_lens[0] if len(set(seq_lens)) == 1 else 'U[1024,32768]'}",
+                   "codec": codec, "kv_bytes_per_step": int(kvb), "variant": args.variant,
+                   "chunk_tokens": args.chunk_tokens, "l2": "flushed (2xL2 write) before every timed step, outside its events",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+        "kernel_sha": sha,
+        "frac_of_8TBs": round(achieved / 8000.0, 4),
+    }
+    if sweep is not None:
+        result["sweep"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args, wl, codec, seq_lens[0] if wl["kv_len"] else 4096)
+    return result
+
+
+def measure_e2e(torch, kvq, layer, flush, iters):
+    """The same step through the public API with host buffers: pinned q and new rows are
+    copied in, the output copied out, every step, inside the timed region."""
+    q_h = layer.q.cpu().pin_memory()
+    k_h = layer.new_k.cpu().pin_memory()
+    v_h = layer.new_v.cpu().pin_memory()
+    out_h = torch.empty(layer.out.shape, dtype=torch.float32).pin_memory()
+    q_d, k_d, v_d = torch.empty_like(layer.q), torch.empty_like(layer.new_k), torch.empty_like(layer.new_v)
+    ms, kvb = [], []
+    for _ in range(iters):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        layer.append(k_d, v_d)
+        layer.decode(q_d)
+        out_h.copy_(layer.out, non_blocking=True)
+        torch.cuda.synchronize()
+        ms.append((time.perf_counter() - t0) * 1e3)
+        kvb.append(layer.kv_bytes())
+    h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
+    return {"ms": round(statistics.median(ms), 5), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(out_h.numel() * 4), "kvb": statistics.mean(kvb),
+            "timing": "host wall clock around H2D + append + decode + D2H, median"}
+
+
+def run_sweep(torch, kvq, args, flush, peak):
+    """Kernel-only decode timings for every codec arm at kv_len 4096 / 16384 / 65536."""
+    wl = WORKLOADS["layer8b"]
+    arms = ["bf16/bf16", "q8_0/bf16", "q8_0/q8_0", "q4s/q4s", "q8_0/q4s"]
+    rows = []
+    for L in (4096, 16384, 65536):
+        base = None
+        for arm in arms:
+            layer = Layer(kvq, torch, wl, arm, [L], 0, seed=77)
+            layer.prepare(args.variant, 0)
+            time_decode_only(torch, layer, flush, 3)
+            ms = time_decode_only(torch, layer, flush, 20)
+            med = statistics.median(ms)
+            gbs = layer.kv_bytes() / (med * 1e-3) / 1e9
+            if arm == "bf16/bf16":
+                base = med
+            rows.append({"kv_len": L, "codec": arm, "us": round(med * 1e3, 2),
+                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "vs_bf16_time": round(med / base, 3),
+                         "cv": round(statistics.pstdev(ms) / statistics.mean(ms), 4)})
+            del layer
+            torch.cuda.empty_cache()
+    return rows
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _oracle_step(wl, codec, L, kv_heads, seed):
+    """The oracle on a bounded sample of one step: dequantize `kv_heads` KV heads' prefixes
+    and attend with their query heads.  Returns (seconds, KV bytes of the sample)."""
+    from oracle import attention as oatt
+    from oracle import codec as ocodec
+    from workloads import make_inputs
+    kc, vc = codec.split("/")
+    g = wl["hq"] // wl["hkv"]
+    inp = make_inputs([L], g * kv_heads, kv_heads, wl["d"], seed=seed, dist=wl["dist"],
+                      channel_scaled=wl["scaled"])
+    q = ocodec.bf16_bits_to_f64(inp.q)
+    t0 = time.perf_counter()
+    d = wl["d"]
+    kd = ocodec.dequantized(inp.k_rows[0].reshape(-1, d), kc).reshape(L, kv_heads, d)
+    vd = ocodec.dequantized(inp.v_rows[0].reshape(-1, d), vc).reshape(L, kv_heads, d)
+    oatt.attention(q, [kd], [vd], kv_heads, 1 / math.sqrt(d))
+    dt = time.perf_counter() - t0
+    return dt, L * kv_heads * token_head_bytes(codec, d)
+
+
+def cpu_baseline(args, wl, codec, L):
+    cores = len(os.sched_getaffinity(0))
+    times, nbytes = [], 0
+    budget = 20.0
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget and len(times) < 8:
+        dt, b = _oracle_step(wl, codec, L, 1, seed=99 + len(times))
+        times.append(dt)
+        nbytes += b
+    value = nbytes / sum(times) / 1e9
+    return {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} x (1 KV head of {wl['hkv']}, its {wl['hq'] // wl['hkv']} query heads, "
+                      f"kv_len {L}, {codec}): float64 NumPy dequantize + attention",
+            "ms_per_layer_step_scaled": round(statistics.mean(times) * wl["hkv"] * 1e3, 1)}
+
+
+def run_reference(args):
+    wl = dict(WORKLOADS[args.workload])
+    codec = args.codec or wl["codec"]
+    L = args.kv_len or wl["kv_len"] or 16384
+    cores = len(os.sched_getaffinity(0))
+    for i in range(args.warmup):
+        _oracle_step(wl, codec, min(L, 4096), 1, seed=5 + i)
+    times, nbytes = [], []
+    for i in range(args.steps):
+        dt, b = _oracle_step(wl, codec, L, 1, seed=50 + i)
+        times.append(dt)
+        nbytes.append(b)
+    ms = statistics.mean(times) * 1e3
+    value = sum(nbytes) / sum(times) / 1e9
+    sample = (f"each step: 1 KV head of {wl['hkv']} with its {wl['hq'] // wl['hkv']} query heads, "
+              f"kv_len {L}, {codec} (float64 NumPy oracle: dequantize + attention)")
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded NumPy)", "impl": "reference",
+            "config": {"workload": f"{args.workload}", "codec": codec, "kv_len": L},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default="layer8b", choices=list(WORKLOADS))
+    ap.add_argument("--codec", default=None)
+    ap.add_argument("--kv-len", type=int, default=None)
+    ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--chunk-tokens", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_mine(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,261 @@
+// Host side of the C ABI declared in include/kvq.h: argument checks, store handles, the
+// split planner and the kernel launches.  No call here waits for the device except
+// kvq_store_get_error, and none copies data to or from the host.
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <new>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t simt_launch_bf16_bf16(const DecodeArgs&, int, cudaStream_t);
+cudaError_t simt_launch_f16_f16(const DecodeArgs&, int, cudaStream_t);
+cudaError_t simt_launch_q8_0_bf16(const DecodeArgs&, int, cudaStream_t);
+cudaError_t simt_launch_q8_0_q8_0(const DecodeArgs&, int, cudaStream_t);
+cudaError_t simt_launch_q4s_q4s(const DecodeArgs&, int, cudaStream_t);
+cudaError_t simt_launch_q8_0_q4s(const DecodeArgs&, int, cudaStream_t);
+
+namespace {
+
+using SimtFn = cudaError_t (*)(const DecodeArgs&, int, cudaStream_t);
+
+SimtFn simt_fn(int kc, int vc) {
+  if (kc == KVQ_CODEC_BF16 && vc == KVQ_CODEC_BF16) return simt_launch_bf16_bf16;
+  if (kc == KVQ_CODEC_F16 && vc == KVQ_CODEC_F16) return simt_launch_f16_f16;
+  if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_BF16) return simt_launch_q8_0_bf16;
+  if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) return simt_launch_q8_0_q8_0;
+  if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) return simt_launch_q4s_q4s;
+  if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) return simt_launch_q8_0_q4s;
+  return nullptr;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kvq_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return KVQ_OK;
+  if (e == cudaErrorNotSupported) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_ERR_CUDA;
+}
+
+bool desc_ok(const kvq_store_desc* d) {
+  if (!d) return false;
+  if (d->codec < KVQ_CODEC_BF16 || d->codec > KVQ_CODEC_Q4S) return false;
+  if (d->num_kv_heads < 1 || d->num_pages < 1) return false;
+  if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return false;
+  if (d->page_size < 64 || d->page_size > 1024 || d->page_size % 64 != 0) return false;
+  return true;
+}
+
+size_t desc_bytes(const kvq_store_desc* d) {
+  const size_t slab = (size_t)d->page_size *
+                      (codec_row_bytes(d->codec, d->head_dim) + 2 * codec_scales(d->codec, d->head_dim));
+  return slab * (size_t)d->num_kv_heads * (size_t)d->num_pages;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Plan {
+  int chunk_tokens;
+  int n_chunks;
+  int variant;
+  size_t o_bytes;
+  size_t ml_off;
+  size_t total;
+};
+
+// Split planner (step a2).  Picks the chunk length so that batch * kv_heads * n_chunks
+// CTAs give about four CTAs per SM for the longest sequence, within [64, 2048] tokens,
+// and sizes the partials workspace.  A pure function of its arguments and the SM count.
+kvq_status make_plan(const kvq_store* k, int batch, int num_q_heads, int max_len_hint,
+                     const kvq_decode_opts* opts, Plan* p) {
+  const int hint = max_len_hint > 0 ? max_len_hint : 1;
+  int chunk = opts ? opts->chunk_tokens : 0;
+  if (chunk < 0 || chunk % 64 != 0) return KVQ_ERR_INVALID_ARG;
+  if (chunk == 0) {
+    const int sms = sm_count();
+    if (sms <= 0) return KVQ_ERR_CUDA;
+    const long long units = (long long)batch * k->desc.num_kv_heads;
+    const long long target = 4LL * sms;
+    const long long want = (target + units - 1) / units;
+    long long c = (hint + want - 1) / want;
+    c = (c + 63) / 64 * 64;
+    if (c < 64) c = 64;
+    if (c > 2048) c = 2048;
+    chunk = (int)c;
+  }
+  p->chunk_tokens = chunk;
+  p->n_chunks = (hint + chunk - 1) / chunk;
+  p->variant = (opts && opts->variant) ? opts->variant : 1;
+  const size_t D = (size_t)k->desc.head_dim;
+  const size_t heads = (size_t)batch * num_q_heads * p->n_chunks;
+  p->o_bytes = round_up(heads * D * sizeof(float), 256);
+  p->ml_off = p->o_bytes;
+  p->total = p->o_bytes + round_up(heads * 2 * sizeof(float), 256);
+  return KVQ_OK;
+}
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+kvq_status kvq_store_bytes(const kvq_store_desc* desc, size_t* bytes) {
+  if (!desc_ok(desc) || !bytes) return KVQ_ERR_INVALID_ARG;
+  *bytes = desc_bytes(desc);
+  return KVQ_OK;
+}
+
+kvq_status kvq_store_create(const kvq_store_desc* desc, void* buf, size_t buf_bytes,
+                            kvq_store** out) {
+  if (!out) return KVQ_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!desc_ok(desc) || !buf || !aligned(buf, 256)) return KVQ_ERR_INVALID_ARG;
+  if (buf_bytes < desc_bytes(desc)) return KVQ_ERR_INVALID_ARG;
+  kvq_store* s = new (std::nothrow) kvq_store();
+  if (!s) return KVQ_ERR_INVALID_ARG;
+  s->desc = *desc;
+  s->buf = static_cast<uint8_t*>(buf);
+  s->bytes = buf_bytes;
+  s->row_bytes = codec_row_bytes(desc->codec, desc->head_dim);
+  s->n_scales = codec_scales(desc->codec, desc->head_dim);
+  s->slab_bytes = (long long)desc->page_size * (s->row_bytes + 2 * s->n_scales);
+  if (cudaGetDevice(&s->device) != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&s->status), sizeof(int32_t)) != cudaSuccess) {
+    delete s;
+    return KVQ_ERR_CUDA;
+  }
+  if (cudaMemset(s->status, 0, sizeof(int32_t)) != cudaSuccess) {
+    cudaFree(s->status);
+    delete s;
+    return KVQ_ERR_CUDA;
+  }
+  *out = s;
+  return KVQ_OK;
+}
+
+kvq_status kvq_destroy(kvq_store* store) {
+  if (!store) return KVQ_OK;
+  const cudaError_t e = cudaFree(store->status);
+  delete store;
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_append(kvq_store* store, const void* rows, int n_new, int batch,
+                      const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                      void* stream) {
+  if (!store || !seq_lens || !page_table || batch < 1 || n_new < 0 || max_pages < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (n_new == 0) return KVQ_OK;
+  if (!rows || !aligned(rows, 2)) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(launch_append(store, static_cast<const __nv_bfloat16*>(rows), n_new, batch,
+                                 seq_lens, page_table, max_pages, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream) {
+  if (!seq_lens || batch < 1) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(launch_seq_lens_add(seq_lens, batch, n, static_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, int batch, int num_q_heads,
+                                      int max_len_hint, const kvq_decode_opts* opts,
+                                      size_t* bytes) {
+  if (!k_store || !bytes || batch < 1 || num_q_heads < 1 || max_len_hint < 0)
+    return KVQ_ERR_INVALID_ARG;
+  Plan p;
+  const kvq_status st = make_plan(k_store, batch, num_q_heads, max_len_hint, opts, &p);
+  if (st != KVQ_OK) return st;
+  *bytes = p.total;
+  return KVQ_OK;
+}
+
+kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                            const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                            kvq_codec codec, float* out, int batch, int num_q_heads,
+                            float softmax_scale, int max_len_hint,
+                            const kvq_decode_opts* opts, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!q || !k_store || !v_store || !seq_lens || !page_table || !out || !workspace)
+    return KVQ_ERR_INVALID_ARG;
+  if (batch < 1 || num_q_heads < 1 || max_pages < 1 || max_len_hint < 0)
+    return KVQ_ERR_INVALID_ARG;
+  const kvq_store_desc& kd = k_store->desc;
+  const kvq_store_desc& vd = v_store->desc;
+  if (kd.num_kv_heads != vd.num_kv_heads || kd.head_dim != vd.head_dim ||
+      kd.page_size != vd.page_size || kd.num_pages != vd.num_pages)
+    return KVQ_ERR_INVALID_ARG;
+  if (codec.k != kd.codec || codec.v != vd.codec) return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % kd.num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if ((long long)max_len_hint > (long long)max_pages * kd.page_size) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16)) return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  const int group = num_q_heads / kd.num_kv_heads;
+  Plan p;
+  kvq_status st = make_plan(k_store, batch, num_q_heads, max_len_hint, opts, &p);
+  if (st != KVQ_OK) return st;
+  if (workspace_bytes < p.total) return KVQ_ERR_WORKSPACE;
+  SimtFn fn = simt_fn(kd.codec, vd.codec);
+  if (!fn || group > 16 || p.variant != 1) return KVQ_ERR_UNSUPPORTED;
+
+  DecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = view_of(k_store);
+  a.v = view_of(v_store);
+  a.seq_lens = seq_lens;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.group = group;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt((float)kd.head_dim);
+  a.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.chunk_tokens = p.chunk_tokens;
+  a.n_chunks = p.n_chunks;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ml_off);
+  a.out = out;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = from_cuda(fn(a, kd.head_dim, s));
+  if (st != KVQ_OK) return st;
+  return from_cuda(launch_combine(a, kd.head_dim, s));
+}
+
+kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code) {
+  if (!store || !device_code) return KVQ_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaMemcpy(&v, store->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  if (cudaMemset(store->status, 0, sizeof(int32_t)) != cudaSuccess) return KVQ_ERR_CUDA;
+  *device_code = v;
+  return v ? KVQ_ERR_DEVICE_FAULT : KVQ_OK;
+}
+
+uint64_t kvq_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARG: return "KVQ_ERR_INVALID_ARG";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+    case KVQ_ERR_DEVICE_FAULT: return "KVQ_ERR_DEVICE_FAULT";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE";
+    default: return "KVQ_UNKNOWN_STATUS";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+struct kvq_store {
+  kvq_store_desc desc;
+  uint8_t* buf;        // caller-owned device memory
+  size_t bytes;
+  int32_t* status;     // device status word, owned by the handle
+  int device;
+  int row_bytes;       // bytes of one row's data
+  int n_scales;        // fp16 scales per row (0 for 16-bit codecs)
+  long long slab_bytes;  // one (page, head) slab
+};
+
+namespace kvq {
+
+constexpr int kBlock = 32;  // elements per quantization block
+
+__host__ __device__ inline int codec_row_bytes(int codec, int head_dim) {
+  return codec == KVQ_CODEC_Q8_0 ? head_dim : codec == KVQ_CODEC_Q4S ? head_dim / 2 : 2 * head_dim;
+}
+__host__ __device__ inline int codec_scales(int codec, int head_dim) {
+  return (codec == KVQ_CODEC_Q8_0 || codec == KVQ_CODEC_Q4S) ? head_dim / kBlock : 0;
+}
+
+// Records the first device fault in a status word (first writer wins, never traps).
+__device__ inline void record_fault(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Geometry of one store as the kernels see it.
+struct StoreView {
+  const uint8_t* buf;
+  int32_t* status;
+  long long slab_bytes;
+  int row_bytes;
+  int n_scales;
+  int num_pages;
+  int num_kv_heads;
+  int page_size;
+};
+
+inline StoreView view_of(const kvq_store* s) {
+  StoreView v;
+  v.buf = s->buf;
+  v.status = s->status;
+  v.slab_bytes = s->slab_bytes;
+  v.row_bytes = s->row_bytes;
+  v.n_scales = s->n_scales;
+  v.num_pages = s->desc.num_pages;
+  v.num_kv_heads = s->desc.num_kv_heads;
+  v.page_size = s->desc.page_size;
+  return v;
+}
+
+// Arguments common to the decode kernels.
+struct DecodeArgs {
+  const __nv_bfloat16* q;      // [B][Hq][D]
+  StoreView k, v;
+  const int32_t* seq_lens;     // [B]
+  const int32_t* page_table;   // [B][max_pages]
+  int max_pages;
+  int batch;
+  int num_q_heads;
+  int group;                   // Hq / Hkv
+  float qk_scale_log2;         // softmax scale * log2(e)
+  int chunk_tokens;            // split-K chunk length
+  int n_chunks;                // chunks per (sequence, kv head)
+  float* part_o;               // [B][Hq][n_chunks][D]
+  float* part_ml;              // [B][Hq][n_chunks][2]  (running max in log2 units, sum)
+  float* out;                  // [B][Hq][D]
+};
+
+// Launchers implemented in the kernel translation units.  Each returns a CUDA error.
+cudaError_t launch_append(const kvq_store* store, const __nv_bfloat16* rows, int n_new, int batch,
+                          const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                          cudaStream_t stream);
+cudaError_t launch_seq_lens_add(int32_t* seq_lens, int batch, int n, cudaStream_t stream);
+// Returns cudaErrorNotSupported when no kernel is built for the combination.
+cudaError_t launch_decode_simt(const DecodeArgs& a, int k_codec, int v_codec, int head_dim,
+                               cudaStream_t stream);
+cudaError_t launch_combine(const DecodeArgs& a, int head_dim, cudaStream_t stream);
+bool decode_simt_supported(int k_codec, int v_codec, int head_dim, int group);
+
+void count_launch();
+
+}  // namespace kvq

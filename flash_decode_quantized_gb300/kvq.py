@@ -1,0 +1,228 @@
+"""Python binding of the kvq C ABI (include/kvq.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does nothing but
+check Python-side types, pass device pointers / sizes / the current CUDA stream through
+ctypes, and raise ``KvqError`` on a non-OK status.  All computation runs in the CUDA
+kernels of libkvq.so; there is no fallback: importing this module without the built
+library raises.  PyTorch is used only to allocate device memory and to name streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
+
+KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_DEVICE_FAULT, \
+    KVQ_ERR_WORKSPACE = range(6)
+CODECS = {"bf16": 0, "f16": 1, "q8_0": 2, "q4s": 3}
+DEVICE_FAULTS = {0: "ok", 1: "bad_page", 2: "bad_position", 3: "bad_seq_len"}
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call} -> {_status_string(status)}")
+
+
+class StoreDesc(ctypes.Structure):
+    _fields_ = [("codec", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32)]
+
+
+class CodecPair(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_int32), ("v", ctypes.c_int32)]
+
+
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("chunk_tokens", ctypes.c_int32), ("variant", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libkvq.so is not built ({_LIB_PATH}); run "
+                          "`python -m flash_decode_quantized_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I, Z, V = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    sig = {
+        "kvq_store_bytes": [ctypes.POINTER(StoreDesc), ctypes.POINTER(Z)],
+        "kvq_store_create": [ctypes.POINTER(StoreDesc), P, Z, ctypes.POINTER(P)],
+        "kvq_destroy": [P],
+        "kvq_append": [P, P, I, I, P, P, I, V],
+        "kvq_seq_lens_add": [P, I, I, V],
+        "kvq_decode_workspace_bytes": [P, I, I, I, ctypes.POINTER(DecodeOpts), ctypes.POINTER(Z)],
+        "kvq_flash_decode": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
+                             ctypes.POINTER(DecodeOpts), P, Z, V],
+        "kvq_store_get_error": [P, ctypes.POINTER(ctypes.c_int32)],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.kvq_launch_count.argtypes = []
+    lib.kvq_launch_count.restype = ctypes.c_uint64
+    lib.kvq_status_string.argtypes = [ctypes.c_int]
+    lib.kvq_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def _status_string(status: int) -> str:
+    return lib.kvq_status_string(status).decode()
+
+
+def _check(status: int, call: str) -> None:
+    if status != KVQ_OK:
+        raise KvqError(status, call)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _opts(chunk_tokens: int, variant: int):
+    return ctypes.byref(DecodeOpts(int(chunk_tokens), int(variant)))
+
+
+class Store:
+    """A store handle plus the device buffer it wraps (owned by this object)."""
+
+    def __init__(self, handle, buf, desc):
+        self._h = handle
+        self.buf = buf
+        self.codec = {v: k for k, v in CODECS.items()}[desc.codec]
+        self.num_kv_heads = desc.num_kv_heads
+        self.head_dim = desc.head_dim
+        self.page_size = desc.page_size
+        self.num_pages = desc.num_pages
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("store was destroyed")
+        return self._h
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None:
+            lib.kvq_destroy(self._h)
+            self._h = None
+
+
+def _desc(codec, num_kv_heads, head_dim, page_size, num_pages) -> StoreDesc:
+    return StoreDesc(CODECS[codec] if isinstance(codec, str) else int(codec), num_kv_heads,
+                     head_dim, page_size, num_pages)
+
+
+def kvq_store_bytes(codec, num_kv_heads: int, head_dim: int, page_size: int, num_pages: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.kvq_store_bytes(ctypes.byref(_desc(codec, num_kv_heads, head_dim, page_size,
+                                                  num_pages)), ctypes.byref(n)), "kvq_store_bytes")
+    return n.value
+
+
+def kvq_store_create(codec, num_kv_heads: int, head_dim: int, page_size: int, num_pages: int,
+                     buf: torch.Tensor | None = None, device=None) -> Store:
+    desc = _desc(codec, num_kv_heads, head_dim, page_size, num_pages)
+    nbytes = kvq_store_bytes(codec, num_kv_heads, head_dim, page_size, num_pages)
+    if buf is None:
+        buf = torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+    h = ctypes.c_void_p()
+    _check(lib.kvq_store_create(ctypes.byref(desc), _ptr(buf, torch.uint8, "buf"), buf.numel(),
+                                ctypes.byref(h)), "kvq_store_create")
+    return Store(h, buf, desc)
+
+
+def kvq_destroy(store: Store) -> None:
+    if store._h is not None:
+        _check(lib.kvq_destroy(store._h), "kvq_destroy")
+        store._h = None
+
+
+def kvq_append(store: Store, rows: torch.Tensor, seq_lens: torch.Tensor, page_table: torch.Tensor,
+               stream=None) -> None:
+    """rows: bf16 [B, n_new, Hkv, D]; writes row i of sequence b at seq_lens[b] + i."""
+    if rows.dim() != 4 or rows.shape[2] != store.num_kv_heads or rows.shape[3] != store.head_dim:
+        raise ValueError("rows must be [batch, n_new, num_kv_heads, head_dim]")
+    bsz, n_new = rows.shape[0], rows.shape[1]
+    if seq_lens.numel() != bsz or page_table.dim() != 2 or page_table.shape[0] != bsz:
+        raise ValueError("seq_lens / page_table do not match the batch")
+    _check(lib.kvq_append(store.handle, _ptr(rows, torch.bfloat16, "rows"), n_new, bsz,
+                          _ptr(seq_lens, torch.int32, "seq_lens"),
+                          _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                          _stream(stream)), "kvq_append")
+
+
+def kvq_seq_lens_add(seq_lens: torch.Tensor, n: int, stream=None) -> None:
+    _check(lib.kvq_seq_lens_add(_ptr(seq_lens, torch.int32, "seq_lens"), seq_lens.numel(), int(n),
+                                _stream(stream)), "kvq_seq_lens_add")
+
+
+def kvq_decode_workspace_bytes(k_store: Store, batch: int, num_q_heads: int, max_len_hint: int,
+                               chunk_tokens: int = 0, variant: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.kvq_decode_workspace_bytes(k_store.handle, batch, num_q_heads, int(max_len_hint),
+                                          _opts(chunk_tokens, variant), ctypes.byref(n)),
+           "kvq_decode_workspace_bytes")
+    return n.value
+
+
+def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: torch.Tensor,
+                     page_table: torch.Tensor, out: torch.Tensor | None = None,
+                     softmax_scale: float = 0.0, max_len_hint: int | None = None,
+                     workspace: torch.Tensor | None = None, chunk_tokens: int = 0,
+                     variant: int = 0, stream=None) -> torch.Tensor:
+    """q: bf16 [B, Hq, D] -> out fp32 [B, Hq, D].  max_len_hint defaults to the page
+    table's capacity (max_pages * page_size)."""
+    bsz, hq, dim = q.shape
+    max_pages = page_table.shape[1]
+    if max_len_hint is None:
+        max_len_hint = max_pages * k_store.page_size
+    if out is None:
+        out = torch.empty((bsz, hq, dim), dtype=torch.float32, device=q.device)
+    need = kvq_decode_workspace_bytes(k_store, bsz, hq, max_len_hint, chunk_tokens, variant)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
+    _check(lib.kvq_flash_decode(_ptr(q, torch.bfloat16, "q"), k_store.handle, v_store.handle,
+                                _ptr(seq_lens, torch.int32, "seq_lens"),
+                                _ptr(page_table, torch.int32, "page_table"), max_pages, codec,
+                                _ptr(out, torch.float32, "out"), bsz, hq, float(softmax_scale),
+                                int(max_len_hint), _opts(chunk_tokens, variant),
+                                _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                _stream(stream)), "kvq_flash_decode")
+    return out
+
+
+def kvq_store_get_error(store: Store) -> int:
+    """Synchronizes; returns (and clears) the first device fault code recorded, or 0."""
+    code = ctypes.c_int32()
+    st = lib.kvq_store_get_error(store.handle, ctypes.byref(code))
+    if st not in (KVQ_OK, KVQ_ERR_DEVICE_FAULT):
+        raise KvqError(st, "kvq_store_get_error")
+    return code.value
+
+
+def kvq_launch_count() -> int:
+    return int(lib.kvq_launch_count())
+
+
+def kvq_status_string(status: int) -> str:
+    return _status_string(status)

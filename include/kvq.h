@@ -1,0 +1,174 @@
+/*
+ * kvq.h -- C ABI of a fused dequant-on-load flash-decode library for a resident,
+ * paged, block-quantized KV cache (NVIDIA GB300, sm_103a).
+ *
+ * What it computes.  Single-token decode attention (split-K flash-decode) that reads
+ * the quantized KV store directly and dequantizes inside the kernel, the
+ * "flash-decode-over-quant" class that rMLX issue #292 ("Root cause", correction)
+ * names as the target, with the "dequantize KV on load" treatment of halobench record
+ * clm-0022 (METHOD) and a 16-bit KV arm kept as the control ("THE CONTROL IS THE
+ * POINT").  The prefix stays resident on the device and new rows are encoded there,
+ * so no step restages the prefix through the host (rMLX issue #295, "Root cause" and
+ * "Fix direction").
+ *
+ * Conventions for every call below.
+ *  - All pointers named "device" are CUDA device pointers on the current device; all
+ *    others are host pointers.  The library never frees memory it did not allocate.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Every call that takes a stream only enqueues work on it and returns; none waits
+ *    for the device, except kvq_store_get_error.
+ *  - Shapes, codecs, alignment and null pointers are checked on the host before any
+ *    work is enqueued; a failed check returns KVQ_ERR_INVALID_ARG or
+ *    KVQ_ERR_UNSUPPORTED and enqueues nothing.
+ *  - Bad values found in device data (a page id outside [0, num_pages), a position past
+ *    the page table, a negative or too-long sequence length) never trap: the kernel
+ *    skips the affected row or tile and records the first such fault in the store's
+ *    device status word, read back by kvq_store_get_error.
+ *  - A CUDA launch failure returns KVQ_ERR_CUDA.
+ *
+ * Store layout (one store holds either K or V of every layer-head it was sized for):
+ *   num_pages pages x num_kv_heads slabs; slab (page, head) =
+ *     [page_size rows x row_bytes]            row data, token-major
+ *     [page_size rows x (head_dim/32) x fp16]  block scales (q8_0 and q4s only)
+ *   row_bytes = 2*head_dim (bf16, f16), head_dim (q8_0), head_dim/2 (q4s).
+ *   Token position pos of sequence b lives in physical page
+ *   page_table[b*max_pages + pos/page_size], row pos % page_size.
+ *
+ * Codecs (blocks of 32 consecutive elements along head_dim; inputs are bf16):
+ *   amax = max|x|; d = fp16_rn(amax / c) (fp32 quotient); q = 0 if d == 0, else
+ *   clamp(round_half_away(x / d) (fp32 quotient), -c, c); c = 127 (q8_0) or 7 (q4s).
+ *   q8_0 stores int8 q; q4s stores u = q + 8 as nibbles, element 2k in the low nibble
+ *   of block byte k.  bf16 stores the input bits; f16 stores fp16_rn(x).
+ *   Dequantized value: d * q.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,   /* bad pointer, shape, size or alignment */
+  KVQ_ERR_UNSUPPORTED = 2,   /* valid but not built: codec pair, head_dim, group size */
+  KVQ_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+  KVQ_ERR_DEVICE_FAULT = 4,  /* kvq_store_get_error: a kernel recorded a data fault */
+  KVQ_ERR_WORKSPACE = 5      /* the workspace passed is smaller than required */
+} kvq_status;
+
+typedef enum kvq_codec_id {
+  KVQ_CODEC_BF16 = 0,        /* 16-bit control arm, bf16 values as given */
+  KVQ_CODEC_F16 = 1,         /* 16-bit control arm, fp16_rn of the bf16 input */
+  KVQ_CODEC_Q8_0 = 2,        /* 8-bit symmetric blocks of 32, fp16 scale */
+  KVQ_CODEC_Q4S = 3          /* 4-bit symmetric blocks of 32, fp16 scale, q in [-7, 7] */
+} kvq_codec_id;
+
+/* Device fault codes recorded in a store's status word (first fault wins). */
+enum {
+  KVQ_DEVICE_OK = 0,
+  KVQ_DEVICE_BAD_PAGE = 1,      /* page id outside [0, num_pages) */
+  KVQ_DEVICE_BAD_POSITION = 2,  /* append position outside [0, max_pages*page_size) */
+  KVQ_DEVICE_BAD_SEQ_LEN = 3    /* sequence length < 0, past the page table, or past
+                                   the max_len_hint that sized the decode split */
+};
+
+/* Shape of one store.  head_dim in {64, 128, 256}; page_size a multiple of 64 in
+ * [64, 1024]; num_kv_heads >= 1; num_pages >= 1. */
+typedef struct kvq_store_desc {
+  int32_t codec;             /* kvq_codec_id */
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;         /* tokens per page */
+  int32_t num_pages;
+} kvq_store_desc;
+
+/* Codec pair a decode call expects; must equal the codecs of the stores passed. */
+typedef struct kvq_codec {
+  int32_t k;                 /* kvq_codec_id of the K store */
+  int32_t v;                 /* kvq_codec_id of the V store */
+} kvq_codec;
+
+/* Optional decode settings (pass NULL for the defaults). */
+typedef struct kvq_decode_opts {
+  int32_t chunk_tokens;      /* split-K chunk length in tokens; 0 = planner's choice.
+                                Must be a positive multiple of 64 otherwise. */
+  int32_t variant;           /* 0 = auto, 1 = CUDA-core kernel, 2 = tensor-core kernel */
+} kvq_decode_opts;
+
+typedef struct kvq_store kvq_store;  /* opaque handle: host metadata + a device status word */
+
+/* Bytes of device memory a store with this shape needs (num_pages * num_kv_heads *
+ * page_size * (row_bytes + 2*head_dim/32 for quantized codecs)).  Pure host call. */
+kvq_status kvq_store_bytes(const kvq_store_desc* desc, size_t* bytes);
+
+/* Wrap caller-owned device memory `buf` (at least kvq_store_bytes bytes, 256-byte
+ * aligned) as a store.  The buffer's previous contents are kept; rows that were never
+ * appended hold whatever the buffer held.  Allocates the handle on the host and a
+ * 4-byte status word on the current device.  `*out` is valid until kvq_destroy. */
+kvq_status kvq_store_create(const kvq_store_desc* desc, void* buf, size_t buf_bytes,
+                            kvq_store** out);
+
+/* Free the handle and its status word.  Does not touch `buf`.  The caller must make
+ * sure no enqueued work still uses the store.  NULL is accepted. */
+kvq_status kvq_destroy(kvq_store* store);
+
+/* Encode new rows into the store, on the device (a1: on-device encode of new K/V rows;
+ * rMLX issue #295 "Fix direction").
+ *   rows       device bf16 [batch][n_new][num_kv_heads][head_dim], contiguous.
+ *   seq_lens   device int32 [batch]: row i of sequence b is written at position
+ *              seq_lens[b] + i.  Not modified (see kvq_seq_lens_add).
+ *   page_table device int32 [batch][max_pages].
+ * Rows whose position or page is invalid are skipped and recorded as device faults. */
+kvq_status kvq_append(kvq_store* store, const void* rows, int n_new, int batch,
+                      const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                      void* stream);
+
+/* seq_lens[b] += n for b < batch, on the device (after the K and the V append). */
+kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
+
+/* Device workspace bytes a kvq_flash_decode call with the same arguments needs. */
+kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, int batch, int num_q_heads,
+                                      int max_len_hint, const kvq_decode_opts* opts,
+                                      size_t* bytes);
+
+/* Split-K flash-decode over the quantized store (a2..a8):
+ *   q          device bf16 [batch][num_q_heads][head_dim]
+ *   k_store, v_store: same num_kv_heads, head_dim, page_size; codecs == `codec`.
+ *   seq_lens   device int32 [batch], each in [0, max_len_hint]
+ *   page_table device int32 [batch][max_pages]
+ *   out        device fp32 [batch][num_q_heads][head_dim]
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   softmax_scale <= 0 selects 1/sqrt(head_dim).
+ *   max_len_hint: host-side upper bound of seq_lens, used to size the split without a
+ *   device round trip; a longer sequence is truncated and recorded as a device fault.
+ *   workspace: device memory of at least kvq_decode_workspace_bytes bytes, 256-byte
+ *   aligned; its contents need no initialisation.
+ * A sequence of length 0 yields zeros. */
+kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                            const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                            kvq_codec codec, float* out, int batch, int num_q_heads,
+                            float softmax_scale, int max_len_hint,
+                            const kvq_decode_opts* opts, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Wait for the device, read and clear the store's status word.  *device_code receives
+ * the first recorded fault (KVQ_DEVICE_*), or 0.  Returns KVQ_ERR_DEVICE_FAULT when a
+ * fault was recorded, KVQ_OK otherwise.  The only call that synchronizes. */
+kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code);
+
+/* Number of decode/append/combine kernels this library has launched in this process
+ * (a dispatch counter for benchmarks and tests). */
+uint64_t kvq_launch_count(void);
+
+/* Static string naming a status code. */
+const char* kvq_status_string(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

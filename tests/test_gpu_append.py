@@ -1,0 +1,97 @@
+"""On-device encode (kvq_append) must match the oracle encode bit for bit."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from kvq_testutil import bf16_tensor, build_store, expected_rows, kvq, store_rows
+from workloads import f32_to_bf16_bits, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+CODECS = ["bf16", "f16", "q8_0", "q4s"]
+
+
+@pytest.mark.parametrize("codec", CODECS)
+@pytest.mark.parametrize("head_dim", [64, 128, 256])
+@pytest.mark.parametrize("dist,scaled", [("normal", False), ("t3", True)])
+def test_append_bit_exact(codec, head_dim, dist, scaled):
+    inp = make_inputs([300, 77], 4, 2, head_dim, seed=head_dim + 7, dist=dist,
+                      channel_scaled=scaled, page_size=64)
+    for which in ("k", "v"):
+        st = build_store(inp, codec, which, chunk_rows=129)
+        for b in range(inp.batch):
+            pos = np.arange(inp.seq_lens[b])
+            gp, gs = store_rows(st, inp, b, pos)
+            ep, es = expected_rows(inp, which, codec, b, pos)
+            assert np.array_equal(gp, ep), f"{codec} {which} b={b}: row bytes differ"
+            assert np.array_equal(gs, es), f"{codec} {which} b={b}: scales differ"
+
+
+@pytest.mark.parametrize("codec", ["q8_0", "q4s"])
+def test_append_golden_blocks(codec):
+    """The hand-derived blocks (ties, subnormal scales, zero blocks) encoded on the GPU."""
+    cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "codec_blocks.json")))
+    rows = []
+    for c in cases["cases"]:
+        if c["codec"] != codec:
+            continue
+        x = np.zeros(128, np.float32)
+        for k, v in c["x"].items():
+            x[int(k)] = float.fromhex(v)
+            x[64 + int(k)] = -float.fromhex(v)   # the mirrored block in the same row
+        rows.append((c, f32_to_bf16_bits(x)))
+    k = kvq()
+    st = k.kvq_store_create(codec, 1, 128, 64, 1)
+    pt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    data = np.stack([r for _, r in rows])[None, :, None, :]
+    k.kvq_append(st, bf16_tensor(data), torch.zeros(1, dtype=torch.int32, device="cuda"), pt)
+    buf = st.buf.cpu().numpy()
+    rb = 128 if codec == "q8_0" else 64
+    for i, (c, _) in enumerate(rows):
+        scales = buf[64 * rb + i * 8: 64 * rb + i * 8 + 8].view(np.uint16)
+        assert int(scales[0]) == int(c["d_bits"], 16), c["name"]
+        assert int(scales[2]) == int(c["d_bits"], 16), c["name"]
+        want = np.zeros(32, np.int64)
+        for kk, v in c["q"].items():
+            want[int(kk)] = v
+        row = buf[i * rb:(i + 1) * rb]
+        if codec == "q8_0":
+            q = row.view(np.int8).astype(np.int64)
+        else:
+            q = np.empty(128, np.int64)
+            q[0::2] = (row & 15).astype(np.int64) - 8
+            q[1::2] = (row >> 4).astype(np.int64) - 8
+        assert np.array_equal(q[:32], want), c["name"]
+        assert np.array_equal(q[64:96], -want), c["name"]
+
+
+def test_row_by_row_equals_bulk():
+    inp = make_inputs([200], 8, 2, 128, seed=3, page_size=64)
+    bulk = build_store(inp, "q8_0", "k")
+    k = kvq()
+    inc = k.kvq_store_create("q8_0", 2, 128, 64, inp.num_pages)
+    seq = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pt = torch.from_numpy(inp.page_table).cuda()
+    rows = bf16_tensor(inp.k_rows[0][None])
+    for i in range(200):
+        k.kvq_append(inc, rows[:, i:i + 1].contiguous(), seq, pt)
+        k.kvq_seq_lens_add(seq, 1)
+    assert int(seq.item()) == 200
+    assert torch.equal(bulk.buf, inc.buf)
+
+
+def test_batched_append_two_sequences():
+    inp = make_inputs([96, 96], 4, 2, 128, seed=5, page_size=64)
+    k = kvq()
+    st = k.kvq_store_create("q4s", 2, 128, 64, inp.num_pages)
+    rows = bf16_tensor(np.stack(inp.k_rows))
+    seq = torch.zeros(2, dtype=torch.int32, device="cuda")
+    k.kvq_append(st, rows, seq, torch.from_numpy(inp.page_table).cuda())
+    for b in range(2):
+        gp, gs = store_rows(st, inp, b, np.arange(96))
+        ep, es = expected_rows(inp, "k", "q4s", b, np.arange(96))
+        assert np.array_equal(gp, ep) and np.array_equal(gs, es)

@@ -1,0 +1,144 @@
+"""Fused flash-decode parity against the oracle run on the same dequantized values."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from kvq_testutil import (assert_close, build_store, device_inputs, kvq, oracle_out,
+                          oracle_values)
+from workloads import make_inputs, ragged_lengths
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [("bf16", "bf16"), ("f16", "f16"), ("q8_0", "bf16"), ("q8_0", "q8_0"),
+         ("q4s", "q4s"), ("q8_0", "q4s")]
+VARIANTS = [1]
+
+
+def run_decode(inp, kc, vc, **kw):
+    k = kvq()
+    ks = build_store(inp, kc, "k")
+    vs = build_store(inp, vc, "v")
+    q, sl, pt = device_inputs(inp)
+    out = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=int(inp.seq_lens.max()), **kw)
+    torch.cuda.synchronize()
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+    return out.cpu().numpy(), (ks, vs, q, sl, pt)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("bf16", "bf16")])
+def test_tiny_workload(kc, vc, variant):
+    # B=1, 4 query heads on 1 KV head, D=128, L=256, N(0,1) bf16
+    inp = make_inputs([256], 4, 1, 128, seed=0)
+    got, _ = run_decode(inp, kc, vc, variant=variant)
+    assert_close(got, oracle_out(inp, kc, vc), f"tiny {kc}/{vc}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("kc,vc", PAIRS)
+def test_layer8b_reduced(kc, vc, variant):
+    # 32/8 heads, D=128, a length spanning several chunks plus a ragged tail
+    inp = make_inputs([3001], 32, 8, 128, seed=11)
+    got, _ = run_decode(inp, kc, vc, variant=variant, chunk_tokens=512)
+    assert_close(got, oracle_out(inp, kc, vc), f"layer8b {kc}/{vc}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("kc,vc", [("f16", "f16"), ("bf16", "bf16"), ("q8_0", "q8_0"),
+                                   ("q4s", "q4s")])
+def test_longctx_reduced(kc, vc, variant):
+    # 32/2 heads (GQA 16:1), D=256, per-channel scales log-uniform in [0.25, 4]
+    inp = make_inputs([2500], 32, 2, 256, seed=12, channel_scaled=True)
+    got, _ = run_decode(inp, kc, vc, variant=variant, chunk_tokens=1024)
+    assert_close(got, oracle_out(inp, kc, vc), f"longctx {kc}/{vc}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q4s", "q4s")])
+def test_ragged_paged_batch(kc, vc, variant):
+    lens = [1, 63, 64, 65, 700, 2049, 256, 0]
+    inp = make_inputs(lens, 32, 8, 128, seed=13)
+    got, _ = run_decode(inp, kc, vc, variant=variant)
+    want = oracle_out(inp, kc, vc)
+    assert_close(got, want, f"ragged {kc}/{vc}")
+    assert np.all(got[7] == 0.0)  # the empty sequence yields zeros
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q8_0", "q4s")])
+def test_heavy_tailed_values(kc, vc, variant):
+    inp = make_inputs([1500], 32, 8, 128, seed=14, dist="t3", channel_scaled=True)
+    got, _ = run_decode(inp, kc, vc, variant=variant)
+    assert_close(got, oracle_out(inp, kc, vc), f"t3 {kc}/{vc}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("group,head_dim", [(1, 128), (2, 64), (8, 128), (16, 128), (4, 256)])
+def test_group_and_head_dim_sweep(group, head_dim, variant):
+    inp = make_inputs([777, 129], 2 * group, 2, head_dim, seed=15)
+    got, _ = run_decode(inp, "q8_0", "q8_0", variant=variant)
+    assert_close(got, oracle_out(inp, "q8_0", "q8_0"), f"G={group} D={head_dim}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_split_invariance(variant):
+    inp = make_inputs([4100], 16, 4, 128, seed=16)
+    want = oracle_out(inp, "q8_0", "q8_0")
+    outs = []
+    for chunk in (64, 128, 512, 2048, 4160):
+        got, _ = run_decode(inp, "q8_0", "q8_0", variant=variant, chunk_tokens=chunk)
+        assert_close(got, want, f"chunk={chunk}")
+        outs.append(got)
+    for o in outs[1:]:
+        assert np.max(np.abs(o - outs[0])) < 1e-3
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_page_permutation_invariance(variant):
+    a = make_inputs([1800, 900], 8, 2, 128, seed=17, permute_pages=True)
+    b = make_inputs([1800, 900], 8, 2, 128, seed=17, permute_pages=False)
+    assert not np.array_equal(a.page_table, b.page_table)
+    ga, _ = run_decode(a, "q4s", "q4s", variant=variant, chunk_tokens=256)
+    gb, _ = run_decode(b, "q4s", "q4s", variant=variant, chunk_tokens=256)
+    assert np.array_equal(ga, gb)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_closed_forms_on_device(variant):
+    # identical keys -> mean of the dequantized V; a single token -> that V row
+    inp = make_inputs([500, 1], 4, 1, 128, seed=18)
+    inp.k_rows[0][:] = inp.k_rows[0][0:1]
+    got, _ = run_decode(inp, "q8_0", "q8_0", variant=variant)
+    _, vs = oracle_values(inp, "q8_0", "q8_0")
+    for h in range(4):
+        assert np.max(np.abs(got[0, h] - vs[0][:, 0].mean(axis=0))) < 2e-3
+        assert np.max(np.abs(got[1, h] - vs[1][0, 0])) < 2e-3
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_explicit_softmax_scale(variant):
+    inp = make_inputs([640], 8, 2, 128, seed=19)
+    got, _ = run_decode(inp, "q8_0", "bf16", variant=variant, softmax_scale=0.3)
+    assert_close(got, oracle_out(inp, "q8_0", "bf16", scale=0.3), "scale=0.3")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_stale_rows_past_length_are_ignored(variant):
+    # rows past seq_len hold NaN bit patterns: they must not reach the output
+    inp = make_inputs([300], 8, 2, 128, seed=20)
+    k = kvq()
+    ks = build_store(inp, "bf16", "k")
+    vs = build_store(inp, "bf16", "v")
+    P = inp.page_size
+    for st in (ks, vs):
+        raw = st.buf.view(torch.int16).view(inp.num_pages, 2, P, 128)
+        last = int(inp.page_table[0, 300 // P])
+        raw[last, :, 300 % P:, :] = 0x7FC0  # bf16 quiet NaN
+    q, sl, pt = device_inputs(inp)
+    out = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=300, variant=variant)
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert_close(got, oracle_out(inp, "bf16", "bf16"), "stale NaN rows")
