@@ -212,8 +212,8 @@ class Layer:
         self.ws = None
 
     def prepare(self, variant, chunk_tokens=0):
-        n = self.kvq.kvq_decode_workspace_bytes(self.k_store, self.batch, self.hq, self.hint,
-                                                chunk_tokens, variant)
+        n = self.kvq.kvq_decode_workspace_bytes(self.k_store, self.v_store, self.batch, self.hq,
+                                                self.hint, chunk_tokens, variant)
         self.ws = self.torch.empty(n, dtype=self.torch.uint8, device="cuda")
         self.variant, self.chunk = variant, chunk_tokens
 
@@ -241,10 +241,18 @@ def l2_flusher(torch):
     return lambda: buf.fill_(1.0)
 
 
+def gpu_lead(torch):
+    """Keeps the GPU busy ~100 µs (a bounded cycle-count wait) so that the host has
+    enqueued the whole step before the GPU reaches the step's first event; otherwise the
+    events would time host launch latency."""
+    torch.cuda._sleep(200_000)
+
+
 def time_decode_only(torch, layer, flush, iters):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
     for i in range(iters):
         flush()
+        gpu_lead(torch)
         ev[i][0].record()
         layer.decode()
         ev[i][1].record()
@@ -287,6 +295,7 @@ def run_mine(args, rank, world):
         t0 = time.perf_counter()
         for i in range(K):
             flush()
+            gpu_lead(torch)
             ev[i][0].record()
             layer.append()
             ev[i][1].record()
@@ -335,7 +344,7 @@ def run_mine(args, rank, world):
         "config": {"workload": f"{args.workload}: B={wl['batch']}, Hq={wl['hq']}, Hkv={wl['hkv']}, "
                                f"D={wl['d']}, kv_len={seq_lens[0] if len(set(seq_lens)) == 1 else 'U[1024,32768]'}",
                    "codec": codec, "kv_bytes_per_step": int(kvb), "variant": args.variant,
-                   "chunk_tokens": args.chunk_tokens, "l2": "flushed (2xL2 write) before every timed step, outside its events",
+                   "chunk_tokens": args.chunk_tokens, "l2": "flushed (2xL2 write) before every timed step, outside its events; ~100 us GPU lead so events exclude host launch latency",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "e2e": e2e,

@@ -1,9 +1,12 @@
 // Host side of the C ABI declared in include/kvq.h: argument checks, store handles, the
 // split planner and the kernel launches.  No call here waits for the device except
 // kvq_store_get_error, and none copies data to or from the host.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
+#include <mutex>
 #include <new>
 
 #include "kvq_internal.cuh"
@@ -19,6 +22,19 @@ cudaError_t simt_launch_q8_0_bf16(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_q8_0_q8_0(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_q4s_q4s(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_q8_0_q4s(const DecodeArgs&, int, cudaStream_t);
+using MmaFn = cudaError_t (*)(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_bf16_bf16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_f16_f16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_q8_0_bf16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_q8_0_q8_0(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_q4s_q4s(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_q8_0_q4s(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+int mma_occupancy_bf16_bf16(int, int);
+int mma_occupancy_f16_f16(int, int);
+int mma_occupancy_q8_0_bf16(int, int);
+int mma_occupancy_q8_0_q8_0(int, int);
+int mma_occupancy_q4s_q4s(int, int);
+int mma_occupancy_q8_0_q4s(int, int);
 
 namespace {
 
@@ -32,6 +48,74 @@ SimtFn simt_fn(int kc, int vc) {
   if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) return simt_launch_q4s_q4s;
   if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) return simt_launch_q8_0_q4s;
   return nullptr;
+}
+
+MmaFn mma_fn(int kc, int vc) {
+  if (kc == KVQ_CODEC_BF16 && vc == KVQ_CODEC_BF16) return mma_launch_bf16_bf16;
+  if (kc == KVQ_CODEC_F16 && vc == KVQ_CODEC_F16) return mma_launch_f16_f16;
+  if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_BF16) return mma_launch_q8_0_bf16;
+  if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) return mma_launch_q8_0_q8_0;
+  if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) return mma_launch_q4s_q4s;
+  if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) return mma_launch_q8_0_q4s;
+  return nullptr;
+}
+
+// Resident CTAs per SM of the tensor-core kernel for this shape (cached per process).
+int mma_occupancy(int kc, int vc, int head_dim, int group) {
+  static std::mutex mu;
+  static int cache[4][4][3][3] = {};
+  const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
+  const int gi = group <= 4 ? 0 : group <= 8 ? 1 : 2;
+  std::lock_guard<std::mutex> lock(mu);
+  int& slot = cache[kc & 3][vc & 3][di][gi];
+  if (slot == 0) {
+    int n = 0;
+    if (kc == KVQ_CODEC_BF16 && vc == KVQ_CODEC_BF16) n = mma_occupancy_bf16_bf16(head_dim, group);
+    else if (kc == KVQ_CODEC_F16 && vc == KVQ_CODEC_F16) n = mma_occupancy_f16_f16(head_dim, group);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_BF16) n = mma_occupancy_q8_0_bf16(head_dim, group);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q8_0_q8_0(head_dim, group);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q4s_q4s(head_dim, group);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q8_0_q4s(head_dim, group);
+    slot = n > 0 ? n : 1;
+  }
+  return slot;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// TMA map over a store's row data: a 4-D byte tensor {row_bytes, page_size, kv_heads,
+// pages} with the slab strides; boxes of 64 rows x min(row_bytes, 128) bytes, swizzled
+// over the box width so that ldmatrix reads of 8 consecutive rows hit distinct banks.
+bool encode_rows_map(kvq_store* s) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int rb = s->row_bytes;
+  const int line = rb >= 128 ? 128 : rb;
+  cuuint64_t dims[4] = {(cuuint64_t)rb, (cuuint64_t)s->desc.page_size, (cuuint64_t)s->desc.num_kv_heads,
+                        (cuuint64_t)s->desc.num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)rb, (cuuint64_t)s->slab_bytes,
+                           (cuuint64_t)s->slab_bytes * (cuuint64_t)s->desc.num_kv_heads};
+  cuuint32_t box[4] = {(cuuint32_t)line, 64u, 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapSwizzle sw = line == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : line == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUresult r = enc(&s->rows_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, s->buf, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -75,29 +159,38 @@ struct Plan {
   size_t total;
 };
 
-// Split planner (step a2).  Picks the chunk length so that batch * kv_heads * n_chunks
-// CTAs give about four CTAs per SM for the longest sequence, within [64, 2048] tokens,
-// and sizes the partials workspace.  A pure function of its arguments and the SM count.
-kvq_status make_plan(const kvq_store* k, int batch, int num_q_heads, int max_len_hint,
-                     const kvq_decode_opts* opts, Plan* p) {
+// Split planner (step a2).  A pure function of its arguments and the device (SM count,
+// resident CTAs per SM of the chosen kernel).  With the default chunk length it fills
+// whole waves: batch * kv_heads * n_chunks CTAs for the longest sequence come to about
+// one wave of resident CTAs (or more whole waves when one wave would need chunks longer
+// than 4096 tokens), with chunks of at least 128 tokens.  It sizes the partials workspace.
+kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_q_heads,
+                     int max_len_hint, const kvq_decode_opts* opts, Plan* p) {
   const int hint = max_len_hint > 0 ? max_len_hint : 1;
   int chunk = opts ? opts->chunk_tokens : 0;
   if (chunk < 0 || chunk % 64 != 0) return KVQ_ERR_INVALID_ARG;
+  p->variant = (opts && opts->variant) ? opts->variant : 2;
   if (chunk == 0) {
     const int sms = sm_count();
     if (sms <= 0) return KVQ_ERR_CUDA;
+    const int group = num_q_heads / k->desc.num_kv_heads;
+    const int per_sm = p->variant == 2 ? mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec,
+                                                       k->desc.head_dim, group)
+                                       : 2;
     const long long units = (long long)batch * k->desc.num_kv_heads;
-    const long long target = 4LL * sms;
-    const long long want = (target + units - 1) / units;
-    long long c = (hint + want - 1) / want;
+    const long long slots = (long long)sms * per_sm;
+    long long waves = 1, c = 0;
+    for (;; ++waves) {
+      const long long want = (slots * waves + units - 1) / units;   // chunks per unit
+      c = (hint + want - 1) / want;
+      if (c <= 4096 || waves >= 64) break;
+    }
     c = (c + 63) / 64 * 64;
-    if (c < 64) c = 64;
-    if (c > 2048) c = 2048;
+    if (c < 128) c = 128;
     chunk = (int)c;
   }
   p->chunk_tokens = chunk;
   p->n_chunks = (hint + chunk - 1) / chunk;
-  p->variant = (opts && opts->variant) ? opts->variant : 1;
   const size_t D = (size_t)k->desc.head_dim;
   const size_t heads = (size_t)batch * num_q_heads * p->n_chunks;
   p->o_bytes = round_up(heads * D * sizeof(float), 256);
@@ -133,6 +226,7 @@ kvq_status kvq_store_create(const kvq_store_desc* desc, void* buf, size_t buf_by
   s->row_bytes = codec_row_bytes(desc->codec, desc->head_dim);
   s->n_scales = codec_scales(desc->codec, desc->head_dim);
   s->slab_bytes = (long long)desc->page_size * (s->row_bytes + 2 * s->n_scales);
+  s->rows_map_ok = encode_rows_map(s);
   if (cudaGetDevice(&s->device) != cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&s->status), sizeof(int32_t)) != cudaSuccess) {
     delete s;
@@ -170,13 +264,14 @@ kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream) {
   return from_cuda(launch_seq_lens_add(seq_lens, batch, n, static_cast<cudaStream_t>(stream)));
 }
 
-kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, int batch, int num_q_heads,
-                                      int max_len_hint, const kvq_decode_opts* opts,
-                                      size_t* bytes) {
-  if (!k_store || !bytes || batch < 1 || num_q_heads < 1 || max_len_hint < 0)
+kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store* v_store,
+                                      int batch, int num_q_heads, int max_len_hint,
+                                      const kvq_decode_opts* opts, size_t* bytes) {
+  if (!k_store || !v_store || !bytes || batch < 1 || num_q_heads < 1 || max_len_hint < 0)
     return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % k_store->desc.num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   Plan p;
-  const kvq_status st = make_plan(k_store, batch, num_q_heads, max_len_hint, opts, &p);
+  const kvq_status st = make_plan(k_store, v_store, batch, num_q_heads, max_len_hint, opts, &p);
   if (st != KVQ_OK) return st;
   *bytes = p.total;
   return KVQ_OK;
@@ -204,11 +299,14 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   const int group = num_q_heads / kd.num_kv_heads;
   Plan p;
-  kvq_status st = make_plan(k_store, batch, num_q_heads, max_len_hint, opts, &p);
+  kvq_status st = make_plan(k_store, v_store, batch, num_q_heads, max_len_hint, opts, &p);
   if (st != KVQ_OK) return st;
   if (workspace_bytes < p.total) return KVQ_ERR_WORKSPACE;
-  SimtFn fn = simt_fn(kd.codec, vd.codec);
-  if (!fn || group > 16 || p.variant != 1) return KVQ_ERR_UNSUPPORTED;
+  if (group > 16 || p.variant < 1 || p.variant > 2) return KVQ_ERR_UNSUPPORTED;
+  SimtFn sfn = simt_fn(kd.codec, vd.codec);
+  MmaFn mfn = mma_fn(kd.codec, vd.codec);
+  if (p.variant == 1 && !sfn) return KVQ_ERR_UNSUPPORTED;
+  if (p.variant == 2 && (!mfn || !k_store->rows_map_ok || !v_store->rows_map_ok)) return KVQ_ERR_UNSUPPORTED;
 
   DecodeArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -228,9 +326,10 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ml_off);
   a.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = from_cuda(fn(a, kd.head_dim, s));
+  st = from_cuda(p.variant == 2 ? mfn(a, kd.head_dim, k_store->rows_map, v_store->rows_map, s)
+                                 : sfn(a, kd.head_dim, s));
   if (st != KVQ_OK) return st;
-  return from_cuda(launch_combine(a, kd.head_dim, s));
+  return from_cuda(launch_combine_pdl(a, kd.head_dim, s));
 }
 
 kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code) {

@@ -1,0 +1,752 @@
+// Tensor-core split-K flash-decode with dequantization fused into the QK^T and PV loops.
+//
+// Same computation and split as the CUDA-core kernel (the "flash-decode-over-quant"
+// class of rMLX issue #292, with halobench record clm-0022's "dequantize KV on load"):
+// quantized K/V tiles are staged in shared memory exactly as stored and converted in
+// registers right before the matrix instructions that consume them.
+//
+// Why tensor cores: the CUDA-core kernel issues ~3.3k lane-instructions per (token, KV
+// head) for q8_0 at GQA 4:1, which caps it near half of HBM bandwidth even at full issue
+// rate.  Here the two contractions run on mma.sync m16n8k16 (fp32 accumulate):
+//
+//  * QK^T, tokens on M: S[t, h] = sum_b d_k[t, b] * sum_{j in b} k_int[t, j] * q[h, j].
+//    A = the stored K rows of 16 tokens, read with ldmatrix and turned into exact f16
+//    integers in registers; B = q (N = 8 heads of the group).  Each 32-element block's
+//    two k16 steps accumulate into a fresh fragment that is then scaled by d_k (and
+//    the softmax scale) and added to S, so the block scale is applied once per block.
+//    The k order inside a 16-element step is permuted to match the bytes ldmatrix
+//    hands each lane; q is laid out with the same permutation.
+//  * PV, head_dim on M: O^T[j, c] += sum_t v_int[t, j] * P[t, c].  A = the stored V rows
+//    (ldmatrix.trans, converted the same way), B = the probabilities.  The V block scale
+//    d_v[t, b] varies along the contraction, so it is folded into B per block:
+//    P_b[t, h] = p[t, h] * d_v[t, b] * 2^(kPScale - E).  To keep fp32-level accuracy from
+//    16-bit operands P_b is split into hi + lo halves (hi = f16(x), lo = f16(x - hi));
+//    with at most 4 heads per warp the hi and lo parts occupy the 8 N columns of one
+//    MMA, so the split costs no extra tensor instructions.  E is a running power-of-two
+//    bound of the V scales seen so far (like the running max of the softmax), which
+//    keeps P_b inside the f16 range whatever the magnitude of V.
+//
+// Data movement: one elected thread streams 64-token tiles of one (page, head) slab with
+// TMA (cp.async.bulk.tensor, 128/64/32-byte swizzle so the ldmatrix reads are free of
+// bank conflicts) plus bulk copies of the fp16 scales into an NS-deep ring of stages
+// guarded by mbarriers (full: copies landed; empty: every warp is done with the stage);
+// the warps take 16 tokens of every tile each and keep their
+// own online-softmax state (running max m and sum l per head, base 2).  Every wait is
+// bounded: on timeout the kernel records KVQ_DEVICE_TIMEOUT and returns.
+//
+// GQA: one CTA serves all heads of a KV head's group from each tile; groups of more than
+// 8 heads are split over warp groups (8 heads each) that read the same tiles.
+#pragma once
+
+#include <cuda.h>
+
+#include "kvq_device.cuh"
+
+namespace kvq {
+namespace mma {
+
+constexpr int kT = 64;            // tokens per stage
+constexpr int kTimeoutIters = 1 << 22;
+// Lazy online softmax: scores are exponentiated against a warp-uniform reference max
+// that is raised only when a score exceeds it by more than kLazy (log2 units), so every
+// p stays <= 2^kLazy and most tiles need no cross-lane reduction.
+constexpr float kLazy = 8.0f;
+// P_b = p * d_v * 2^(kPScale - E) <= 2^(kLazy + kPScale) = 2^14 fits f16 (max 65504).
+constexpr int kPScale = 6;
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done;
+}
+// Bounded wait, by every lane of a warp, for the phase of parity `parity` to complete.
+// Each lane observes the completion itself (acquire); the result is warp-uniform, so
+// the warp leaves together.  False on timeout.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+  for (int it = 0; it < kTimeoutIters; ++it)
+    if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+  return false;
+}
+// Bounded wait by a single thread.
+__device__ __forceinline__ bool mbar_wait_one(uint32_t bar, uint32_t parity) {
+  for (int it = 0; it < kTimeoutIters; ++it)
+    if (mbar_try(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (BF16) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+// ---------------------------------------------------------------- conversions
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t x, uint32_t y) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&y));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// Signed bytes packed in `u_biased` (each byte already XORed with 0x80, i.e. b + 128)
+// to an exact f16 pair, selecting the two bytes named by `sel` (0x4X4Y picks X, Y).
+// Magic-number conversion: f16 bits 0x64 << 8 | u encode 1024 + u; subtract 1152.
+__device__ __forceinline__ uint32_t i8pair_f16(uint32_t u_biased, uint32_t sel) {
+  return hsub2_u32(__byte_perm(u_biased, 0x64646464u, sel), 0x64806480u);
+}
+// Nibble pair (bits 0-3 and 16-19 of w) holding u = q + 8 -> exact f16 pair of q.
+__device__ __forceinline__ uint32_t u4pair_f16(uint32_t w) {
+  return hsub2_u32((w & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (BF16) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
+  } else {
+    return __half22float2(*reinterpret_cast<__half2*>(&v));
+  }
+}
+// x -> (hi, lo) pairs with hi = round(x), lo = round(x - hi), for two values.
+template <bool BF16>
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack2<BF16>(x0, x1);
+  const float2 h = unpack2<BF16>(hi);
+  lo = pack2<BF16>(x0 - h.x, x1 - h.y);
+}
+
+// ---------------------------------------------------------------- layout
+
+template <int KC, int VC, int D, int GW, int HG>
+struct Cfg {
+  static constexpr int NW = 4 * HG;                       // warps (4 per head group)
+  static constexpr int THREADS = NW * 32;
+  static constexpr int NPV = GW <= 4 ? 1 : 2;             // PV n-tiles per warp
+  static constexpr bool KBF = KC == KVQ_CODEC_BF16;       // MMA type of QK^T
+  static constexpr bool VBF = VC == KVQ_CODEC_BF16;       // MMA type of PV
+  static constexpr bool KQ = is_quant(KC), VQ = is_quant(VC);
+  static constexpr int KRB = KC == KVQ_CODEC_Q8_0 ? D : KC == KVQ_CODEC_Q4S ? D / 2 : 2 * D;
+  static constexpr int VRB = VC == KVQ_CODEC_Q8_0 ? D : VC == KVQ_CODEC_Q4S ? D / 2 : 2 * D;
+  static constexpr int NB = D / kBlock;                   // blocks per row
+  static constexpr int KLINE = KRB >= 128 ? 128 : KRB;    // TMA box width / swizzle span
+  static constexpr int VLINE = VRB >= 128 ? 128 : VRB;
+  static constexpr int al1k(int x) { return (x + 1023) / 1024 * 1024; }
+  static constexpr int KROWS = al1k(kT * KRB);
+  static constexpr int KSC = KQ ? al1k(kT * NB * 2) : 0;
+  static constexpr int VROWS = al1k(kT * VRB);
+  static constexpr int VSC = VQ ? al1k(kT * NB * 2) : 0;
+  static constexpr int STAGE = KROWS + KSC + VROWS + VSC;
+  // ring depth: as many stages (2..4) as fit the per-CTA budget that keeps the
+  // register-limited number of resident CTAs per SM
+  static constexpr int SMEM_BUDGET = HG == 2 ? 200 * 1024 : (D == 256 ? 100 * 1024 : 70 * 1024);
+  static constexpr int NS0 = (SMEM_BUDGET - 4096) / STAGE;
+  static constexpr int NS = NS0 > 4 ? 4 : (NS0 < 2 ? 2 : NS0);
+  static constexpr int OBUF = NW * 8 * D * 4;             // merge buffer (reuses the ring)
+  static constexpr int RING = NS * STAGE > OBUF ? NS * STAGE : OBUF;
+  static constexpr int BAR_OFF = RING;                    // 2*NS mbarriers
+  static constexpr int ML_OFF = BAR_OFF + 2 * NS * 8;     // per-warp m, l [8][2]
+  static constexpr int SMEM = ML_OFF + NW * 8 * 2 * 4 + 1024;  // +1024: runtime alignment
+  static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
+  static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
+  static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
+};
+
+// Shared-memory address of 16-byte chunk `chunk` of tile row `t` (rows as TMA wrote them).
+template <int RB>
+__device__ __forceinline__ uint32_t row_chunk(uint32_t base, int t, int chunk) {
+  if constexpr (RB >= 128) {
+    return base + (chunk >> 3) * (kT * 128) + t * 128 + (((chunk & 7) ^ (t & 7)) << 4);
+  } else if constexpr (RB == 64) {
+    return base + t * 64 + ((chunk ^ ((t >> 1) & 3)) << 4);
+  } else {
+    return base + t * 32 + ((chunk ^ ((t >> 2) & 1)) << 4);
+  }
+}
+
+// Element of head_dim held by k-slot `k` (0..15) of QK^T step `s` for the K codec.
+template <int KC>
+__device__ __forceinline__ int qk_dim(int s, int k) {
+  const int i = (k & 7) >> 1, e = k & 1, hi = k >> 3;
+  if constexpr (KC == KVQ_CODEC_Q8_0) return 16 * s + 4 * i + 2 * hi + e;
+  else if constexpr (KC == KVQ_CODEC_Q4S) return 32 * (s >> 1) + 8 * i + 2 * (s & 1) + hi + 4 * e;
+  else return 16 * s + k;
+}
+// Element of head_dim held by row `row` (0..15) of PV M-tile `mt` for the V codec.
+template <int VC>
+__device__ __forceinline__ int pv_dim(int mt, int row) {
+  const int b = mt >> 1, x = mt & 1, r = row & 7, top = row >> 3;
+  if constexpr (VC == KVQ_CODEC_Q8_0) return 32 * b + 16 * top + 2 * r + x;
+  else if constexpr (VC == KVQ_CODEC_Q4S) return 32 * b + 4 * r + 2 * x + top;
+  else return 16 * mt + row;
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int KC, int VC, int D, int GW, int HG>
+__global__ void __launch_bounds__(Cfg<KC, VC, D, GW, HG>::THREADS, 1)
+decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  DecodeArgs a) {
+  using C = Cfg<KC, VC, D, GW, HG>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle pattern
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + C::BAR_OFF;           // + 8*s
+  const uint32_t bar_empty = sbase + C::BAR_OFF + 8 * C::NS;
+  float* ml_all = reinterpret_cast<float*>(smem + C::ML_OFF);
+
+  const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.group;
+  const int P = a.k.page_size;
+
+  const long long cap = min((long long)a.max_pages * P, (long long)a.n_chunks * a.chunk_tokens);
+  long long Lraw = a.seq_lens[b];
+  if (Lraw < 0 || Lraw > cap) {
+    if (tid == 0 && chunk == 0 && kvh == 0) {
+      record_fault(a.k.status, KVQ_DEVICE_BAD_SEQ_LEN);
+      record_fault(a.v.status, KVQ_DEVICE_BAD_SEQ_LEN);
+    }
+    Lraw = Lraw < 0 ? 0 : cap;
+  }
+  const int L = (int)Lraw;
+  const int t_begin = chunk * a.chunk_tokens;
+  if (t_begin >= L) return;
+  const int t_end = min(L, t_begin + a.chunk_tokens);
+  const int n_tiles = (t_end - t_begin + kT - 1) / kT;
+  const int32_t* pt = a.page_table + (long long)b * a.max_pages;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, C::NW);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------ tile producer
+  // Lane 0 of warp 0 issues the copies: the first NS tiles up front, then tile k + NS
+  // into stage k % NS as soon as every warp has released tile k.
+  auto issue_tile = [&](int tile) {
+    const int s = tile % C::NS;
+    const int pos0 = t_begin + tile * kT;
+    const int page = pt[pos0 / P];
+    const int row0 = pos0 % P;
+    const uint32_t full = bar_full + 8 * s;
+    if (page < 0 || page >= a.k.num_pages || page >= a.v.num_pages) {
+      record_fault(a.k.status, KVQ_DEVICE_BAD_PAGE);
+      record_fault(a.v.status, KVQ_DEVICE_BAD_PAGE);
+      mbar_arrive(full);
+      return;
+    }
+    mbar_expect_tx(full, C::K_TX + C::V_TX);
+    const uint32_t st = sbase + s * C::STAGE;
+#pragma unroll
+    for (int seg = 0; seg < (C::KRB + 127) / 128; ++seg)
+      tma_load_4d(st + seg * kT * 128, &tmk, seg * 128, row0, kvh, page, full);
+    const uint32_t vst = st + C::KROWS + C::KSC;
+#pragma unroll
+    for (int seg = 0; seg < (C::VRB + 127) / 128; ++seg)
+      tma_load_4d(vst + seg * kT * 128, &tmv, seg * 128, row0, kvh, page, full);
+    if constexpr (C::KQ) {
+      const uint8_t* src = a.k.buf + ((long long)page * a.k.num_kv_heads + kvh) * a.k.slab_bytes +
+                           (long long)P * C::KRB + (long long)row0 * C::NB * 2;
+      bulk_load(st + C::KROWS, src, kT * C::NB * 2, full);
+    }
+    if constexpr (C::VQ) {
+      const uint8_t* src = a.v.buf + ((long long)page * a.v.num_kv_heads + kvh) * a.v.slab_bytes +
+                           (long long)P * C::VRB + (long long)row0 * C::NB * 2;
+      bulk_load(vst + C::VROWS, src, kT * C::NB * 2, full);
+    }
+  };
+  const bool producer = tid == 0;
+  if (producer)
+    for (int tile = 0; tile < n_tiles && tile < C::NS; ++tile) issue_tile(tile);
+  __syncwarp();
+
+  // ------------------------------------------------------------ compute warps
+  const int hg = warp >> 2;          // head group
+  const int ws = warp & 3;           // 16-token slice of every tile
+  const int r = lane >> 2, i4 = lane & 3;
+  const int t0 = ws * 16;
+
+  // q fragments (B operand of QK^T): column r, k-slots {2i, 2i+1} and {2i+8, 2i+9}.
+  // With at most 4 heads per warp, columns 4..7 repeat heads 0..3, so that after the
+  // transpose of p every PV column (head, hi|lo) finds its head's p in its own lane.
+  uint32_t qf[C::QSTEPS][2];
+  {
+    const int h = hg * 8 + (GW <= 4 ? (r & 3) : r);
+    const bool hv = h < G;
+    const __nv_bfloat16* qrow = a.q + ((long long)b * a.num_q_heads + (long long)kvh * G + (hv ? h : 0)) * D;
+#pragma unroll
+    for (int s = 0; s < C::QSTEPS; ++s) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float x0 = hv ? __bfloat162float(qrow[qk_dim<KC>(s, 8 * half + 2 * i4)]) : 0.0f;
+        const float x1 = hv ? __bfloat162float(qrow[qk_dim<KC>(s, 8 * half + 2 * i4 + 1)]) : 0.0f;
+        qf[s][half] = pack2<C::KBF>(x0, x1);
+      }
+    }
+  }
+
+  float o[C::QSTEPS][C::NPV][4];   // O^T accumulators: D/16 M-tiles x NPV n-tiles
+#pragma unroll
+  for (int mt = 0; mt < C::QSTEPS; ++mt)
+#pragma unroll
+    for (int n = 0; n < C::NPV; ++n)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[mt][n][k] = 0.0f;
+  // reference max (warp-uniform) and this lane's partial sum for QK columns 2*i4, 2*i4+1
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  int E = -100;                                                 // running V-scale exponent bound
+  bool timed_out = false;
+
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    const int s = tile % C::NS;
+    if (!mbar_wait_warp(bar_full + 8 * s, (tile / C::NS) & 1)) {
+      timed_out = true;
+      break;
+    }
+    const int pos_w = t_begin + tile * kT + t0;
+    const int page = pt[(t_begin + tile * kT) / P];
+    const bool tile_ok = page >= 0 && page < a.k.num_pages && page < a.v.num_pages;
+    const int n_valid = tile_ok ? max(0, min(16, t_end - pos_w)) : 0;
+    if (n_valid > 0) {
+      const uint32_t st = sbase + s * C::STAGE;
+      const uint32_t kst = st, vst = st + C::KROWS + C::KSC;
+      const __half* ksc = reinterpret_cast<const __half*>(smem + s * C::STAGE + C::KROWS);
+      const __half* vsc = reinterpret_cast<const __half*>(smem + s * C::STAGE + C::KROWS + C::KSC + C::VROWS);
+      const int mi = lane >> 3, mr = lane & 7;
+
+      // ---------------- QK^T: S[tok r / r+8][heads 2i, 2i+1]
+      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if constexpr (C::KQ) {
+        // per-token block scales of rows r and r+8, times the softmax scale (log2 units)
+        float dk[2][C::NB];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+          for (int bb = 0; bb < C::NB; ++bb)
+            dk[rr][bb] = __half2float(ksc[(t0 + r + 8 * rr) * C::NB + bb]) * a.qk_scale_log2;
+        if constexpr (KC == KVQ_CODEC_Q8_0) {
+#pragma unroll
+          for (int bb = 0; bb < C::NB; ++bb) {
+            uint32_t x0, x1, x2, x3;
+            ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * bb + (mi >> 1)), x0, x1, x2, x3);
+            x0 ^= 0x80808080u; x1 ^= 0x80808080u; x2 ^= 0x80808080u; x3 ^= 0x80808080u;
+            float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            uint32_t af[4];
+            af[0] = i8pair_f16(x0, 0x4140); af[1] = i8pair_f16(x1, 0x4140);
+            af[2] = i8pair_f16(x0, 0x4342); af[3] = i8pair_f16(x1, 0x4342);
+            mma16816<false>(cb, af, qf[2 * bb][0], qf[2 * bb][1]);
+            af[0] = i8pair_f16(x2, 0x4140); af[1] = i8pair_f16(x3, 0x4140);
+            af[2] = i8pair_f16(x2, 0x4342); af[3] = i8pair_f16(x3, 0x4342);
+            mma16816<false>(cb, af, qf[2 * bb + 1][0], qf[2 * bb + 1][1]);
+            sc[0] = fmaf(dk[0][bb], cb[0], sc[0]);
+            sc[1] = fmaf(dk[0][bb], cb[1], sc[1]);
+            sc[2] = fmaf(dk[1][bb], cb[2], sc[2]);
+            sc[3] = fmaf(dk[1][bb], cb[3], sc[3]);
+          }
+        } else {  // q4s: one ldmatrix.x4 covers two blocks
+#pragma unroll
+          for (int bb = 0; bb < C::NB; bb += 2) {
+            uint32_t x[4];
+            ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), x[0], x[1], x[2], x[3]);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t ra = x[2 * h2], rb = x[2 * h2 + 1];  // rows r and r+8 of block bb+h2
+              float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+              uint32_t af[4];
+              af[0] = u4pair_f16(ra); af[1] = u4pair_f16(rb);
+              af[2] = u4pair_f16(ra >> 4); af[3] = u4pair_f16(rb >> 4);
+              mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
+              af[0] = u4pair_f16(ra >> 8); af[1] = u4pair_f16(rb >> 8);
+              af[2] = u4pair_f16(ra >> 12); af[3] = u4pair_f16(rb >> 12);
+              mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
+              sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
+              sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);
+              sc[2] = fmaf(dk[1][bb + h2], cb[2], sc[2]);
+              sc[3] = fmaf(dk[1][bb + h2], cb[3], sc[3]);
+            }
+          }
+        }
+      } else {  // 16-bit K: natural k order, one ldmatrix.x4 per k16 step
+#pragma unroll
+        for (int ks = 0; ks < C::QSTEPS; ++ks) {
+          uint32_t af[4];
+          ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), af[0], af[1], af[2], af[3]);
+          mma16816<C::KBF>(sc, af, qf[ks][0], qf[ks][1]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[k] *= a.qk_scale_log2;
+      }
+      const bool v_r = r < n_valid, v_r8 = r + 8 < n_valid;
+      if (!v_r) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+      if (!v_r8) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+
+      // ---------------- V scales of this lane's PV tokens (2i, 2i+1, 2i+8, 2i+9)
+      const int tk[4] = {2 * i4, 2 * i4 + 1, 2 * i4 + 8, 2 * i4 + 9};
+      float dv[4][C::NB];
+      int ex_lane = -127;   // dmax < 2^ex_lane over this lane's tokens
+      if constexpr (C::VQ) {
+        float dmax = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int bb = 0; bb < C::NB; ++bb) {
+            const float d = tk[u] < n_valid ? __half2float(vsc[(t0 + tk[u]) * C::NB + bb]) : 0.0f;
+            dv[u][bb] = d;
+            dmax = fmaxf(dmax, d);
+          }
+        if (dmax > 0.0f) ex_lane = (int)((__float_as_uint(dmax) >> 23) & 0xff) - 127 + 1;
+      } else {
+        ex_lane = 0;
+      }
+
+      // ---------------- lazy online softmax over the warp's 16 tokens (columns = heads)
+      const float lm0 = fmaxf(sc[0], sc[2]), lm1 = fmaxf(sc[1], sc[3]);
+      const bool over = (lm0 > m0 + kLazy) || (lm1 > m1 + kLazy) || (ex_lane > E);
+      if (__any_sync(0xffffffffu, over)) {
+        float mx0 = lm0, mx1 = lm1;
+        int ex = ex_lane;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, 1));
+        ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, 2));
+        const int E_new = max(E, ex);
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float e2 = __uint_as_float((uint32_t)(127 + E - E_new) << 23);  // 2^(E - E_new)
+        float f0 = (mn0 == -INFINITY) ? 1.0f : fast_exp2(m0 - mn0);
+        float f1 = (mn1 == -INFINITY) ? 1.0f : fast_exp2(m1 - mn1);
+        l0 *= f0;
+        l1 *= f1;
+        f0 *= e2;
+        f1 *= e2;
+#pragma unroll
+        for (int mt = 0; mt < C::QSTEPS; ++mt)
+#pragma unroll
+          for (int n = 0; n < C::NPV; ++n) {
+            o[mt][n][0] *= f0; o[mt][n][1] *= f1; o[mt][n][2] *= f0; o[mt][n][3] *= f1;
+          }
+        m0 = mn0;
+        m1 = mn1;
+        E = E_new;
+      }
+      const float p0 = (m0 == -INFINITY) ? 0.0f : fast_exp2(sc[0] - m0);
+      const float p1 = (m1 == -INFINITY) ? 0.0f : fast_exp2(sc[1] - m1);
+      const float p2 = (m0 == -INFINITY) ? 0.0f : fast_exp2(sc[2] - m0);
+      const float p3 = (m1 == -INFINITY) ? 0.0f : fast_exp2(sc[3] - m1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+
+      // ---------------- transpose p (fp32, as two 16-bit halves) to the PV B layout:
+      // lane (r, i) receives p[tok 2i, 2i+1, 2i+8, 2i+9][column r]
+      float pv[4];
+      {
+        const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+        const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
+        const uint32_t ah = movtrans(__byte_perm(u0, u1, 0x7632)), al = movtrans(__byte_perm(u0, u1, 0x5410));
+        const uint32_t bh = movtrans(__byte_perm(u2, u3, 0x7632)), bl = movtrans(__byte_perm(u2, u3, 0x5410));
+        pv[0] = __uint_as_float(__byte_perm(al, ah, 0x5410));
+        pv[1] = __uint_as_float(__byte_perm(al, ah, 0x7632));
+        pv[2] = __uint_as_float(__byte_perm(bl, bh, 0x5410));
+        pv[3] = __uint_as_float(__byte_perm(bl, bh, 0x7632));
+      }
+      const float pscale = __uint_as_float((uint32_t)(127 + kPScale - E) << 23);  // 2^(kPScale - E)
+
+      // ---------------- PV
+      if constexpr (C::VQ) {
+#pragma unroll
+        for (int bb = 0; bb < C::NB; ++bb) {
+          float x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) x[u] = pv[u] * dv[u][bb] * pscale;
+          uint32_t bh0, bl0, bh1, bl1;
+          split2<false>(x[0], x[1], bh0, bl0);
+          split2<false>(x[2], x[3], bh1, bl1);
+          uint32_t bf[C::NPV][2];
+          if constexpr (C::NPV == 1) {
+            const bool lo = r >= 4;
+            bf[0][0] = lo ? bl0 : bh0;
+            bf[0][1] = lo ? bl1 : bh1;
+          } else {
+            bf[0][0] = bh0; bf[0][1] = bh1;
+            bf[1][0] = bl0; bf[1][1] = bl1;
+          }
+          if constexpr (VC == KVQ_CODEC_Q8_0) {
+            uint32_t y0, y1, y2, y3;
+            // matrices: (tok 0-7, chunk 2b), (tok 0-7, chunk 2b+1), (tok 8-15, 2b), (tok 8-15, 2b+1)
+            ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * bb + (mi & 1)), y0, y1, y2, y3);
+            y0 ^= 0x80808080u; y1 ^= 0x80808080u; y2 ^= 0x80808080u; y3 ^= 0x80808080u;
+            uint32_t ae[4] = {i8pair_f16(y0, 0x4240), i8pair_f16(y1, 0x4240), i8pair_f16(y2, 0x4240),
+                              i8pair_f16(y3, 0x4240)};
+            uint32_t ao[4] = {i8pair_f16(y0, 0x4341), i8pair_f16(y1, 0x4341), i8pair_f16(y2, 0x4341),
+                              i8pair_f16(y3, 0x4341)};
+#pragma unroll
+            for (int n = 0; n < C::NPV; ++n) {
+              mma16816<false>(o[2 * bb][n], ae, bf[n][0], bf[n][1]);
+              mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
+            }
+          } else {  // q4s: matrices (tok 0-7, chunk b), (tok 8-15, chunk b) for this block
+            uint32_t y0, y1, y2, y3;
+            ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, (bb & ~1) + (mi >> 1)), y0, y1, y2, y3);
+            const uint32_t ya = (bb & 1) ? y2 : y0, yb = (bb & 1) ? y3 : y1;
+            uint32_t a01[4] = {u4pair_f16(ya), u4pair_f16(ya >> 4), u4pair_f16(yb), u4pair_f16(yb >> 4)};
+            uint32_t a23[4] = {u4pair_f16(ya >> 8), u4pair_f16(ya >> 12), u4pair_f16(yb >> 8),
+                               u4pair_f16(yb >> 12)};
+#pragma unroll
+            for (int n = 0; n < C::NPV; ++n) {
+              mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
+              mma16816<false>(o[2 * bb + 1][n], a23, bf[n][0], bf[n][1]);
+            }
+          }
+        }
+      } else {
+        // 16-bit V: one B operand for every M-tile; zero the A lanes of tokens past the end
+        float x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = pv[u] * pscale;
+        uint32_t bh0, bl0, bh1, bl1;
+        split2<C::VBF>(x[0], x[1], bh0, bl0);
+        split2<C::VBF>(x[2], x[3], bh1, bl1);
+        uint32_t bf[C::NPV][2];
+        if constexpr (C::NPV == 1) {
+          const bool lo = r >= 4;
+          bf[0][0] = lo ? bl0 : bh0;
+          bf[0][1] = lo ? bl1 : bh1;
+        } else {
+          bf[0][0] = bh0; bf[0][1] = bh1;
+          bf[1][0] = bl0; bf[1][1] = bl1;
+        }
+        uint32_t kmask_lo = 0xffffffffu, kmask_hi = 0xffffffffu;
+        if (n_valid < 16) {
+          kmask_lo = (tk[0] < n_valid ? 0x0000ffffu : 0u) | (tk[1] < n_valid ? 0xffff0000u : 0u);
+          kmask_hi = (tk[2] < n_valid ? 0x0000ffffu : 0u) | (tk[3] < n_valid ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::QSTEPS; ++mt) {
+          uint32_t af[4];
+          // matrices: (tok 0-7, chunk 2mt), (tok 0-7, chunk 2mt+1), (tok 8-15, 2mt), (tok 8-15, 2mt+1)
+          ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * mt + (mi & 1)), af[0], af[1], af[2], af[3]);
+          af[0] &= kmask_lo; af[1] &= kmask_lo; af[2] &= kmask_hi; af[3] &= kmask_hi;
+#pragma unroll
+          for (int n = 0; n < C::NPV; ++n) mma16816<C::VBF>(o[mt][n], af, bf[n][0], bf[n][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    if (warp == 0) {
+      bool fail = false;
+      if (producer && tile + C::NS < n_tiles) {
+        if (mbar_wait_one(bar_empty + 8 * s, (tile / C::NS) & 1)) issue_tile(tile + C::NS);
+        else fail = true;
+      }
+      // reconverges warp 0 after the producer lane's branch
+      if (__shfl_sync(0xffffffffu, (int)fail, 0)) {
+        timed_out = true;
+        break;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ merge (a7)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int NWT = C::NW * 32;
+  if (timed_out) record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
+  // every warp reaches the barriers below (a timed-out warp skips only its tiles)
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+  // per-head sums of the lanes' partials; O true scale: O * 2^(E - kPScale)
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  const float oscale = __uint_as_float((uint32_t)(127 + E - kPScale) << 23);
+  float* ml = ml_all + warp * 16;
+  if (r == 0) {
+    ml[(2 * i4) * 2] = m0;
+    ml[(2 * i4) * 2 + 1] = l0;
+    ml[(2 * i4 + 1) * 2] = m1;
+    ml[(2 * i4 + 1) * 2 + 1] = l1;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+  float* obuf = reinterpret_cast<float*>(smem);  // the ring is idle now
+  {
+    // heads of this lane's O columns after folding: 2*i4, 2*i4+1 (lanes i4 < GW/2 only)
+    const int hA = 2 * i4, hB = 2 * i4 + 1;
+    float fA = 0.0f, fB = 0.0f;
+    {
+      float MA = -INFINITY, MB = -INFINITY;
+      const int wg0 = hg * 4;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        MA = fmaxf(MA, ml_all[(wg0 + w) * 16 + (hA & 7) * 2]);
+        MB = fmaxf(MB, ml_all[(wg0 + w) * 16 + (hB & 7) * 2]);
+      }
+      const float mA = __shfl_sync(0xffffffffu, m0, (lane & ~3) | (i4 & (GW <= 4 ? 1 : 3)));
+      const float mB = __shfl_sync(0xffffffffu, m1, (lane & ~3) | (i4 & (GW <= 4 ? 1 : 3)));
+      fA = (mA == -INFINITY) ? 0.0f : fast_exp2(mA - MA) * oscale;
+      fB = (mB == -INFINITY) ? 0.0f : fast_exp2(mB - MB) * oscale;
+    }
+#pragma unroll
+    for (int mt = 0; mt < C::QSTEPS; ++mt) {
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float x = o[mt][0][k];
+        if constexpr (C::NPV == 2) x += o[mt][1][k];
+        else x += __shfl_xor_sync(0xffffffffu, x, 2);  // add the lo columns (lanes i4 ^ 2)
+        v[k] = x;
+      }
+      if (GW > 4 || i4 < 2) {
+        const int d0 = pv_dim<VC>(mt, r), d1 = pv_dim<VC>(mt, r + 8);
+        obuf[(warp * 8 + hA) * D + d0] = v[0] * fA;
+        obuf[(warp * 8 + hB) * D + d0] = v[1] * fB;
+        obuf[(warp * 8 + hA) * D + d1] = v[2] * fA;
+        obuf[(warp * 8 + hB) * D + d1] = v[3] * fB;
+      }
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+  const long long head0 = (long long)b * a.num_q_heads + (long long)kvh * G;
+  const int gcount = G < 8 * HG ? G : 8 * HG;
+  for (int idx = tid; idx < gcount * D; idx += NWT) {
+    const int h = idx / D, j = idx % D;
+    const int hgi = h >> 3, hl = h & 7;
+    if (hl >= GW) continue;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
+    a.part_o[((head0 + h) * a.n_chunks + chunk) * D + j] = sum;
+  }
+  for (int h = tid; h < gcount; h += NWT) {
+    const int hgi = h >> 3, hl = h & 7;
+    if (hl >= GW) continue;
+    float M = -INFINITY;
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, ml_all[(hgi * 4 + w) * 16 + hl * 2]);
+    float lsum = 0.0f;
+    for (int w = 0; w < 4; ++w) {
+      const float mw = ml_all[(hgi * 4 + w) * 16 + hl * 2];
+      if (mw != -INFINITY) lsum += fast_exp2(mw - M) * ml_all[(hgi * 4 + w) * 16 + hl * 2 + 1];
+    }
+    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2] = M;
+    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2 + 1] = lsum;
+  }
+}
+
+template <int KC, int VC, int D, int GW, int HG>
+cudaError_t launch(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
+  using C = Cfg<KC, VC, D, GW, HG>;
+  auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_chunks, a.k.num_kv_heads, a.batch);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tmk, tmv, a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Resident CTAs per SM of one instantiation (0 on error).
+template <int KC, int VC, int D, int GW, int HG>
+int occupancy() {
+  using C = Cfg<KC, VC, D, GW, HG>;
+  auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int KC, int VC>
+int occupancy_pair(int head_dim, int g) {
+#define KVQ_MMA_O(D)                                         \
+  if (g <= 4) return occupancy<KC, VC, D, 4, 1>();           \
+  if (g <= 8) return occupancy<KC, VC, D, 8, 1>();           \
+  if (g <= 16) return occupancy<KC, VC, D, 8, 2>();          \
+  return 0;
+  switch (head_dim) {
+    case 64: { KVQ_MMA_O(64) }
+    case 128: { KVQ_MMA_O(128) }
+    case 256: { KVQ_MMA_O(256) }
+    default: return 0;
+  }
+#undef KVQ_MMA_O
+}
+
+template <int KC, int VC>
+cudaError_t launch_pair(const DecodeArgs& a, int head_dim, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                        cudaStream_t stream) {
+  const int g = a.group;
+#define KVQ_MMA_G(D)                                                         \
+  if (g <= 4) return launch<KC, VC, D, 4, 1>(a, tmk, tmv, stream);          \
+  if (g <= 8) return launch<KC, VC, D, 8, 1>(a, tmk, tmv, stream);          \
+  if (g <= 16) return launch<KC, VC, D, 8, 2>(a, tmk, tmv, stream);         \
+  return cudaErrorNotSupported;
+  switch (head_dim) {
+    case 64: { KVQ_MMA_G(64) }
+    case 128: { KVQ_MMA_G(128) }
+    case 256: { KVQ_MMA_G(256) }
+    default: return cudaErrorNotSupported;
+  }
+#undef KVQ_MMA_G
+}
+
+}  // namespace mma
+}  // namespace kvq

@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_simt_kernel(DecodeArgs a) 
   }
 
   // ---- merge the four warps' (m, l, acc) and write the chunk's partials (a7) ----
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   cp_async_wait<0>();
   __syncthreads();
   if (lane == 0) {

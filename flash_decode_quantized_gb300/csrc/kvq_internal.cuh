@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -9,6 +10,8 @@
 #include "../../include/kvq.h"
 
 struct kvq_store {
+  CUtensorMap rows_map;  // TMA map of the row data: {row_bytes, page_size, kv_heads, pages}
+  bool rows_map_ok;
   kvq_store_desc desc;
   uint8_t* buf;        // caller-owned device memory
   size_t bytes;
@@ -83,11 +86,7 @@ cudaError_t launch_append(const kvq_store* store, const __nv_bfloat16* rows, int
                           const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                           cudaStream_t stream);
 cudaError_t launch_seq_lens_add(int32_t* seq_lens, int batch, int n, cudaStream_t stream);
-// Returns cudaErrorNotSupported when no kernel is built for the combination.
-cudaError_t launch_decode_simt(const DecodeArgs& a, int k_codec, int v_codec, int head_dim,
-                               cudaStream_t stream);
-cudaError_t launch_combine(const DecodeArgs& a, int head_dim, cudaStream_t stream);
-bool decode_simt_supported(int k_codec, int v_codec, int head_dim, int group);
+cudaError_t launch_combine_pdl(const DecodeArgs& a, int head_dim, cudaStream_t stream);
 
 void count_launch();
 

@@ -1,0 +1,12 @@
+// Tensor-core decode kernels for K=F16, V=F16 (instantiations of kvq_decode_mma.cuh).
+#include "kvq_decode_mma.cuh"
+
+namespace kvq {
+cudaError_t mma_launch_f16_f16(const DecodeArgs& a, int head_dim, const CUtensorMap& tmk,
+                            const CUtensorMap& tmv, cudaStream_t stream) {
+  return mma::launch_pair<KVQ_CODEC_F16, KVQ_CODEC_F16>(a, head_dim, tmk, tmv, stream);
+}
+int mma_occupancy_f16_f16(int head_dim, int group) {
+  return mma::occupancy_pair<KVQ_CODEC_F16, KVQ_CODEC_F16>(head_dim, group);
+}
+}  // namespace kvq

@@ -19,7 +19,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so"
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_DEVICE_FAULT, \
     KVQ_ERR_WORKSPACE = range(6)
 CODECS = {"bf16": 0, "f16": 1, "q8_0": 2, "q4s": 3}
-DEVICE_FAULTS = {0: "ok", 1: "bad_page", 2: "bad_position", 3: "bad_seq_len"}
+DEVICE_FAULTS = {0: "ok", 1: "bad_page", 2: "bad_position", 3: "bad_seq_len", 4: "timeout"}
 
 
 class KvqError(RuntimeError):
@@ -54,7 +54,7 @@ def _load():
         "kvq_destroy": [P],
         "kvq_append": [P, P, I, I, P, P, I, V],
         "kvq_seq_lens_add": [P, I, I, V],
-        "kvq_decode_workspace_bytes": [P, I, I, I, ctypes.POINTER(DecodeOpts), ctypes.POINTER(Z)],
+        "kvq_decode_workspace_bytes": [P, P, I, I, I, ctypes.POINTER(DecodeOpts), ctypes.POINTER(Z)],
         "kvq_flash_decode": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
                              ctypes.POINTER(DecodeOpts), P, Z, V],
         "kvq_store_get_error": [P, ctypes.POINTER(ctypes.c_int32)],
@@ -175,10 +175,11 @@ def kvq_seq_lens_add(seq_lens: torch.Tensor, n: int, stream=None) -> None:
                                 _stream(stream)), "kvq_seq_lens_add")
 
 
-def kvq_decode_workspace_bytes(k_store: Store, batch: int, num_q_heads: int, max_len_hint: int,
-                               chunk_tokens: int = 0, variant: int = 0) -> int:
+def kvq_decode_workspace_bytes(k_store: Store, v_store: Store, batch: int, num_q_heads: int,
+                               max_len_hint: int, chunk_tokens: int = 0, variant: int = 0) -> int:
     n = ctypes.c_size_t()
-    _check(lib.kvq_decode_workspace_bytes(k_store.handle, batch, num_q_heads, int(max_len_hint),
+    _check(lib.kvq_decode_workspace_bytes(k_store.handle, v_store.handle, batch, num_q_heads,
+                                          int(max_len_hint),
                                           _opts(chunk_tokens, variant), ctypes.byref(n)),
            "kvq_decode_workspace_bytes")
     return n.value
@@ -197,7 +198,7 @@ def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: 
         max_len_hint = max_pages * k_store.page_size
     if out is None:
         out = torch.empty((bsz, hq, dim), dtype=torch.float32, device=q.device)
-    need = kvq_decode_workspace_bytes(k_store, bsz, hq, max_len_hint, chunk_tokens, variant)
+    need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq, max_len_hint, chunk_tokens, variant)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])

@@ -72,8 +72,10 @@ enum {
   KVQ_DEVICE_OK = 0,
   KVQ_DEVICE_BAD_PAGE = 1,      /* page id outside [0, num_pages) */
   KVQ_DEVICE_BAD_POSITION = 2,  /* append position outside [0, max_pages*page_size) */
-  KVQ_DEVICE_BAD_SEQ_LEN = 3    /* sequence length < 0, past the page table, or past
+  KVQ_DEVICE_BAD_SEQ_LEN = 3,   /* sequence length < 0, past the page table, or past
                                    the max_len_hint that sized the decode split */
+  KVQ_DEVICE_TIMEOUT = 4        /* a kernel's bounded wait for its own tile copies ran
+                                   out; the kernel stopped and its outputs are invalid */
 };
 
 /* Shape of one store.  head_dim in {64, 128, 256}; page_size a multiple of 64 in
@@ -130,10 +132,11 @@ kvq_status kvq_append(kvq_store* store, const void* rows, int n_new, int batch,
 /* seq_lens[b] += n for b < batch, on the device (after the K and the V append). */
 kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
 
-/* Device workspace bytes a kvq_flash_decode call with the same arguments needs. */
-kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, int batch, int num_q_heads,
-                                      int max_len_hint, const kvq_decode_opts* opts,
-                                      size_t* bytes);
+/* Device workspace bytes a kvq_flash_decode call with the same stores, batch, head
+ * count, max_len_hint and options needs (the split depends on both stores' codecs). */
+kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store* v_store,
+                                      int batch, int num_q_heads, int max_len_hint,
+                                      const kvq_decode_opts* opts, size_t* bytes);
 
 /* Split-K flash-decode over the quantized store (a2..a8):
  *   q          device bf16 [batch][num_q_heads][head_dim]

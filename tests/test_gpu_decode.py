@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 PAIRS = [("bf16", "bf16"), ("f16", "f16"), ("q8_0", "bf16"), ("q8_0", "q8_0"),
          ("q4s", "q4s"), ("q8_0", "q4s")]
-VARIANTS = [1]
+VARIANTS = [1, 2]
 
 
 def run_decode(inp, kc, vc, **kw):

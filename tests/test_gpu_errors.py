@@ -31,7 +31,7 @@ def test_position_past_page_table_is_recorded():
     assert k.kvq_store_get_error(st) == 2
 
 
-@pytest.mark.parametrize("variant", [1])
+@pytest.mark.parametrize("variant", [1, 2])
 def test_bad_page_in_decode_is_recorded(variant):
     inp = make_inputs([500], 8, 2, 128, seed=1)
     k = kvq()
@@ -45,7 +45,7 @@ def test_bad_page_in_decode_is_recorded(variant):
     assert np.all(np.isfinite(out.cpu().numpy()))
 
 
-@pytest.mark.parametrize("variant", [1])
+@pytest.mark.parametrize("variant", [1, 2])
 def test_seq_len_past_hint_is_recorded(variant):
     inp = make_inputs([500], 8, 2, 128, seed=2)
     k = kvq()
