@@ -156,6 +156,7 @@ struct Plan {
   int variant;
   size_t o_bytes;
   size_t ml_off;
+  size_t cnt_off;
   size_t total;
 };
 
@@ -195,7 +196,8 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   const size_t heads = (size_t)batch * num_q_heads * p->n_chunks;
   p->o_bytes = round_up(heads * D * sizeof(float), 256);
   p->ml_off = p->o_bytes;
-  p->total = p->o_bytes + round_up(heads * 2 * sizeof(float), 256);
+  p->cnt_off = p->ml_off + round_up(heads * 2 * sizeof(float), 256);
+  p->total = p->cnt_off + round_up((size_t)batch * k->desc.num_kv_heads * sizeof(unsigned), 256);
   return KVQ_OK;
 }
 
@@ -277,6 +279,11 @@ kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store*
   return KVQ_OK;
 }
 
+kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes == 0) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_store* v_store,
                             const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                             kvq_codec codec, float* out, int batch, int num_q_heads,
@@ -324,10 +331,12 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   a.n_chunks = p.n_chunks;
   a.part_o = static_cast<float*>(workspace);
   a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ml_off);
+  a.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + p.cnt_off);
   a.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = from_cuda(p.variant == 2 ? mfn(a, kd.head_dim, k_store->rows_map, v_store->rows_map, s)
-                                 : sfn(a, kd.head_dim, s));
+  if (p.variant == 2)  // the tensor-core kernel merges the split itself (last CTA per unit)
+    return from_cuda(mfn(a, kd.head_dim, k_store->rows_map, v_store->rows_map, s));
+  st = from_cuda(sfn(a, kd.head_dim, s));
   if (st != KVQ_OK) return st;
   return from_cuda(launch_combine_pdl(a, kd.head_dim, s));
 }

@@ -167,6 +167,28 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = pack2<BF16>(x0 - h.x, x1 - h.y);
 }
 
+// (x0, x1) -> f16/bf16 pair of x (lo_sel = 0: the hi part) or of x - hi (lo_sel = 1).
+template <bool BF16>
+__device__ __forceinline__ uint32_t hi_or_lo(float x0, float x1, float lo_sel) {
+  const float2 h = unpack2<BF16>(pack2<BF16>(x0, x1));
+  return pack2<BF16>(fmaf(-lo_sel, h.x, x0), fmaf(-lo_sel, h.y, x1));
+}
+
+// The NB fp16 scales of tile row t (a contiguous NB*2-byte run) as NB/2 packed words.
+template <int NB>
+__device__ __forceinline__ void load_scale_words(const uint8_t* base, int t, uint32_t* w) {
+  const uint8_t* p = base + t * NB * 2;
+  if constexpr (NB == 2) {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  } else if constexpr (NB == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  }
+}
+
 // ---------------------------------------------------------------- layout
 
 template <int KC, int VC, int D, int GW, int HG>
@@ -196,8 +218,9 @@ struct Cfg {
   static constexpr int OBUF = NW * 8 * D * 4;             // merge buffer (reuses the ring)
   static constexpr int RING = NS * STAGE > OBUF ? NS * STAGE : OBUF;
   static constexpr int BAR_OFF = RING;                    // 2*NS mbarriers
-  static constexpr int ML_OFF = BAR_OFF + 2 * NS * 8;     // per-warp m, l [8][2]
-  static constexpr int SMEM = ML_OFF + NW * 8 * 2 * 4 + 1024;  // +1024: runtime alignment
+  static constexpr int OK_OFF = BAR_OFF + 2 * NS * 8;     // per-stage "tile is valid" flags
+  static constexpr int ML_OFF = OK_OFF + 32;              // per-warp m, l [8][2]
+  static constexpr int SMEM = ML_OFF + (NW + 2) * 16 * 4 + 1024;  // + per-head (M, l); +1024: alignment
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
   static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
@@ -246,6 +269,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   const uint32_t bar_full = sbase + C::BAR_OFF;           // + 8*s
   const uint32_t bar_empty = sbase + C::BAR_OFF + 8 * C::NS;
   float* ml_all = reinterpret_cast<float*>(smem + C::ML_OFF);
+  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + C::OK_OFF);
 
   const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -263,7 +287,13 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   }
   const int L = (int)Lraw;
   const int t_begin = chunk * a.chunk_tokens;
-  if (t_begin >= L) return;
+  if (t_begin >= L) {
+    if (L == 0 && chunk == 0) {  // empty sequence: its heads' outputs are zero
+      const long long h0 = (long long)b * a.num_q_heads + (long long)kvh * G;
+      for (int idx = tid; idx < G * D; idx += C::THREADS) a.out[h0 * D + idx] = 0.0f;
+    }
+    return;
+  }
   const int t_end = min(L, t_begin + a.chunk_tokens);
   const int n_tiles = (t_end - t_begin + kT - 1) / kT;
   const int32_t* pt = a.page_table + (long long)b * a.max_pages;
@@ -286,7 +316,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int page = pt[pos0 / P];
     const int row0 = pos0 % P;
     const uint32_t full = bar_full + 8 * s;
-    if (page < 0 || page >= a.k.num_pages || page >= a.v.num_pages) {
+    // the flag is published to the warps by the mbarrier phase that completes below
+    const bool ok = page >= 0 && page < a.k.num_pages && page < a.v.num_pages;
+    stage_ok[s] = ok ? 1 : 0;
+    if (!ok) {
       record_fault(a.k.status, KVQ_DEVICE_BAD_PAGE);
       record_fault(a.v.status, KVQ_DEVICE_BAD_PAGE);
       mbar_arrive(full);
@@ -361,26 +394,32 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       break;
     }
     const int pos_w = t_begin + tile * kT + t0;
-    const int page = pt[(t_begin + tile * kT) / P];
-    const bool tile_ok = page >= 0 && page < a.k.num_pages && page < a.v.num_pages;
+    const bool tile_ok = stage_ok[s] != 0;
     const int n_valid = tile_ok ? max(0, min(16, t_end - pos_w)) : 0;
     if (n_valid > 0) {
+      const bool partial = n_valid < 16;
       const uint32_t st = sbase + s * C::STAGE;
       const uint32_t kst = st, vst = st + C::KROWS + C::KSC;
-      const __half* ksc = reinterpret_cast<const __half*>(smem + s * C::STAGE + C::KROWS);
-      const __half* vsc = reinterpret_cast<const __half*>(smem + s * C::STAGE + C::KROWS + C::KSC + C::VROWS);
+      const uint8_t* ksc = smem + s * C::STAGE + C::KROWS;
+      const uint8_t* vsc = smem + s * C::STAGE + C::KROWS + C::KSC + C::VROWS;
       const int mi = lane >> 3, mr = lane & 7;
 
-      // ---------------- QK^T: S[tok r / r+8][heads 2i, 2i+1]
+      // ---------------- QK^T: S[tok r / r+8][heads 2i, 2i+1] (log2 units after scaling)
       float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (C::KQ) {
-        // per-token block scales of rows r and r+8, times the softmax scale (log2 units)
+        // block scales of rows r and r+8
         float dk[2][C::NB];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
+        for (int rr = 0; rr < 2; ++rr) {
+          uint32_t w[C::NB / 2];
+          load_scale_words<C::NB>(ksc, t0 + r + 8 * rr, w);
 #pragma unroll
-          for (int bb = 0; bb < C::NB; ++bb)
-            dk[rr][bb] = __half2float(ksc[(t0 + r + 8 * rr) * C::NB + bb]) * a.qk_scale_log2;
+          for (int k = 0; k < C::NB / 2; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+            dk[rr][2 * k] = f.x;
+            dk[rr][2 * k + 1] = f.y;
+          }
+        }
         if constexpr (KC == KVQ_CODEC_Q8_0) {
 #pragma unroll
           for (int bb = 0; bb < C::NB; ++bb) {
@@ -430,30 +469,33 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), af[0], af[1], af[2], af[3]);
           mma16816<C::KBF>(sc, af, qf[ks][0], qf[ks][1]);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) sc[k] *= a.qk_scale_log2;
       }
-      const bool v_r = r < n_valid, v_r8 = r + 8 < n_valid;
-      if (!v_r) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
-      if (!v_r8) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sc[k] *= a.qk_scale_log2;
+      if (partial) {
+        if (r >= n_valid) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+        if (r + 8 >= n_valid) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+      }
 
       // ---------------- V scales of this lane's PV tokens (2i, 2i+1, 2i+8, 2i+9)
       const int tk[4] = {2 * i4, 2 * i4 + 1, 2 * i4 + 8, 2 * i4 + 9};
-      float dv[4][C::NB];
-      int ex_lane = -127;   // dmax < 2^ex_lane over this lane's tokens
+      uint32_t dvw[4][C::NB / 2 > 0 ? C::NB / 2 : 1];
+      int ex_lane = 0;   // every scale of this lane's tokens is < 2^ex_lane
       if constexpr (C::VQ) {
-        float dmax = 0.0f;
+        uint32_t mx = 0;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 4; ++u) {
+          load_scale_words<C::NB>(vsc, t0 + tk[u], dvw[u]);
+          if (partial && tk[u] >= n_valid) {
 #pragma unroll
-          for (int bb = 0; bb < C::NB; ++bb) {
-            const float d = tk[u] < n_valid ? __half2float(vsc[(t0 + tk[u]) * C::NB + bb]) : 0.0f;
-            dv[u][bb] = d;
-            dmax = fmaxf(dmax, d);
+            for (int k = 0; k < C::NB / 2; ++k) dvw[u][k] = 0u;
           }
-        if (dmax > 0.0f) ex_lane = (int)((__float_as_uint(dmax) >> 23) & 0xff) - 127 + 1;
-      } else {
-        ex_lane = 0;
+#pragma unroll
+          for (int k = 0; k < C::NB / 2; ++k) mx = __vmaxu2(mx, dvw[u][k]);
+        }
+        const uint32_t hmax = max(mx & 0xffffu, mx >> 16);   // scales are >= 0: bits order as values
+        const int e = (int)(hmax >> 10);
+        ex_lane = hmax ? max(e, 1) - 14 : -127;
       }
 
       // ---------------- lazy online softmax over the warp's 16 tokens (columns = heads)
@@ -488,10 +530,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         m1 = mn1;
         E = E_new;
       }
-      const float p0 = (m0 == -INFINITY) ? 0.0f : fast_exp2(sc[0] - m0);
-      const float p1 = (m1 == -INFINITY) ? 0.0f : fast_exp2(sc[1] - m1);
-      const float p2 = (m0 == -INFINITY) ? 0.0f : fast_exp2(sc[2] - m0);
-      const float p3 = (m1 == -INFINITY) ? 0.0f : fast_exp2(sc[3] - m1);
+      // m0, m1 are finite here: the warp has a valid token, whose score raised them
+      const float p0 = fast_exp2(sc[0] - m0);
+      const float p1 = fast_exp2(sc[1] - m1);
+      const float p2 = fast_exp2(sc[2] - m0);
+      const float p3 = fast_exp2(sc[3] - m1);
       l0 += p0 + p2;
       l1 += p1 + p3;
 
@@ -508,26 +551,30 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         pv[2] = __uint_as_float(__byte_perm(bl, bh, 0x5410));
         pv[3] = __uint_as_float(__byte_perm(bl, bh, 0x7632));
       }
-      const float pscale = __uint_as_float((uint32_t)(127 + kPScale - E) << 23);  // 2^(kPScale - E)
 
       // ---------------- PV
+      const float pscale = __uint_as_float((uint32_t)(127 + kPScale - E) << 23);  // 2^(kPScale - E)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pv[u] *= pscale;
+      // PV column r of an 8-column tile is head r&3's hi part (r < 4) or lo part (r >= 4)
+      // when one n-tile carries both; lo lanes feed x - f16(x) instead of x.
+      const float lo_sel = (C::NPV == 1 && r >= 4) ? 1.0f : 0.0f;
       if constexpr (C::VQ) {
 #pragma unroll
         for (int bb = 0; bb < C::NB; ++bb) {
           float x[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) x[u] = pv[u] * dv[u][bb] * pscale;
-          uint32_t bh0, bl0, bh1, bl1;
-          split2<false>(x[0], x[1], bh0, bl0);
-          split2<false>(x[2], x[3], bh1, bl1);
+          for (int u = 0; u < 4; ++u) {
+            const __half hv = __ushort_as_half((unsigned short)(dvw[u][bb >> 1] >> (16 * (bb & 1))));
+            x[u] = pv[u] * __half2float(hv);
+          }
           uint32_t bf[C::NPV][2];
           if constexpr (C::NPV == 1) {
-            const bool lo = r >= 4;
-            bf[0][0] = lo ? bl0 : bh0;
-            bf[0][1] = lo ? bl1 : bh1;
+            bf[0][0] = hi_or_lo<C::VBF>(x[0], x[1], lo_sel);
+            bf[0][1] = hi_or_lo<C::VBF>(x[2], x[3], lo_sel);
           } else {
-            bf[0][0] = bh0; bf[0][1] = bh1;
-            bf[1][0] = bl0; bf[1][1] = bl1;
+            split2<C::VBF>(x[0], x[1], bf[0][0], bf[1][0]);
+            split2<C::VBF>(x[2], x[3], bf[0][1], bf[1][1]);
           }
           if constexpr (VC == KVQ_CODEC_Q8_0) {
             uint32_t y0, y1, y2, y3;
@@ -559,23 +606,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
       } else {
         // 16-bit V: one B operand for every M-tile; zero the A lanes of tokens past the end
-        float x[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) x[u] = pv[u] * pscale;
-        uint32_t bh0, bl0, bh1, bl1;
-        split2<C::VBF>(x[0], x[1], bh0, bl0);
-        split2<C::VBF>(x[2], x[3], bh1, bl1);
         uint32_t bf[C::NPV][2];
         if constexpr (C::NPV == 1) {
-          const bool lo = r >= 4;
-          bf[0][0] = lo ? bl0 : bh0;
-          bf[0][1] = lo ? bl1 : bh1;
+          bf[0][0] = hi_or_lo<C::VBF>(pv[0], pv[1], lo_sel);
+          bf[0][1] = hi_or_lo<C::VBF>(pv[2], pv[3], lo_sel);
         } else {
-          bf[0][0] = bh0; bf[0][1] = bh1;
-          bf[1][0] = bl0; bf[1][1] = bl1;
+          split2<C::VBF>(pv[0], pv[1], bf[0][0], bf[1][0]);
+          split2<C::VBF>(pv[2], pv[3], bf[0][1], bf[1][1]);
         }
         uint32_t kmask_lo = 0xffffffffu, kmask_hi = 0xffffffffu;
-        if (n_valid < 16) {
+        if (partial) {
           kmask_lo = (tk[0] < n_valid ? 0x0000ffffu : 0u) | (tk[1] < n_valid ? 0xffff0000u : 0u);
           kmask_hi = (tk[2] < n_valid ? 0x0000ffffu : 0u) | (tk[3] < n_valid ? 0xffff0000u : 0u);
         }
@@ -606,8 +646,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
   }
 
-  // ------------------------------------------------------------ merge (a7)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // ------------------------------------------------------------ merge the warps
+
   const int NWT = C::NW * 32;
   if (timed_out) record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
   // every warp reaches the barriers below (a timed-out warp skips only its tiles)
@@ -667,18 +707,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
   const long long head0 = (long long)b * a.num_q_heads + (long long)kvh * G;
   const int gcount = G < 8 * HG ? G : 8 * HG;
-  for (int idx = tid; idx < gcount * D; idx += NWT) {
-    const int h = idx / D, j = idx % D;
-    const int hgi = h >> 3, hl = h & 7;
-    if (hl >= GW) continue;
-    float sum = 0.0f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
-    a.part_o[((head0 + h) * a.n_chunks + chunk) * D + j] = sum;
-  }
+  // per-head (M, l) of the whole CTA
+  float* hml = ml_all + C::NW * 16;     // [16][2]
   for (int h = tid; h < gcount; h += NWT) {
     const int hgi = h >> 3, hl = h & 7;
-    if (hl >= GW) continue;
     float M = -INFINITY;
     for (int w = 0; w < 4; ++w) M = fmaxf(M, ml_all[(hgi * 4 + w) * 16 + hl * 2]);
     float lsum = 0.0f;
@@ -686,9 +718,85 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       const float mw = ml_all[(hgi * 4 + w) * 16 + hl * 2];
       if (mw != -INFINITY) lsum += fast_exp2(mw - M) * ml_all[(hgi * 4 + w) * 16 + hl * 2 + 1];
     }
-    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2] = M;
-    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2 + 1] = lsum;
+    hml[2 * h] = M;
+    hml[2 * h + 1] = lsum;
   }
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+  const int nv = (L + a.chunk_tokens - 1) / a.chunk_tokens;   // CTAs with work for this (b, kvh)
+  if (nv == 1) {
+    // the whole sequence is this chunk: normalize and write the output (no split)
+    for (int idx = tid; idx < gcount * D; idx += NWT) {
+      const int h = idx / D, j = idx % D;
+      const int hgi = h >> 3, hl = h & 7;
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
+      const float lsum = hml[2 * h + 1];
+      a.out[(head0 + h) * D + j] = lsum > 0.0f ? sum / lsum : 0.0f;
+    }
+    return;
+  }
+  // ------------------------------------------------------------ partial write (a7)
+  for (int idx = tid; idx < gcount * D; idx += NWT) {
+    const int h = idx / D, j = idx % D;
+    const int hgi = h >> 3, hl = h & 7;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
+    a.part_o[((head0 + h) * a.n_chunks + chunk) * D + j] = sum;
+  }
+  for (int h = tid; h < gcount; h += NWT) {
+    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2] = hml[2 * h];
+    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2 + 1] = hml[2 * h + 1];
+  }
+
+  // ------------------------------------------------------------ split-K combine (a8)
+  // The last CTA of this (sequence, KV head) to finish merges every chunk's partials,
+  // in chunk order, while they are still in L2.  Arrival is counted with an atomic in
+  // the workspace; the last CTA returns the counter to zero for the next call.
+  __threadfence();
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+  volatile int* last_flag = stage_ok + 4;
+  if (tid == 0) {
+    const unsigned old = atomicAdd(&a.counters[(long long)b * a.k.num_kv_heads + kvh], 1u);
+    if (old >= (unsigned)nv) record_fault(a.k.status, KVQ_DEVICE_BAD_WORKSPACE);
+    *last_flag = (old == (unsigned)nv - 1) ? 1 : 0;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+  if (!*last_flag) return;
+  __threadfence();
+  constexpr int DPL = D / 32;   // dims per lane
+  for (int h = warp; h < gcount; h += C::NW) {
+    const long long head = head0 + h;
+    const float* ml = a.part_ml + head * a.n_chunks * 2;
+    const float* po = a.part_o + head * a.n_chunks * D + lane * DPL;
+    float M = -INFINITY, den = 0.0f, acc[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.0f;
+    for (int c = 0; c < nv; ++c) {
+      const float2 mlc = __ldcg(reinterpret_cast<const float2*>(ml + 2 * c));
+      if (mlc.x == -INFINITY) continue;
+      if (mlc.x > M) {
+        const float f = fast_exp2(M - mlc.x);   // 0 when M = -inf
+        den *= f;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[k] *= f;
+        M = mlc.x;
+      }
+      const float w = fast_exp2(mlc.x - M);
+      den = fmaf(w, mlc.y, den);
+#pragma unroll
+      for (int k = 0; k < DPL; k += 2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(po + (long long)c * D + k));
+        acc[k] = fmaf(w, v.x, acc[k]);
+        acc[k + 1] = fmaf(w, v.y, acc[k + 1]);
+      }
+    }
+    const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) a.out[head * D + lane * DPL + k] = acc[k] * inv;
+  }
+  if (tid == 0) a.counters[(long long)b * a.k.num_kv_heads + kvh] = 0u;
 }
 
 template <int KC, int VC, int D, int GW, int HG>

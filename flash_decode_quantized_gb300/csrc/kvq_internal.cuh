@@ -7,7 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kvq.h"
+#include "kvq.h"
 
 struct kvq_store {
   CUtensorMap rows_map;  // TMA map of the row data: {row_bytes, page_size, kv_heads, pages}
@@ -78,6 +78,7 @@ struct DecodeArgs {
   int n_chunks;                // chunks per (sequence, kv head)
   float* part_o;               // [B][Hq][n_chunks][D]
   float* part_ml;              // [B][Hq][n_chunks][2]  (running max in log2 units, sum)
+  unsigned* counters;          // [B][Hkv] chunk arrival counters (zero between calls)
   float* out;                  // [B][Hq][D]
 };
 

@@ -19,7 +19,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so"
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_DEVICE_FAULT, \
     KVQ_ERR_WORKSPACE = range(6)
 CODECS = {"bf16": 0, "f16": 1, "q8_0": 2, "q4s": 3}
-DEVICE_FAULTS = {0: "ok", 1: "bad_page", 2: "bad_position", 3: "bad_seq_len", 4: "timeout"}
+DEVICE_FAULTS = {0: "ok", 1: "bad_page", 2: "bad_position", 3: "bad_seq_len", 4: "timeout",
+                 5: "bad_workspace"}
 
 
 class KvqError(RuntimeError):
@@ -58,6 +59,7 @@ def _load():
         "kvq_flash_decode": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
                              ctypes.POINTER(DecodeOpts), P, Z, V],
         "kvq_store_get_error": [P, ctypes.POINTER(ctypes.c_int32)],
+        "kvq_decode_workspace_init": [P, Z, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -200,7 +202,7 @@ def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: 
         out = torch.empty((bsz, hq, dim), dtype=torch.float32, device=q.device)
     need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq, max_len_hint, chunk_tokens, variant)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
     _check(lib.kvq_flash_decode(_ptr(q, torch.bfloat16, "q"), k_store.handle, v_store.handle,
                                 _ptr(seq_lens, torch.int32, "seq_lens"),
@@ -210,6 +212,12 @@ def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: 
                                 _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                 _stream(stream)), "kvq_flash_decode")
     return out
+
+
+def kvq_decode_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    """Zeroes a decode workspace (required once before its first use)."""
+    _check(lib.kvq_decode_workspace_init(_ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                         _stream(stream)), "kvq_decode_workspace_init")
 
 
 def kvq_store_get_error(store: Store) -> int:

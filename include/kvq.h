@@ -74,8 +74,10 @@ enum {
   KVQ_DEVICE_BAD_POSITION = 2,  /* append position outside [0, max_pages*page_size) */
   KVQ_DEVICE_BAD_SEQ_LEN = 3,   /* sequence length < 0, past the page table, or past
                                    the max_len_hint that sized the decode split */
-  KVQ_DEVICE_TIMEOUT = 4        /* a kernel's bounded wait for its own tile copies ran
+  KVQ_DEVICE_TIMEOUT = 4,       /* a kernel's bounded wait for its own tile copies ran
                                    out; the kernel stopped and its outputs are invalid */
+  KVQ_DEVICE_BAD_WORKSPACE = 5  /* the workspace's arrival counters were not zero at the
+                                   start of a decode (see kvq_decode_workspace_init) */
 };
 
 /* Shape of one store.  head_dim in {64, 128, 256}; page_size a multiple of 64 in
@@ -133,7 +135,9 @@ kvq_status kvq_append(kvq_store* store, const void* rows, int n_new, int batch,
 kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
 
 /* Device workspace bytes a kvq_flash_decode call with the same stores, batch, head
- * count, max_len_hint and options needs (the split depends on both stores' codecs). */
+ * count, max_len_hint and options needs (the split depends on both stores' codecs).
+ * The workspace holds the split-K partials and, at its end, one arrival counter per
+ * (sequence, KV head). */
 kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store* v_store,
                                       int batch, int num_q_heads, int max_len_hint,
                                       const kvq_decode_opts* opts, size_t* bytes);
@@ -148,9 +152,14 @@ kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store*
  *   softmax_scale <= 0 selects 1/sqrt(head_dim).
  *   max_len_hint: host-side upper bound of seq_lens, used to size the split without a
  *   device round trip; a longer sequence is truncated and recorded as a device fault.
- *   workspace: device memory of at least kvq_decode_workspace_bytes bytes, 256-byte
- *   aligned; its contents need no initialisation.
+ *   workspace: device memory of at least kvq_decode_workspace_bytes bytes, 16-byte
+ *   aligned, zeroed once before its first use (kvq_decode_workspace_init); calls that
+ *   share a workspace must not overlap on the device.
  * A sequence of length 0 yields zeros. */
+/* Zero a decode workspace (its arrival counters must be zero before its first use;
+ * every completed kvq_flash_decode leaves them zero again).  Enqueued on `stream`. */
+kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
 kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_store* v_store,
                             const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                             kvq_codec codec, float* out, int batch, int num_q_heads,

@@ -142,3 +142,36 @@ def test_stale_rows_past_length_are_ignored(variant):
     got = out.cpu().numpy()
     assert np.all(np.isfinite(got))
     assert_close(got, oracle_out(inp, "bf16", "bf16"), "stale NaN rows")
+
+
+def test_workspace_counters_return_to_zero():
+    # the split-K merge counts arrivals in the workspace; each call must leave it reusable
+    inp = make_inputs([5000, 3000], 16, 4, 128, seed=21)
+    k = kvq()
+    ks = build_store(inp, "q8_0", "k")
+    vs = build_store(inp, "q8_0", "v")
+    q, sl, pt = device_inputs(inp)
+    need = k.kvq_decode_workspace_bytes(ks, vs, 2, 16, 5000, chunk_tokens=256)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    k.kvq_decode_workspace_init(ws)
+    outs = [k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=5000, workspace=ws,
+                               chunk_tokens=256).cpu().numpy() for _ in range(3)]
+    assert k.kvq_store_get_error(ks) == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert_close(outs[0], oracle_out(inp, "q8_0", "q8_0"), "reused workspace")
+
+
+def test_dirty_workspace_is_reported():
+    inp = make_inputs([3000], 8, 2, 128, seed=22)
+    k = kvq()
+    ks = build_store(inp, "q8_0", "k")
+    vs = build_store(inp, "q8_0", "v")
+    q, sl, pt = device_inputs(inp)
+    need = k.kvq_decode_workspace_bytes(ks, vs, 1, 8, 3000, chunk_tokens=256)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=3000, workspace=ws, chunk_tokens=256)
+    assert k.kvq_store_get_error(ks) == 5
+    k.kvq_decode_workspace_init(ws)
+    out = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=3000, workspace=ws, chunk_tokens=256)
+    assert k.kvq_store_get_error(ks) == 0
+    assert_close(out.cpu().numpy(), oracle_out(inp, "q8_0", "q8_0"), "after re-init")
