@@ -153,18 +153,24 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Plan {
   int chunk_tokens;
   int n_chunks;
+  int n_groups;
   int variant;
-  size_t o_bytes;
-  size_t ml_off;
-  size_t cnt_off;
+  size_t ml_off;     // chunk partials: o at 0, (m, l) at ml_off
+  size_t go_off;     // group partials: o at go_off, (m, l) at gml_off
+  size_t gml_off;
+  size_t cnt_off;    // unit counters, then group counters
   size_t total;
 };
 
 // Split planner (step a2).  A pure function of its arguments and the device (SM count,
-// resident CTAs per SM of the chosen kernel).  With the default chunk length it fills
-// whole waves: batch * kv_heads * n_chunks CTAs for the longest sequence come to about
-// one wave of resident CTAs (or more whole waves when one wave would need chunks longer
-// than 4096 tokens), with chunks of at least 128 tokens.  It sizes the partials workspace.
+// resident CTAs per SM of the chosen kernel).  The default split gives each (sequence,
+// KV head) n_chunks = slots / units CTAs, where slots = SMs x resident CTAs per SM and
+// units = batch x kv_heads, so the longest sequence fills one wave; chunk_tokens =
+// ceil(max_len / n_chunks) rounded up to 64 is the number of tokens a CTA covers (the
+// tensor-core kernel deals the 64-token tiles to its CTAs round-robin).  When units
+// outnumber slots, chunks are capped at 1024 tokens so long sequences still spread.
+// It sizes the workspace: chunk partials, group partials (groups of kMergeGroup chunks)
+// and the arrival counters of the merge.
 kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_q_heads,
                      int max_len_hint, const kvq_decode_opts* opts, Plan* p) {
   const int hint = max_len_hint > 0 ? max_len_hint : 1;
@@ -180,24 +186,24 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
                                        : 2;
     const long long units = (long long)batch * k->desc.num_kv_heads;
     const long long slots = (long long)sms * per_sm;
-    long long waves = 1, c = 0;
-    for (;; ++waves) {
-      const long long want = (slots * waves + units - 1) / units;   // chunks per unit
-      c = (hint + want - 1) / want;
-      if (c <= 4096 || waves >= 64) break;
-    }
+    const long long want = slots >= units ? slots / units : 1;   // chunks per unit
+    long long c = (hint + want - 1) / want;
     c = (c + 63) / 64 * 64;
     if (c < 128) c = 128;
+    if (units > slots && c > 1024) c = 1024;
     chunk = (int)c;
   }
   p->chunk_tokens = chunk;
   p->n_chunks = (hint + chunk - 1) / chunk;
+  p->n_groups = (p->n_chunks + kMergeGroup - 1) / kMergeGroup;
   const size_t D = (size_t)k->desc.head_dim;
-  const size_t heads = (size_t)batch * num_q_heads * p->n_chunks;
-  p->o_bytes = round_up(heads * D * sizeof(float), 256);
-  p->ml_off = p->o_bytes;
-  p->cnt_off = p->ml_off + round_up(heads * 2 * sizeof(float), 256);
-  p->total = p->cnt_off + round_up((size_t)batch * k->desc.num_kv_heads * sizeof(unsigned), 256);
+  const size_t heads = (size_t)batch * num_q_heads;
+  const size_t units = (size_t)batch * k->desc.num_kv_heads;
+  p->ml_off = round_up(heads * p->n_chunks * D * sizeof(float), 256);
+  p->go_off = p->ml_off + round_up(heads * p->n_chunks * 2 * sizeof(float), 256);
+  p->gml_off = p->go_off + round_up(heads * p->n_groups * D * sizeof(float), 256);
+  p->cnt_off = p->gml_off + round_up(heads * p->n_groups * 2 * sizeof(float), 256);
+  p->total = p->cnt_off + round_up(units * (1 + p->n_groups) * sizeof(unsigned), 256);
   return KVQ_OK;
 }
 
@@ -315,7 +321,7 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   if (p.variant == 1 && !sfn) return KVQ_ERR_UNSUPPORTED;
   if (p.variant == 2 && (!mfn || !k_store->rows_map_ok || !v_store->rows_map_ok)) return KVQ_ERR_UNSUPPORTED;
 
-  DecodeArgs a;
+  DecodeArgs a = {};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = view_of(k_store);
   a.v = view_of(v_store);
@@ -330,8 +336,13 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   a.chunk_tokens = p.chunk_tokens;
   a.n_chunks = p.n_chunks;
   a.part_o = static_cast<float*>(workspace);
-  a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + p.ml_off);
-  a.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(workspace) + p.cnt_off);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.part_ml = reinterpret_cast<float*>(ws + p.ml_off);
+  a.gpart_o = reinterpret_cast<float*>(ws + p.go_off);
+  a.gpart_ml = reinterpret_cast<float*>(ws + p.gml_off);
+  a.n_groups = p.n_groups;
+  a.counters = reinterpret_cast<unsigned*>(ws + p.cnt_off);
+  a.grp_counter_off = (long long)batch * kd.num_kv_heads;
   a.out = out;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.variant == 2)  // the tensor-core kernel merges the split itself (last CTA per unit)

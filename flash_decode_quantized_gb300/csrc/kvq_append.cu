@@ -103,6 +103,14 @@ cudaError_t launch_codec(const kvq_store* s, const __nv_bfloat16* rows, int n_ne
   const long long n_rows = (long long)batch * n_new * s->desc.num_kv_heads;
   const unsigned grid = (unsigned)((n_rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
   const StoreView v = view_of(s);
+  // same carveout as the decode kernels, so a step's kernels run without reconfiguring
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaFuncSetAttribute(append_kernel<CODEC, 2>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(append_kernel<CODEC, 4>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(append_kernel<CODEC, 8>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    carveout_set = true;
+  }
   switch (s->desc.head_dim) {
     case 64:
       append_kernel<CODEC, 2><<<grid, kWarpsPerBlock * 32, 0, stream>>>(v, rows, n_new, batch, seq_lens, page_table, max_pages);

@@ -130,16 +130,23 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t x, uint32_t y) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&y));
   return *reinterpret_cast<uint32_t*>(&r);
 }
-// Signed bytes packed in `u_biased` (each byte already XORed with 0x80, i.e. b + 128)
-// to an exact f16 pair, selecting the two bytes named by `sel` (0x4X4Y picks X, Y).
-// Magic-number conversion: f16 bits 0x64 << 8 | u encode 1024 + u; subtract 1152.
-__device__ __forceinline__ uint32_t i8pair_f16(uint32_t u_biased, uint32_t sel) {
-  return hsub2_u32(__byte_perm(u_biased, 0x64646464u, sel), 0x64806480u);
+// Magic-number conversion of integer codes to f16: the bits 0x64 << 8 | u encode the
+// f16 value 1024 + u exactly (u < 1024).  The constant offset is not subtracted per
+// element; the MMAs remove it (see kBias8 / kBias4).
+//
+// Signed bytes packed in `u_biased` (each byte already XORed with 0x80, i.e. q + 128)
+// to the f16 pair (1152 + q) of the two bytes named by `sel` (0x4X4Y picks bytes X, Y).
+__device__ __forceinline__ uint32_t i8pair_raw(uint32_t u_biased, uint32_t sel) {
+  return __byte_perm(u_biased, 0x64646464u, sel);
 }
-// Nibble pair (bits 0-3 and 16-19 of w) holding u = q + 8 -> exact f16 pair of q.
-__device__ __forceinline__ uint32_t u4pair_f16(uint32_t w) {
-  return hsub2_u32((w & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+// Nibble pair (bits 0-3 and 16-19 of w) holding u = q + 8 -> the f16 pair (1032 + q).
+__device__ __forceinline__ uint32_t u4pair_raw(uint32_t w) {
+  return (w & 0x000F000Fu) | 0x64006400u;
 }
+constexpr float kBias8 = 1152.0f;            // offset of i8pair_raw values
+constexpr float kBias4 = 1032.0f;            // offset of u4pair_raw values
+constexpr uint32_t kNegBias8 = 0xE480E480u;  // f16 pair (-1152, -1152)
+constexpr uint32_t kNegBias4 = 0xE408E408u;  // f16 pair (-1032, -1032)
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -219,7 +226,8 @@ struct Cfg {
   static constexpr int RING = NS * STAGE > OBUF ? NS * STAGE : OBUF;
   static constexpr int BAR_OFF = RING;                    // 2*NS mbarriers
   static constexpr int OK_OFF = BAR_OFF + 2 * NS * 8;     // per-stage "tile is valid" flags
-  static constexpr int ML_OFF = OK_OFF + 32;              // per-warp m, l [8][2]
+  static constexpr int KB_OFF = OK_OFF + 32;              // QK accumulator seeds [HG][NB][4] f32x2
+  static constexpr int ML_OFF = KB_OFF + HG * NB * 4 * 8; // per-warp m, l [8][2]
   static constexpr int SMEM = ML_OFF + (NW + 2) * 16 * 4 + 1024;  // + per-head (M, l); +1024: alignment
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
@@ -255,6 +263,113 @@ __device__ __forceinline__ int pv_dim(int mt, int row) {
   else return 16 * mt + row;
 }
 
+// ---------------------------------------------------------------- split-K merge helpers
+
+constexpr int kGroup = kMergeGroup;
+
+// Publishes this CTA's writes, counts its arrival on `counter` and tells whether it is the
+// last of `expected` arrivals (all threads get the answer).  The last CTA sees every
+// other CTA's published writes.
+__device__ __forceinline__ bool arrive_last(unsigned* counter, int expected, int tid, int nthreads,
+                                            volatile int* flag, int32_t* status) {
+  __threadfence();
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  if (tid == 0) {
+    const unsigned old = atomicAdd(counter, 1u);
+    if (old >= (unsigned)expected) record_fault(status, KVQ_DEVICE_BAD_WORKSPACE);
+    *flag = (old == (unsigned)expected - 1) ? 1 : 0;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  const bool last = *flag != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// Merges `count` split-K partials of each of `gcount` consecutive heads:
+//   M = max_c m_c, l = sum_c 2^(m_c - M) l_c, O = sum_c 2^(m_c - M) O_c.
+// Head h's partial c sits at ml[(h * stride + c) * 2] and o[(h * stride + c) * D].
+// With `final` the normalized output O / l goes to out[h * D]; otherwise (M, l, O) go
+// to out_ml[h * out_stride * 2] / out_o[h * out_stride * D].  Weights are staged in
+// shared memory when they fit; every thread of the CTA takes part.
+template <int D, int NW>
+__device__ void merge_partials(const float* ml, const float* o, long long stride, int count, int gcount,
+                               bool final, float* wbuf, long long wcap, float* hml, int tid, int warp,
+                               int lane, float* out_ml, float* out_o, long long out_stride, float* out) {
+  const int nthreads = NW * 32;
+  const bool wfit = (long long)gcount * count <= wcap;
+  for (int h = warp; h < gcount; h += NW) {
+    const float* m_h = ml + h * stride * 2;
+    float M = -INFINITY;
+    for (int c = lane; c < count; c += 32) M = fmaxf(M, __ldcg(m_h + 2 * c));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float den = 0.0f;
+    for (int c = lane; c < count; c += 32) {
+      const float2 mlc = __ldcg(reinterpret_cast<const float2*>(m_h + 2 * c));
+      const float w = (mlc.x == -INFINITY) ? 0.0f : fast_exp2(mlc.x - M);
+      den = fmaf(w, mlc.y, den);
+      if (wfit) wbuf[h * count + c] = w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    if (lane == 0) {
+      hml[2 * h] = M;
+      hml[2 * h + 1] = den;
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+  constexpr int D4 = D / 4;
+  for (int item = tid; item < gcount * D4; item += nthreads) {
+    const int h = item / D4, col = item % D4;
+    const float* m_h = ml + h * stride * 2;
+    const float4* o_h = reinterpret_cast<const float4*>(o + h * stride * D) + col;
+    const float M = hml[2 * h];
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    auto weight = [&](int c) -> float {
+      if (wfit) return wbuf[h * count + c];
+      const float m = __ldcg(m_h + 2 * c);
+      return (m == -INFINITY) ? 0.0f : fast_exp2(m - M);
+    };
+    int c = 0;
+    for (; c + 8 <= count; c += 8) {
+      float4 v[8];
+      float w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        v[u] = __ldcg(o_h + (long long)(c + u) * D4);
+        w[u] = weight(c + u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x = fmaf(w[u], v[u].x, acc.x);
+        acc.y = fmaf(w[u], v[u].y, acc.y);
+        acc.z = fmaf(w[u], v[u].z, acc.z);
+        acc.w = fmaf(w[u], v[u].w, acc.w);
+      }
+    }
+    for (; c < count; ++c) {
+      const float4 v = __ldcg(o_h + (long long)c * D4);
+      const float w = weight(c);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (final) {
+      const float den = hml[2 * h + 1];
+      const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+      reinterpret_cast<float4*>(out + h * D)[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      reinterpret_cast<float4*>(out_o + h * out_stride * D)[col] = acc;
+      if (col == 0) {
+        out_ml[h * out_stride * 2] = M;
+        out_ml[h * out_stride * 2 + 1] = hml[2 * h + 1];
+      }
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------- kernel
 
 template <int KC, int VC, int D, int GW, int HG>
@@ -276,6 +391,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   const int G = a.group;
   const int P = a.k.page_size;
 
+  if (tid == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+  }
   const long long cap = min((long long)a.max_pages * P, (long long)a.n_chunks * a.chunk_tokens);
   long long Lraw = a.seq_lens[b];
   if (Lraw < 0 || Lraw > cap) {
@@ -286,16 +405,18 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     Lraw = Lraw < 0 ? 0 : cap;
   }
   const int L = (int)Lraw;
-  const int t_begin = chunk * a.chunk_tokens;
-  if (t_begin >= L) {
+  // The sequence's 64-token tiles are dealt round-robin to its n_chunks CTAs: CTA c
+  // takes tiles c, c + n_chunks, ... so that every CTA streams from all of the
+  // sequence's pages (evens out per-CTA speed) and all finish together.
+  const int NT = (L + kT - 1) / kT;                 // tiles of the sequence
+  if (chunk >= NT) {
     if (L == 0 && chunk == 0) {  // empty sequence: its heads' outputs are zero
       const long long h0 = (long long)b * a.num_q_heads + (long long)kvh * G;
       for (int idx = tid; idx < G * D; idx += C::THREADS) a.out[h0 * D + idx] = 0.0f;
     }
     return;
   }
-  const int t_end = min(L, t_begin + a.chunk_tokens);
-  const int n_tiles = (t_end - t_begin + kT - 1) / kT;
+  const int n_tiles = (NT - chunk + a.n_chunks - 1) / a.n_chunks;
   const int32_t* pt = a.page_table + (long long)b * a.max_pages;
 
   if (tid == 0) {
@@ -312,7 +433,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   // into stage k % NS as soon as every warp has released tile k.
   auto issue_tile = [&](int tile) {
     const int s = tile % C::NS;
-    const int pos0 = t_begin + tile * kT;
+    const int pos0 = (chunk + tile * a.n_chunks) * kT;
     const int page = pt[pos0 / P];
     const int row0 = pos0 % P;
     const uint32_t full = bar_full + 8 * s;
@@ -375,6 +496,34 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
   }
 
+  // Per block: -bias * sum_j q[h, j] for the S columns 2i, 2i+1 of this lane (zero for
+  // 16-bit K), the seed of the block's QK accumulator.  Summed from the f16 values the
+  // MMA multiplies; lanes r = n hold column n's B operand, so column n's sum comes from
+  // lane 4n after a quad reduction.
+  // Kept in shared memory ([head group][block][i4], float2): every lane of a head group
+  // with the same i4 needs the same pair.
+  float2* kbs = reinterpret_cast<float2*>(smem + C::KB_OFF);
+#pragma unroll
+  for (int bb = 0; bb < C::NB; ++bb) {
+    float part = 0.0f;
+    if constexpr (C::KQ) {
+#pragma unroll
+      for (int st = 2 * bb; st < 2 * bb + 2; ++st)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const float2 f = unpack2<false>(qf[st][half]);
+          part += f.x + f.y;
+        }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+    }
+    const float bias = KC == KVQ_CODEC_Q4S ? kBias4 : kBias8;
+    const float k0 = -bias * __shfl_sync(0xffffffffu, part, 4 * (2 * i4));
+    const float k1 = -bias * __shfl_sync(0xffffffffu, part, 4 * (2 * i4 + 1));
+    if (ws == 0 && r == 0) kbs[(hg * C::NB + bb) * 4 + i4] = make_float2(k0, k1);
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(C::THREADS) : "memory");
+
   float o[C::QSTEPS][C::NPV][4];   // O^T accumulators: D/16 M-tiles x NPV n-tiles
 #pragma unroll
   for (int mt = 0; mt < C::QSTEPS; ++mt)
@@ -393,9 +542,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       timed_out = true;
       break;
     }
-    const int pos_w = t_begin + tile * kT + t0;
+    const int pos_w = (chunk + tile * a.n_chunks) * kT + t0;
     const bool tile_ok = stage_ok[s] != 0;
-    const int n_valid = tile_ok ? max(0, min(16, t_end - pos_w)) : 0;
+    const int n_valid = tile_ok ? max(0, min(16, L - pos_w)) : 0;
     if (n_valid > 0) {
       const bool partial = n_valid < 16;
       const uint32_t st = sbase + s * C::STAGE;
@@ -426,13 +575,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             uint32_t x0, x1, x2, x3;
             ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * bb + (mi >> 1)), x0, x1, x2, x3);
             x0 ^= 0x80808080u; x1 ^= 0x80808080u; x2 ^= 0x80808080u; x3 ^= 0x80808080u;
-            float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // accumulator seeded with -1152 * sum(q) of the block: removes the code offset
+            const float2 kb = kbs[(hg * C::NB + bb) * 4 + i4];
+            float cb[4] = {kb.x, kb.y, kb.x, kb.y};
             uint32_t af[4];
-            af[0] = i8pair_f16(x0, 0x4140); af[1] = i8pair_f16(x1, 0x4140);
-            af[2] = i8pair_f16(x0, 0x4342); af[3] = i8pair_f16(x1, 0x4342);
+            af[0] = i8pair_raw(x0, 0x4140); af[1] = i8pair_raw(x1, 0x4140);
+            af[2] = i8pair_raw(x0, 0x4342); af[3] = i8pair_raw(x1, 0x4342);
             mma16816<false>(cb, af, qf[2 * bb][0], qf[2 * bb][1]);
-            af[0] = i8pair_f16(x2, 0x4140); af[1] = i8pair_f16(x3, 0x4140);
-            af[2] = i8pair_f16(x2, 0x4342); af[3] = i8pair_f16(x3, 0x4342);
+            af[0] = i8pair_raw(x2, 0x4140); af[1] = i8pair_raw(x3, 0x4140);
+            af[2] = i8pair_raw(x2, 0x4342); af[3] = i8pair_raw(x3, 0x4342);
             mma16816<false>(cb, af, qf[2 * bb + 1][0], qf[2 * bb + 1][1]);
             sc[0] = fmaf(dk[0][bb], cb[0], sc[0]);
             sc[1] = fmaf(dk[0][bb], cb[1], sc[1]);
@@ -447,13 +598,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const uint32_t ra = x[2 * h2], rb = x[2 * h2 + 1];  // rows r and r+8 of block bb+h2
-              float cb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+              const float2 kb = kbs[(hg * C::NB + bb + h2) * 4 + i4];
+              float cb[4] = {kb.x, kb.y, kb.x, kb.y};
               uint32_t af[4];
-              af[0] = u4pair_f16(ra); af[1] = u4pair_f16(rb);
-              af[2] = u4pair_f16(ra >> 4); af[3] = u4pair_f16(rb >> 4);
+              af[0] = u4pair_raw(ra); af[1] = u4pair_raw(rb);
+              af[2] = u4pair_raw(ra >> 4); af[3] = u4pair_raw(rb >> 4);
               mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
-              af[0] = u4pair_f16(ra >> 8); af[1] = u4pair_f16(rb >> 8);
-              af[2] = u4pair_f16(ra >> 12); af[3] = u4pair_f16(rb >> 12);
+              af[0] = u4pair_raw(ra >> 8); af[1] = u4pair_raw(rb >> 8);
+              af[2] = u4pair_raw(ra >> 12); af[3] = u4pair_raw(rb >> 12);
               mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
               sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
               sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);
@@ -581,26 +733,54 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             // matrices: (tok 0-7, chunk 2b), (tok 0-7, chunk 2b+1), (tok 8-15, 2b), (tok 8-15, 2b+1)
             ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * bb + (mi & 1)), y0, y1, y2, y3);
             y0 ^= 0x80808080u; y1 ^= 0x80808080u; y2 ^= 0x80808080u; y3 ^= 0x80808080u;
-            uint32_t ae[4] = {i8pair_f16(y0, 0x4240), i8pair_f16(y1, 0x4240), i8pair_f16(y2, 0x4240),
-                              i8pair_f16(y3, 0x4240)};
-            uint32_t ao[4] = {i8pair_f16(y0, 0x4341), i8pair_f16(y1, 0x4341), i8pair_f16(y2, 0x4341),
-                              i8pair_f16(y3, 0x4341)};
+            uint32_t ae[4] = {i8pair_raw(y0, 0x4240), i8pair_raw(y1, 0x4240), i8pair_raw(y2, 0x4240),
+                              i8pair_raw(y3, 0x4240)};
+            uint32_t ao[4] = {i8pair_raw(y0, 0x4341), i8pair_raw(y1, 0x4341), i8pair_raw(y2, 0x4341),
+                              i8pair_raw(y3, 0x4341)};
+            if constexpr (C::NPV == 1) {
+              // (1152 + v) P, then -1152 P: the code offset cancels in the accumulator
+              const uint32_t an[4] = {kNegBias8, kNegBias8, kNegBias8, kNegBias8};
+              mma16816<false>(o[2 * bb][0], ae, bf[0][0], bf[0][1]);
+              mma16816<false>(o[2 * bb][0], an, bf[0][0], bf[0][1]);
+              mma16816<false>(o[2 * bb + 1][0], ao, bf[0][0], bf[0][1]);
+              mma16816<false>(o[2 * bb + 1][0], an, bf[0][0], bf[0][1]);
+            } else {
+              // two n-tiles share the A operand: subtract the offset once in registers
 #pragma unroll
-            for (int n = 0; n < C::NPV; ++n) {
-              mma16816<false>(o[2 * bb][n], ae, bf[n][0], bf[n][1]);
-              mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
+              for (int k = 0; k < 4; ++k) {
+                ae[k] = hsub2_u32(ae[k], 0x64806480u);
+                ao[k] = hsub2_u32(ao[k], 0x64806480u);
+              }
+#pragma unroll
+              for (int n = 0; n < C::NPV; ++n) {
+                mma16816<false>(o[2 * bb][n], ae, bf[n][0], bf[n][1]);
+                mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
+              }
             }
           } else {  // q4s: matrices (tok 0-7, chunk b), (tok 8-15, chunk b) for this block
             uint32_t y0, y1, y2, y3;
             ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, (bb & ~1) + (mi >> 1)), y0, y1, y2, y3);
             const uint32_t ya = (bb & 1) ? y2 : y0, yb = (bb & 1) ? y3 : y1;
-            uint32_t a01[4] = {u4pair_f16(ya), u4pair_f16(ya >> 4), u4pair_f16(yb), u4pair_f16(yb >> 4)};
-            uint32_t a23[4] = {u4pair_f16(ya >> 8), u4pair_f16(ya >> 12), u4pair_f16(yb >> 8),
-                               u4pair_f16(yb >> 12)};
+            uint32_t a01[4] = {u4pair_raw(ya), u4pair_raw(ya >> 4), u4pair_raw(yb), u4pair_raw(yb >> 4)};
+            uint32_t a23[4] = {u4pair_raw(ya >> 8), u4pair_raw(ya >> 12), u4pair_raw(yb >> 8),
+                               u4pair_raw(yb >> 12)};
+            if constexpr (C::NPV == 1) {
+              const uint32_t an[4] = {kNegBias4, kNegBias4, kNegBias4, kNegBias4};
+              mma16816<false>(o[2 * bb][0], a01, bf[0][0], bf[0][1]);
+              mma16816<false>(o[2 * bb][0], an, bf[0][0], bf[0][1]);
+              mma16816<false>(o[2 * bb + 1][0], a23, bf[0][0], bf[0][1]);
+              mma16816<false>(o[2 * bb + 1][0], an, bf[0][0], bf[0][1]);
+            } else {
 #pragma unroll
-            for (int n = 0; n < C::NPV; ++n) {
-              mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
-              mma16816<false>(o[2 * bb + 1][n], a23, bf[n][0], bf[n][1]);
+              for (int k = 0; k < 4; ++k) {
+                a01[k] = hsub2_u32(a01[k], 0x64086408u);
+                a23[k] = hsub2_u32(a23[k], 0x64086408u);
+              }
+#pragma unroll
+              for (int n = 0; n < C::NPV; ++n) {
+                mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
+                mma16816<false>(o[2 * bb + 1][n], a23, bf[n][0], bf[n][1]);
+              }
             }
           }
         }
@@ -722,7 +902,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     hml[2 * h + 1] = lsum;
   }
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
-  const int nv = (L + a.chunk_tokens - 1) / a.chunk_tokens;   // CTAs with work for this (b, kvh)
+  const int nv = min(a.n_chunks, NT);   // CTAs with work for this (b, kvh)
   if (nv == 1) {
     // the whole sequence is this chunk: normalize and write the output (no split)
     for (int idx = tid; idx < gcount * D; idx += NWT) {
@@ -751,59 +931,59 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   }
 
   // ------------------------------------------------------------ split-K combine (a8)
-  // The last CTA of this (sequence, KV head) to finish merges every chunk's partials,
-  // in chunk order, while they are still in L2.  Arrival is counted with an atomic in
-  // the workspace; the last CTA returns the counter to zero for the next call.
-  __threadfence();
-  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+  // Two levels, both done by whichever CTA arrives last (atomic counters in the
+  // workspace, returned to zero by that CTA):
+  //   group: the last of the <= kGroup chunks of a group merges their partials into a
+  //          group partial while the rest of the grid is still streaming;
+  //   unit:  the last group of a (sequence, KV head) merges the group partials into the
+  //          output.  A single group (up to 64 chunks form one) writes the output directly.
+  const long long unit = (long long)b * a.k.num_kv_heads + kvh;
+  const int gsz = nv <= 4 * kGroup ? nv : kGroup;   // up to 64 partials: one level
+  const int ng = (nv + gsz - 1) / gsz;
+  const int g = chunk / gsz;
+  const int g_first = g * gsz;
+  const int g_count = min(gsz, nv - g_first);
   volatile int* last_flag = stage_ok + 4;
-  if (tid == 0) {
-    const unsigned old = atomicAdd(&a.counters[(long long)b * a.k.num_kv_heads + kvh], 1u);
-    if (old >= (unsigned)nv) record_fault(a.k.status, KVQ_DEVICE_BAD_WORKSPACE);
-    *last_flag = (old == (unsigned)nv - 1) ? 1 : 0;
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
-  if (!*last_flag) return;
-  __threadfence();
-  constexpr int DPL = D / 32;   // dims per lane
-  for (int h = warp; h < gcount; h += C::NW) {
-    const long long head = head0 + h;
-    const float* ml = a.part_ml + head * a.n_chunks * 2;
-    const float* po = a.part_o + head * a.n_chunks * D + lane * DPL;
-    float M = -INFINITY, den = 0.0f, acc[DPL];
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) acc[k] = 0.0f;
-    for (int c = 0; c < nv; ++c) {
-      const float2 mlc = __ldcg(reinterpret_cast<const float2*>(ml + 2 * c));
-      if (mlc.x == -INFINITY) continue;
-      if (mlc.x > M) {
-        const float f = fast_exp2(M - mlc.x);   // 0 when M = -inf
-        den *= f;
-#pragma unroll
-        for (int k = 0; k < DPL; ++k) acc[k] *= f;
-        M = mlc.x;
-      }
-      const float w = fast_exp2(mlc.x - M);
-      den = fmaf(w, mlc.y, den);
-#pragma unroll
-      for (int k = 0; k < DPL; k += 2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(po + (long long)c * D + k));
-        acc[k] = fmaf(w, v.x, acc[k]);
-        acc[k + 1] = fmaf(w, v.y, acc[k + 1]);
-      }
-    }
-    const float inv = den > 0.0f ? 1.0f / den : 0.0f;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) a.out[head * D + lane * DPL + k] = acc[k] * inv;
-  }
-  if (tid == 0) a.counters[(long long)b * a.k.num_kv_heads + kvh] = 0u;
+  if (!arrive_last(a.counters + a.grp_counter_off + unit * a.n_groups + g, g_count, tid, NWT, last_flag,
+                   a.k.status))
+    return;
+  // merge this group's chunk partials
+  merge_partials<D, C::NW>(
+      a.part_ml + (head0 * a.n_chunks + g_first) * 2, a.part_o + (head0 * a.n_chunks + g_first) * D,
+      (long long)a.n_chunks, g_count, gcount, ng == 1, obuf, (long long)C::RING / 4, hml, tid, warp, lane,
+      a.gpart_ml + (head0 * a.n_groups + g) * 2, a.gpart_o + (head0 * a.n_groups + g) * D,
+      (long long)a.n_groups, a.out + head0 * D);
+  if (tid == 0) a.counters[a.grp_counter_off + unit * a.n_groups + g] = 0u;
+  if (ng == 1) return;
+  if (!arrive_last(a.counters + unit, ng, tid, NWT, last_flag, a.k.status)) return;
+  merge_partials<D, C::NW>(a.gpart_ml + head0 * a.n_groups * 2, a.gpart_o + head0 * a.n_groups * D,
+                           (long long)a.n_groups, ng, gcount, true, obuf, (long long)C::RING / 4, hml,
+                           tid, warp, lane, nullptr, nullptr, 0, a.out + head0 * D);
+  if (tid == 0) a.counters[unit] = 0u;
+}
+
+// Sets the kernel's shared-memory attributes once per device.
+template <int KC, int VC, int D, int GW, int HG>
+cudaError_t prepare() {
+  using C = Cfg<KC, VC, D, GW, HG>;
+  static unsigned long long done = 0;   // bit per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && (done >> dev) & 1ull) return cudaSuccess;
+  auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_RELAXED);
+  return e;
 }
 
 template <int KC, int VC, int D, int GW, int HG>
 cudaError_t launch(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
   using C = Cfg<KC, VC, D, GW, HG>;
   auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t e = prepare<KC, VC, D, GW, HG>();
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_chunks, a.k.num_kv_heads, a.batch);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(tmk, tmv, a);
@@ -816,7 +996,7 @@ template <int KC, int VC, int D, int GW, int HG>
 int occupancy() {
   using C = Cfg<KC, VC, D, GW, HG>;
   auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return 0;
+  if (prepare<KC, VC, D, GW, HG>() != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM) != cudaSuccess) return 0;
   return n;

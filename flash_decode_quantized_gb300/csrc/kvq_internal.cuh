@@ -24,7 +24,8 @@ struct kvq_store {
 
 namespace kvq {
 
-constexpr int kBlock = 32;  // elements per quantization block
+constexpr int kBlock = 32;       // elements per quantization block
+constexpr int kMergeGroup = 16;  // split-K chunks merged per group partial
 
 __host__ __device__ inline int codec_row_bytes(int codec, int head_dim) {
   return codec == KVQ_CODEC_Q8_0 ? head_dim : codec == KVQ_CODEC_Q4S ? head_dim / 2 : 2 * head_dim;
@@ -78,7 +79,12 @@ struct DecodeArgs {
   int n_chunks;                // chunks per (sequence, kv head)
   float* part_o;               // [B][Hq][n_chunks][D]
   float* part_ml;              // [B][Hq][n_chunks][2]  (running max in log2 units, sum)
-  unsigned* counters;          // [B][Hkv] chunk arrival counters (zero between calls)
+  float* gpart_o;              // [B][Hq][n_groups][D]  group partials of the split
+  float* gpart_ml;             // [B][Hq][n_groups][2]
+  int n_groups;                // groups of chunks per (sequence, kv head)
+  unsigned* counters;          // [B*Hkv] unit counters, then [B*Hkv][n_groups] group
+                               // counters at grp_counter_off (all zero between calls)
+  long long grp_counter_off;
   float* out;                  // [B][Hq][D]
 };
 
