@@ -208,6 +208,22 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
 }
 
 }  // namespace
+
+// Workspace size of a decode call and the offset of its arrival counters (the part a
+// reused workspace must have zeroed before a call).
+kvq_status decode_workspace_layout(const kvq_store* k_store, const kvq_store* v_store, int batch,
+                                   int num_q_heads, int max_len_hint, const kvq_decode_opts* opts,
+                                   size_t* total, size_t* counters_off) {
+  if (!k_store || !v_store || batch < 1 || num_q_heads < 1 || max_len_hint < 0) return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % k_store->desc.num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  Plan p;
+  const kvq_status st = make_plan(k_store, v_store, batch, num_q_heads, max_len_hint, opts, &p);
+  if (st != KVQ_OK) return st;
+  *total = p.total;
+  *counters_off = p.cnt_off;
+  return KVQ_OK;
+}
+
 }  // namespace kvq
 
 using namespace kvq;

@@ -96,5 +96,8 @@ cudaError_t launch_seq_lens_add(int32_t* seq_lens, int batch, int n, cudaStream_
 cudaError_t launch_combine_pdl(const DecodeArgs& a, int head_dim, cudaStream_t stream);
 
 void count_launch();
+kvq_status decode_workspace_layout(const kvq_store* k_store, const kvq_store* v_store, int batch,
+                                   int num_q_heads, int max_len_hint, const kvq_decode_opts* opts,
+                                   size_t* total, size_t* counters_off);
 
 }  // namespace kvq

@@ -60,6 +60,8 @@ def _load():
                              ctypes.POINTER(DecodeOpts), P, Z, V],
         "kvq_store_get_error": [P, ctypes.POINTER(ctypes.c_int32)],
         "kvq_decode_workspace_init": [P, Z, V],
+        "kvq_flash_decode_static_ws": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
+                                       ctypes.POINTER(DecodeOpts), V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -211,6 +213,29 @@ def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: 
                                 int(max_len_hint), _opts(chunk_tokens, variant),
                                 _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                 _stream(stream)), "kvq_flash_decode")
+    return out
+
+
+def kvq_flash_decode_static_ws(q: torch.Tensor, k_store: Store, v_store: Store,
+                               seq_lens: torch.Tensor, page_table: torch.Tensor,
+                               out: torch.Tensor | None = None, softmax_scale: float = 0.0,
+                               max_len_hint: int | None = None, chunk_tokens: int = 0,
+                               variant: int = 0, stream=None) -> torch.Tensor:
+    """kvq_flash_decode whose workspace is the library's fixed device array (no
+    allocation by the library; `out` is allocated here only when not given)."""
+    bsz, hq, dim = q.shape
+    max_pages = page_table.shape[1]
+    if max_len_hint is None:
+        max_len_hint = max_pages * k_store.page_size
+    if out is None:
+        out = torch.empty((bsz, hq, dim), dtype=torch.float32, device=q.device)
+    codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
+    _check(lib.kvq_flash_decode_static_ws(_ptr(q, torch.bfloat16, "q"), k_store.handle, v_store.handle,
+                                          _ptr(seq_lens, torch.int32, "seq_lens"),
+                                          _ptr(page_table, torch.int32, "page_table"), max_pages, codec,
+                                          _ptr(out, torch.float32, "out"), bsz, hq, float(softmax_scale),
+                                          int(max_len_hint), _opts(chunk_tokens, variant), _stream(stream)),
+           "kvq_flash_decode_static_ws")
     return out
 
 

@@ -167,6 +167,26 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
                             const kvq_decode_opts* opts, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* kvq_flash_decode without a workspace argument, for callers that cannot allocate
+ * device memory where they decode (inside host callbacks, under a memory manager that
+ * owns all device memory, or in loops where cudaMalloc's implicit synchronization is
+ * not acceptable).  The pages this library follows have no counterpart of this call.
+ * The workspace is a fixed 16 MiB array in the library's own device memory (one per
+ * GPU that loads the library, held until the process exits).  A call whose
+ * kvq_decode_workspace_bytes would exceed 16 MiB returns KVQ_ERR_WORKSPACE and enqueues
+ * nothing.  The first call on a device looks up the array's address (set-up, a
+ * synchronous runtime query); make that first call before any stream capture.  Every
+ * call zeroes the array's merge counters with an asynchronous memset on `stream`
+ * (no allocation).  All calls share the one array, so calls that overlap on the device
+ * (other streams, concurrent graphs) race; serialize them.  Other arguments, results
+ * and errors are those of kvq_flash_decode. */
+kvq_status kvq_flash_decode_static_ws(const void* q, const kvq_store* k_store,
+                                      const kvq_store* v_store, const int32_t* seq_lens,
+                                      const int32_t* page_table, int max_pages, kvq_codec codec,
+                                      float* out, int batch, int num_q_heads,
+                                      float softmax_scale, int max_len_hint,
+                                      const kvq_decode_opts* opts, void* stream);
+
 /* Wait for the device, read and clear the store's status word.  *device_code receives
  * the first recorded fault (KVQ_DEVICE_*), or 0.  Returns KVQ_ERR_DEVICE_FAULT when a
  * fault was recorded, KVQ_OK otherwise.  The only call that synchronizes. */
