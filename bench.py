@@ -1,8 +1,9 @@
 """Benchmark: decode-attention µs per layer-step and effective KV GB/s (% of HBM peak).
 
 One step = one pass of the whole hot path on one layer: on-device encode of the new K and
-V row into the resident store (kvq_append x2), seq_lens += 1, and the split-K fused
-dequant flash-decode (kvq_flash_decode: decode kernel + combine kernel).  The store grows
+V row into the resident store with seq_lens += 1 (kvq_append_kv, one launch), and the
+split-K fused dequant flash-decode (kvq_flash_decode, one launch for the tensor-core
+kernel, whose last CTAs also merge the split).  The store grows
 by one token per step.  Inputs are resident in HBM when the timed region starts; the L2
 is flushed before every timed step by reading a 2 x L2 buffer (leaving clean lines, so
 the timed kernel pays no write-back), outside its events, with a bounded ~100 µs GPU
@@ -221,10 +222,10 @@ class Layer:
         self.variant, self.chunk = variant, chunk_tokens
 
     def append(self, new_k=None, new_v=None):
-        kvq = self.kvq
-        kvq.kvq_append(self.k_store, self.new_k if new_k is None else new_k, self.seq_lens, self.page_table)
-        kvq.kvq_append(self.v_store, self.new_v if new_v is None else new_v, self.seq_lens, self.page_table)
-        kvq.kvq_seq_lens_add(self.seq_lens, 1)
+        # one launch: encode the step's K and V rows, then seq_lens += 1
+        self.kvq.kvq_append_kv(self.k_store, self.v_store, self.new_k if new_k is None else new_k,
+                               self.new_v if new_v is None else new_v, self.seq_lens, self.page_table,
+                               advance=True)
         self.host_lens = [L + 1 for L in self.host_lens]
 
     def decode(self, q=None):

@@ -283,6 +283,22 @@ kvq_status kvq_append(kvq_store* store, const void* rows, int n_new, int batch,
                                  seq_lens, page_table, max_pages, static_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_append_kv(kvq_store* k_store, kvq_store* v_store, const void* k_rows, const void* v_rows,
+                         int n_new, int batch, int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                         int advance, void* stream) {
+  if (!k_store || !v_store || !seq_lens || !page_table || batch < 1 || n_new < 0 || max_pages < 1)
+    return KVQ_ERR_INVALID_ARG;
+  const kvq_store_desc& kd = k_store->desc;
+  const kvq_store_desc& vd = v_store->desc;
+  if (kd.num_kv_heads != vd.num_kv_heads || kd.head_dim != vd.head_dim || kd.page_size != vd.page_size)
+    return KVQ_ERR_INVALID_ARG;
+  if (n_new == 0) return KVQ_OK;
+  if (!k_rows || !v_rows || !aligned(k_rows, 2) || !aligned(v_rows, 2)) return KVQ_ERR_INVALID_ARG;
+  return from_cuda(launch_append_kv(k_store, v_store, static_cast<const __nv_bfloat16*>(k_rows),
+                                    static_cast<const __nv_bfloat16*>(v_rows), n_new, batch, seq_lens, page_table,
+                                    max_pages, advance ? 1 : 0, static_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream) {
   if (!seq_lens || batch < 1) return KVQ_ERR_INVALID_ARG;
   return from_cuda(launch_seq_lens_add(seq_lens, batch, n, static_cast<cudaStream_t>(stream)));

@@ -20,24 +20,17 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
+// Encodes row `row_id` of `rows` ([batch][n_new][Hkv][D]) into store `st` at position
+// base + i, where (b, i, h) are the row's coordinates and base = seq_lens[b].  One warp.
 template <int CODEC, int EPL>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-append_kernel(StoreView st, const __nv_bfloat16* __restrict__ rows, int n_new, int batch,
-              const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ page_table,
-              int max_pages) {
+__device__ __forceinline__ void encode_row(const StoreView& st, const __nv_bfloat16* __restrict__ rows,
+                                           long long row_id, int n_new, long long base, int b, int i, int h,
+                                           const int32_t* __restrict__ page_table, int max_pages) {
   constexpr int D = EPL * 32;
   constexpr int LANES_PER_BLOCK = kBlock / EPL;
   const int lane = threadIdx.x & 31;
-  const long long row_id = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  const long long n_rows = (long long)batch * n_new * st.num_kv_heads;
-  if (row_id >= n_rows) return;
-  const int h = (int)(row_id % st.num_kv_heads);
-  const long long bi = row_id / st.num_kv_heads;
-  const int i = (int)(bi % n_new);
-  const int b = (int)(bi / n_new);
-
-  const long long pos = (long long)seq_lens[b] + i;
-  if (pos < 0 || pos >= (long long)max_pages * st.page_size) {
+  const long long pos = base + i;
+  if (base < 0 || pos >= (long long)max_pages * st.page_size) {
     if (lane == 0) record_fault(st.status, KVQ_DEVICE_BAD_POSITION);
     return;
   }
@@ -96,6 +89,53 @@ append_kernel(StoreView st, const __nv_bfloat16* __restrict__ rows, int n_new, i
   }
 }
 
+template <int CODEC, int EPL>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+append_kernel(StoreView st, const __nv_bfloat16* __restrict__ rows, int n_new, int batch,
+              const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ page_table,
+              int max_pages) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long row_id = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const long long n_rows = (long long)batch * n_new * st.num_kv_heads;
+  if (row_id >= n_rows) return;
+  const int h = (int)(row_id % st.num_kv_heads);
+  const long long bi = row_id / st.num_kv_heads;
+  const int i = (int)(bi % n_new);
+  const int b = (int)(bi / n_new);
+  encode_row<CODEC, EPL>(st, rows, row_id, n_new, (long long)seq_lens[b], b, i, h, page_table, max_pages);
+}
+
+// K and V rows of one step in one launch.  CTA (x, b) encodes warps' worth of sequence
+// b's rows: the first n_new*Hkv row slots are K rows, the next n_new*Hkv are V rows.
+// With `advance` (only when one CTA covers a sequence), the CTA adds n_new to
+// seq_lens[b] after every warp has read it.
+template <int KCODEC, int VCODEC, int EPL>
+__global__ void __launch_bounds__(512)
+append_kv_kernel(StoreView ks, StoreView vs, const __nv_bfloat16* __restrict__ k_rows,
+                 const __nv_bfloat16* __restrict__ v_rows, int n_new, int32_t* __restrict__ seq_lens,
+                 const int32_t* __restrict__ page_table, int max_pages, int advance) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.y;
+  const long long per_store = (long long)n_new * ks.num_kv_heads;
+  const long long slot = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long base = seq_lens[b];
+  if (slot < 2 * per_store) {
+    const bool is_v = slot >= per_store;
+    const long long r = is_v ? slot - per_store : slot;   // row within this sequence
+    const int h = (int)(r % ks.num_kv_heads);
+    const int i = (int)(r / ks.num_kv_heads);
+    const long long row_id = (long long)b * per_store + r;
+    if (is_v) encode_row<VCODEC, EPL>(vs, v_rows, row_id, n_new, base, b, i, h, page_table, max_pages);
+    else encode_row<KCODEC, EPL>(ks, k_rows, row_id, n_new, base, b, i, h, page_table, max_pages);
+  }
+  if (advance) {
+    __syncthreads();
+    if (threadIdx.x == 0) seq_lens[b] = (int32_t)(base + n_new);
+  }
+}
+
 template <int CODEC>
 cudaError_t launch_codec(const kvq_store* s, const __nv_bfloat16* rows, int n_new, int batch,
                          const int32_t* seq_lens, const int32_t* page_table, int max_pages,
@@ -111,26 +151,64 @@ cudaError_t launch_codec(const kvq_store* s, const __nv_bfloat16* rows, int n_ne
     cudaFuncSetAttribute(append_kernel<CODEC, 8>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     carveout_set = true;
   }
+  cudaError_t e;
   switch (s->desc.head_dim) {
     case 64:
-      append_kernel<CODEC, 2><<<grid, kWarpsPerBlock * 32, 0, stream>>>(v, rows, n_new, batch, seq_lens, page_table, max_pages);
+      e = launch_pdl(append_kernel<CODEC, 2>, dim3(grid), dim3(kWarpsPerBlock * 32), 0, stream, v, rows, n_new, batch, seq_lens, page_table, max_pages);
       break;
     case 128:
-      append_kernel<CODEC, 4><<<grid, kWarpsPerBlock * 32, 0, stream>>>(v, rows, n_new, batch, seq_lens, page_table, max_pages);
+      e = launch_pdl(append_kernel<CODEC, 4>, dim3(grid), dim3(kWarpsPerBlock * 32), 0, stream, v, rows, n_new, batch, seq_lens, page_table, max_pages);
       break;
     case 256:
-      append_kernel<CODEC, 8><<<grid, kWarpsPerBlock * 32, 0, stream>>>(v, rows, n_new, batch, seq_lens, page_table, max_pages);
+      e = launch_pdl(append_kernel<CODEC, 8>, dim3(grid), dim3(kWarpsPerBlock * 32), 0, stream, v, rows, n_new, batch, seq_lens, page_table, max_pages);
       break;
     default:
       return cudaErrorNotSupported;
   }
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 __global__ void seq_lens_add_kernel(int32_t* seq_lens, int batch, int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < batch) seq_lens[b] += n;
+}
+
+template <int KC, int VC>
+cudaError_t launch_kv_pair(const kvq_store* ks, const kvq_store* vs, const __nv_bfloat16* k_rows,
+                           const __nv_bfloat16* v_rows, int n_new, int batch, int32_t* seq_lens,
+                           const int32_t* page_table, int max_pages, int advance, cudaStream_t stream) {
+  const long long slots = 2LL * n_new * ks->desc.num_kv_heads;   // warps per sequence
+  const int warps = (int)(slots < 16 ? slots : 16);
+  const unsigned gx = (unsigned)((slots + warps - 1) / warps);
+  const int adv = (advance && gx == 1) ? 1 : 0;
+  const StoreView kv = view_of(ks), vv = view_of(vs);
+  cudaError_t e;
+  switch (ks->desc.head_dim) {
+    case 64: e = launch_pdl(append_kv_kernel<KC, VC, 2>, dim3(gx, batch), dim3(32 * warps), 0, stream, kv, vv, k_rows, v_rows, n_new, seq_lens, page_table, max_pages, adv); break;
+    case 128: e = launch_pdl(append_kv_kernel<KC, VC, 4>, dim3(gx, batch), dim3(32 * warps), 0, stream, kv, vv, k_rows, v_rows, n_new, seq_lens, page_table, max_pages, adv); break;
+    case 256: e = launch_pdl(append_kv_kernel<KC, VC, 8>, dim3(gx, batch), dim3(32 * warps), 0, stream, kv, vv, k_rows, v_rows, n_new, seq_lens, page_table, max_pages, adv); break;
+    default: return cudaErrorNotSupported;
+  }
+  count_launch();
+  if (e != cudaSuccess || !advance || adv) return e;
+  // several CTAs per sequence: advance in a separate launch, after all of them
+  return launch_seq_lens_add(seq_lens, batch, n_new, stream);
+}
+
+template <int KC>
+cudaError_t launch_kv_v(const kvq_store* ks, const kvq_store* vs, const __nv_bfloat16* k_rows,
+                        const __nv_bfloat16* v_rows, int n_new, int batch, int32_t* seq_lens,
+                        const int32_t* page_table, int max_pages, int advance, cudaStream_t stream) {
+  switch (vs->desc.codec) {
+    case KVQ_CODEC_BF16: return launch_kv_pair<KC, KVQ_CODEC_BF16>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    case KVQ_CODEC_F16: return launch_kv_pair<KC, KVQ_CODEC_F16>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    case KVQ_CODEC_Q8_0: return launch_kv_pair<KC, KVQ_CODEC_Q8_0>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    case KVQ_CODEC_Q4S: return launch_kv_pair<KC, KVQ_CODEC_Q4S>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace
@@ -148,9 +226,21 @@ cudaError_t launch_append(const kvq_store* s, const __nv_bfloat16* rows, int n_n
 }
 
 cudaError_t launch_seq_lens_add(int32_t* seq_lens, int batch, int n, cudaStream_t stream) {
-  seq_lens_add_kernel<<<(batch + 255) / 256, 256, 0, stream>>>(seq_lens, batch, n);
+  const cudaError_t e = launch_pdl(seq_lens_add_kernel, dim3((batch + 255) / 256), dim3(256), 0, stream, seq_lens, batch, n);
   count_launch();
-  return cudaGetLastError();
+  return e;
+}
+
+cudaError_t launch_append_kv(const kvq_store* ks, const kvq_store* vs, const __nv_bfloat16* k_rows,
+                             const __nv_bfloat16* v_rows, int n_new, int batch, int32_t* seq_lens,
+                             const int32_t* page_table, int max_pages, int advance, cudaStream_t stream) {
+  switch (ks->desc.codec) {
+    case KVQ_CODEC_BF16: return launch_kv_v<KVQ_CODEC_BF16>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    case KVQ_CODEC_F16: return launch_kv_v<KVQ_CODEC_F16>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    case KVQ_CODEC_Q8_0: return launch_kv_v<KVQ_CODEC_Q8_0>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    case KVQ_CODEC_Q4S: return launch_kv_v<KVQ_CODEC_Q4S>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table, max_pages, advance, stream);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace kvq

@@ -267,22 +267,22 @@ __device__ __forceinline__ int pv_dim(int mt, int row) {
 
 constexpr int kGroup = kMergeGroup;
 
-// Publishes this CTA's writes, counts its arrival on `counter` and tells whether it is the
-// last of `expected` arrivals (all threads get the answer).  The last CTA sees every
-// other CTA's published writes.
+// Counts this CTA's arrival on `counter` after its partial writes and tells whether it
+// is the last of `expected` arrivals (all threads get the answer).  The last CTA sees
+// every other CTA's writes.
 __device__ __forceinline__ bool arrive_last(unsigned* counter, int expected, int tid, int nthreads,
                                             volatile int* flag, int32_t* status) {
-  __threadfence();
+  // bar.sync orders every thread's partial writes before thread 0's release-add at GPU
+  // scope; the last CTA's acquire-add (and bar.sync) makes all of them visible to it.
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
   if (tid == 0) {
-    const unsigned old = atomicAdd(counter, 1u);
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
     if (old >= (unsigned)expected) record_fault(status, KVQ_DEVICE_BAD_WORKSPACE);
     *flag = (old == (unsigned)expected - 1) ? 1 : 0;
   }
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-  const bool last = *flag != 0;
-  if (last) __threadfence();
-  return last;
+  return *flag != 0;
 }
 
 // Merges `count` split-K partials of each of `gcount` consecutive heads:
@@ -293,81 +293,58 @@ __device__ __forceinline__ bool arrive_last(unsigned* counter, int expected, int
 // shared memory when they fit; every thread of the CTA takes part.
 template <int D, int NW>
 __device__ void merge_partials(const float* ml, const float* o, long long stride, int count, int gcount,
-                               bool final, float* wbuf, long long wcap, float* hml, int tid, int warp,
-                               int lane, float* out_ml, float* out_o, long long out_stride, float* out) {
-  const int nthreads = NW * 32;
-  const bool wfit = (long long)gcount * count <= wcap;
-  for (int h = warp; h < gcount; h += NW) {
-    const float* m_h = ml + h * stride * 2;
-    float M = -INFINITY;
-    for (int c = lane; c < count; c += 32) M = fmaxf(M, __ldcg(m_h + 2 * c));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float den = 0.0f;
-    for (int c = lane; c < count; c += 32) {
-      const float2 mlc = __ldcg(reinterpret_cast<const float2*>(m_h + 2 * c));
-      const float w = (mlc.x == -INFINITY) ? 0.0f : fast_exp2(mlc.x - M);
-      den = fmaf(w, mlc.y, den);
-      if (wfit) wbuf[h * count + c] = w;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    if (lane == 0) {
-      hml[2 * h] = M;
-      hml[2 * h + 1] = den;
-    }
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+                               bool final, float* out_ml, float* out_o, long long out_stride, float* out) {
+  // Thread per (head, 4 consecutive elements).  One pass: each batch of up to 16 chunks
+  // loads their (m, l) and rows together (one L2 round trip per batch) and folds them in
+  // with a running maximum, in chunk order.
   constexpr int D4 = D / 4;
-  for (int item = tid; item < gcount * D4; item += nthreads) {
+  constexpr int BATCH = 16;
+  for (int item = threadIdx.x; item < gcount * D4; item += NW * 32) {
     const int h = item / D4, col = item % D4;
-    const float* m_h = ml + h * stride * 2;
+    const float2* ml_h = reinterpret_cast<const float2*>(ml + h * stride * 2);
     const float4* o_h = reinterpret_cast<const float4*>(o + h * stride * D) + col;
-    const float M = hml[2 * h];
+    float M = -INFINITY, den = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    auto weight = [&](int c) -> float {
-      if (wfit) return wbuf[h * count + c];
-      const float m = __ldcg(m_h + 2 * c);
-      return (m == -INFINITY) ? 0.0f : fast_exp2(m - M);
-    };
-    int c = 0;
-    for (; c + 8 <= count; c += 8) {
-      float4 v[8];
-      float w[8];
+    for (int c0 = 0; c0 < count; c0 += BATCH) {
+      const int n = min(BATCH, count - c0);
+      float2 mlv[BATCH];
+      float4 v[BATCH];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        v[u] = __ldcg(o_h + (long long)(c + u) * D4);
-        w[u] = weight(c + u);
+      for (int u = 0; u < BATCH; ++u) {
+        if (u < n) {
+          mlv[u] = __ldcg(ml_h + c0 + u);
+          v[u] = __ldcg(o_h + (long long)(c0 + u) * D4);
+        }
       }
+      float bm = M;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x = fmaf(w[u], v[u].x, acc.x);
-        acc.y = fmaf(w[u], v[u].y, acc.y);
-        acc.z = fmaf(w[u], v[u].z, acc.z);
-        acc.w = fmaf(w[u], v[u].w, acc.w);
+      for (int u = 0; u < BATCH; ++u)
+        if (u < n) bm = fmaxf(bm, mlv[u].x);
+      if (bm == -INFINITY) continue;
+      const float f = fast_exp2(M - bm);   // 0 when M = -inf
+      den *= f;
+      acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+      M = bm;
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        if (u < n && mlv[u].x != -INFINITY) {
+          const float w = fast_exp2(mlv[u].x - M);
+          den = fmaf(w, mlv[u].y, den);
+          acc.x = fmaf(w, v[u].x, acc.x);
+          acc.y = fmaf(w, v[u].y, acc.y);
+          acc.z = fmaf(w, v[u].z, acc.z);
+          acc.w = fmaf(w, v[u].w, acc.w);
+        }
       }
-    }
-    for (; c < count; ++c) {
-      const float4 v = __ldcg(o_h + (long long)c * D4);
-      const float w = weight(c);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
     }
     if (final) {
-      const float den = hml[2 * h + 1];
       const float inv = den > 0.0f ? 1.0f / den : 0.0f;
       reinterpret_cast<float4*>(out + h * D)[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     } else {
       reinterpret_cast<float4*>(out_o + h * out_stride * D)[col] = acc;
-      if (col == 0) {
-        out_ml[h * out_stride * 2] = M;
-        out_ml[h * out_stride * 2 + 1] = hml[2 * h + 1];
-      }
+      if (col == 0) reinterpret_cast<float2*>(out_ml + h * out_stride * 2)[0] = make_float2(M, den);
     }
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- kernel
@@ -395,6 +372,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
+  // Launched with programmatic stream serialization: nothing above reads memory an
+  // earlier kernel may write; wait for that kernel here, and let the next one launch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long cap = min((long long)a.max_pages * P, (long long)a.n_chunks * a.chunk_tokens);
   long long Lraw = a.seq_lens[b];
   if (Lraw < 0 || Lraw > cap) {
@@ -950,15 +931,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   // merge this group's chunk partials
   merge_partials<D, C::NW>(
       a.part_ml + (head0 * a.n_chunks + g_first) * 2, a.part_o + (head0 * a.n_chunks + g_first) * D,
-      (long long)a.n_chunks, g_count, gcount, ng == 1, obuf, (long long)C::RING / 4, hml, tid, warp, lane,
+      (long long)a.n_chunks, g_count, gcount, ng == 1,
       a.gpart_ml + (head0 * a.n_groups + g) * 2, a.gpart_o + (head0 * a.n_groups + g) * D,
       (long long)a.n_groups, a.out + head0 * D);
   if (tid == 0) a.counters[a.grp_counter_off + unit * a.n_groups + g] = 0u;
   if (ng == 1) return;
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");   // group partial written before arriving
   if (!arrive_last(a.counters + unit, ng, tid, NWT, last_flag, a.k.status)) return;
+  // the group partials were written by other CTAs before their arrivals
   merge_partials<D, C::NW>(a.gpart_ml + head0 * a.n_groups * 2, a.gpart_o + head0 * a.n_groups * D,
-                           (long long)a.n_groups, ng, gcount, true, obuf, (long long)C::RING / 4, hml,
-                           tid, warp, lane, nullptr, nullptr, 0, a.out + head0 * D);
+                           (long long)a.n_groups, ng, gcount, true, nullptr, nullptr, 0, a.out + head0 * D);
   if (tid == 0) a.counters[unit] = 0u;
 }
 
@@ -986,9 +968,9 @@ cudaError_t launch(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMa
   cudaError_t e = prepare<KC, VC, D, GW, HG>();
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_chunks, a.k.num_kv_heads, a.batch);
-  kern<<<grid, C::THREADS, C::SMEM, stream>>>(tmk, tmv, a);
+  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, stream, tmk, tmv, a);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // Resident CTAs per SM of one instantiation (0 on error).

@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_simt_kernel(DecodeArgs a) 
   const int G = a.group;
   const int P = a.k.page_size;
 
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // no-op unless launched programmatically
   const long long cap = min((long long)a.max_pages * P, (long long)a.n_chunks * a.chunk_tokens);
   long long Lraw = a.seq_lens[b];
   if (Lraw < 0 || Lraw > cap) {

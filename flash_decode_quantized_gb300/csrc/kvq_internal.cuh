@@ -93,6 +93,28 @@ cudaError_t launch_append(const kvq_store* store, const __nv_bfloat16* rows, int
                           const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                           cudaStream_t stream);
 cudaError_t launch_seq_lens_add(int32_t* seq_lens, int batch, int n, cudaStream_t stream);
+cudaError_t launch_append_kv(const kvq_store* ks, const kvq_store* vs, const __nv_bfloat16* k_rows,
+                             const __nv_bfloat16* v_rows, int n_new, int batch, int32_t* seq_lens,
+                             const int32_t* page_table, int max_pages, int advance, cudaStream_t stream);
+
+// Launches `kern` with programmatic stream serialization: the launch may begin while the
+// stream's previous kernel finishes; every kernel of this library waits on
+// griddepcontrol.wait before touching data a previous kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 cudaError_t launch_combine_pdl(const DecodeArgs& a, int head_dim, cudaStream_t stream);
 
 void count_launch();

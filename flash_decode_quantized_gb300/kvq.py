@@ -55,6 +55,7 @@ def _load():
         "kvq_destroy": [P],
         "kvq_append": [P, P, I, I, P, P, I, V],
         "kvq_seq_lens_add": [P, I, I, V],
+        "kvq_append_kv": [P, P, P, P, I, I, P, P, I, I, V],
         "kvq_decode_workspace_bytes": [P, P, I, I, I, ctypes.POINTER(DecodeOpts), ctypes.POINTER(Z)],
         "kvq_flash_decode": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
                              ctypes.POINTER(DecodeOpts), P, Z, V],
@@ -172,6 +173,26 @@ def kvq_append(store: Store, rows: torch.Tensor, seq_lens: torch.Tensor, page_ta
                           _ptr(seq_lens, torch.int32, "seq_lens"),
                           _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
                           _stream(stream)), "kvq_append")
+
+
+def kvq_append_kv(k_store: Store, v_store: Store, k_rows: torch.Tensor, v_rows: torch.Tensor,
+                  seq_lens: torch.Tensor, page_table: torch.Tensor, advance: bool = True,
+                  stream=None) -> None:
+    """K and V rows (bf16 [B, n_new, Hkv, D] each) appended in one launch; with `advance`,
+    seq_lens += n_new afterwards."""
+    for name, rows, st in (("k_rows", k_rows, k_store), ("v_rows", v_rows, v_store)):
+        if rows.dim() != 4 or rows.shape[2] != st.num_kv_heads or rows.shape[3] != st.head_dim:
+            raise ValueError(f"{name} must be [batch, n_new, num_kv_heads, head_dim]")
+    if k_rows.shape != v_rows.shape:
+        raise ValueError("k_rows and v_rows differ in shape")
+    bsz, n_new = k_rows.shape[0], k_rows.shape[1]
+    if seq_lens.numel() != bsz or page_table.dim() != 2 or page_table.shape[0] != bsz:
+        raise ValueError("seq_lens / page_table do not match the batch")
+    _check(lib.kvq_append_kv(k_store.handle, v_store.handle, _ptr(k_rows, torch.bfloat16, "k_rows"),
+                             _ptr(v_rows, torch.bfloat16, "v_rows"), n_new, bsz,
+                             _ptr(seq_lens, torch.int32, "seq_lens"),
+                             _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                             1 if advance else 0, _stream(stream)), "kvq_append_kv")
 
 
 def kvq_seq_lens_add(seq_lens: torch.Tensor, n: int, stream=None) -> None:

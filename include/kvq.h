@@ -131,6 +131,15 @@ kvq_status kvq_append(kvq_store* store, const void* rows, int n_new, int batch,
                       const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                       void* stream);
 
+/* kvq_append for the K and the V rows of a step in one launch (rows as for kvq_append,
+ * k_rows into k_store and v_rows into v_store, both at seq_lens[b] + i).  With
+ * advance != 0, seq_lens[b] += n_new afterwards, in stream order, so a decode step is
+ * kvq_append_kv + kvq_flash_decode.  The stores must share num_kv_heads, head_dim and
+ * page_size; faults are recorded in the store being written. */
+kvq_status kvq_append_kv(kvq_store* k_store, kvq_store* v_store, const void* k_rows,
+                         const void* v_rows, int n_new, int batch, int32_t* seq_lens,
+                         const int32_t* page_table, int max_pages, int advance, void* stream);
+
 /* seq_lens[b] += n for b < batch, on the device (after the K and the V append). */
 kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
 

@@ -95,3 +95,24 @@ def test_batched_append_two_sequences():
         gp, gs = store_rows(st, inp, b, np.arange(96))
         ep, es = expected_rows(inp, "k", "q4s", b, np.arange(96))
         assert np.array_equal(gp, ep) and np.array_equal(gs, es)
+
+
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q8_0", "q4s"), ("bf16", "bf16")])
+@pytest.mark.parametrize("n_new", [1, 3, 200])
+def test_append_kv_matches_oracle_and_advances(kc, vc, n_new):
+    # K and V rows of a step in one launch, seq_lens advanced afterwards; 200 rows per
+    # sequence take several CTAs (advance in a second launch)
+    inp = make_inputs([n_new, n_new], 8, 2, 128, seed=40 + n_new, page_size=64)
+    k = kvq()
+    ks = k.kvq_store_create(kc, 2, 128, 64, inp.num_pages)
+    vs = k.kvq_store_create(vc, 2, 128, 64, inp.num_pages)
+    seq = torch.zeros(2, dtype=torch.int32, device="cuda")
+    k.kvq_append_kv(ks, vs, bf16_tensor(np.stack(inp.k_rows)), bf16_tensor(np.stack(inp.v_rows)), seq,
+                    torch.from_numpy(inp.page_table).cuda(), advance=True)
+    assert seq.cpu().tolist() == [n_new, n_new]
+    for b in range(2):
+        for which, st, codec in (("k", ks, kc), ("v", vs, vc)):
+            gp, gs = store_rows(st, inp, b, np.arange(n_new))
+            ep, es = expected_rows(inp, which, codec, b, np.arange(n_new))
+            assert np.array_equal(gp, ep) and np.array_equal(gs, es), (which, b)
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0

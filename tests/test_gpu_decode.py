@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from kvq_testutil import (assert_close, build_store, device_inputs, kvq, oracle_out,
+from kvq_testutil import (assert_close, bf16_tensor, build_store, device_inputs, kvq, oracle_out,
                           oracle_values)
 from workloads import make_inputs, ragged_lengths
 
@@ -175,3 +175,37 @@ def test_dirty_workspace_is_reported():
     out = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=3000, workspace=ws, chunk_tokens=256)
     assert k.kvq_store_get_error(ks) == 0
     assert_close(out.cpu().numpy(), oracle_out(inp, "q8_0", "q8_0"), "after re-init")
+
+
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q8_0", "q4s")])
+def test_resident_append_decode_loop(kc, vc):
+    # resident-loop workload at reduced size: a heavy-tailed prefix, then steps of
+    # kvq_append_kv (encode one K and V row, seq_lens += 1) + kvq_flash_decode, all on the
+    # device; outputs checked against the oracle at several steps
+    L0, steps = 1000, 24
+    inp = make_inputs([L0 + steps], 32, 8, 128, seed=23, dist="t3", channel_scaled=True)
+    k = kvq()
+    ks = k.kvq_store_create(kc, 8, 128, inp.page_size, inp.num_pages)
+    vs = k.kvq_store_create(vc, 8, 128, inp.page_size, inp.num_pages)
+    pt = torch.from_numpy(inp.page_table).cuda()
+    seq = torch.zeros(1, dtype=torch.int32, device="cuda")
+    krows, vrows = bf16_tensor(inp.k_rows[0]), bf16_tensor(inp.v_rows[0])
+    k.kvq_append_kv(ks, vs, krows[None, :L0].contiguous(), vrows[None, :L0].contiguous(), seq, pt)
+    q = bf16_tensor(inp.q)
+    ws = torch.zeros(k.kvq_decode_workspace_bytes(ks, vs, 1, 32, L0 + steps), dtype=torch.uint8, device="cuda")
+    outs = {}
+    for step in range(steps):
+        k.kvq_append_kv(ks, vs, krows[None, L0 + step:L0 + step + 1].contiguous(),
+                        vrows[None, L0 + step:L0 + step + 1].contiguous(), seq, pt)
+        out = k.kvq_flash_decode(q, ks, vs, seq, pt, max_len_hint=L0 + steps, workspace=ws)
+        if step in (0, 7, steps - 1):
+            outs[step] = out.cpu().numpy()
+    assert int(seq.item()) == L0 + steps
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+    for step, got in outs.items():
+        L = L0 + step + 1
+        sub = make_inputs([L], 32, 8, 128, seed=23, dist="t3", channel_scaled=True)
+        sub.k_rows[0] = inp.k_rows[0][:L]
+        sub.v_rows[0] = inp.v_rows[0][:L]
+        sub.q = inp.q
+        assert_close(got, oracle_out(sub, kc, vc), f"step {step}")
