@@ -342,9 +342,11 @@ def run_mine(args, rank, world):
     e2e = measure_e2e(torch, kvq, layer, flush, max(3, min(K, 20)))
     e2e["value"] = round(world * e2e.pop("kvb") / (e2e["ms"] * 1e-3) / 1e9, 1)
 
-    sweep = None
+    sweep = extras = None
     if rank == 0 and not args.no_sweep and args.workload == "layer8b":
         sweep = run_sweep(torch, kvq, args, flush, peak)
+        if not args.no_extras:
+            extras = run_extras(torch, kvq, args, flush, peak)
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -367,6 +369,8 @@ def run_mine(args, rank, world):
     }
     if sweep is not None:
         result["sweep"] = sweep
+    if extras is not None:
+        result["workloads"] = extras
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, wl, codec, seq_lens[0] if wl["kv_len"] else 4096)
     return result
@@ -398,6 +402,64 @@ def measure_e2e(torch, kvq, layer, flush, iters):
     return {"ms": round(statistics.median(ms), 5), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(out_h.numel() * 4), "kvb": statistics.mean(kvb),
             "timing": "host wall clock around H2D + append + decode + D2H, median"}
+
+
+def run_extras(torch, kvq, args, flush, peak):
+    """The other workloads at full size: the long-context depth sweep (f16 control vs
+    q8_0 K+V, GQA 16:1, D=256), the 64-sequence ragged paged batch, and the resident
+    append + decode loop (128 steps from a 65536-token heavy-tailed prefix)."""
+    out = []
+    wl = WORKLOADS["longctx"]
+    for L in (32768, 131072, 204800):
+        base = None
+        for arm in ("f16/f16", "q8_0/q8_0"):
+            layer = Layer(kvq, torch, wl, arm, [L], 0, seed=88)
+            layer.prepare(args.variant, 0)
+            time_decode_only(torch, layer, flush, 3)
+            ms = statistics.median(time_decode_only(torch, layer, flush, 10))
+            gbs = layer.kv_bytes() / (ms * 1e-3) / 1e9
+            base = ms if arm == "f16/f16" else base
+            out.append({"workload": "longctx", "kv_len": L, "codec": arm, "us": round(ms * 1e3, 2),
+                        "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                        "vs_f16_time": round(ms / base, 3)})
+            del layer
+            torch.cuda.empty_cache()
+    from workloads import ragged_lengths
+    lens = [int(x) for x in ragged_lengths(1234, 64)]
+    for arm in ("q8_0/q8_0", "q4s/q4s"):
+        layer = Layer(kvq, torch, WORKLOADS["ragged"], arm, lens, 0, seed=89)
+        layer.prepare(args.variant, 0)
+        time_decode_only(torch, layer, flush, 2)
+        ms = statistics.median(time_decode_only(torch, layer, flush, 8))
+        gbs = layer.kv_bytes() / (ms * 1e-3) / 1e9
+        out.append({"workload": "ragged", "batch": 64, "total_tokens": sum(lens), "codec": arm,
+                    "us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)})
+        del layer
+        torch.cuda.empty_cache()
+    for arm in ("q8_0/q8_0", "q8_0/q4s"):
+        layer = Layer(kvq, torch, WORKLOADS["resident"], arm, [65536], 160, seed=90)
+        layer.prepare(args.variant, 0)
+        for _ in range(3):
+            layer.append()
+            layer.decode()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        kvb = 0
+        e0.record()
+        for _ in range(128):
+            layer.append()
+            layer.decode()
+            kvb += layer.kv_bytes()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 128
+        gbs = kvb / 128 / (ms * 1e-3) / 1e9
+        out.append({"workload": "resident", "steps": 128, "codec": arm, "us_per_step": round(ms * 1e3, 2),
+                    "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "note": "back-to-back append_kv + decode, L2 not flushed between steps"})
+        del layer
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_sweep(torch, kvq, args, flush, peak):
@@ -502,6 +564,7 @@ def main():
     ap.add_argument("--variant", type=int, default=0)
     ap.add_argument("--chunk-tokens", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' cells")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

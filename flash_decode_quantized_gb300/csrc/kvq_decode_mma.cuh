@@ -145,8 +145,6 @@ __device__ __forceinline__ uint32_t u4pair_raw(uint32_t w) {
 }
 constexpr float kBias8 = 1152.0f;            // offset of i8pair_raw values
 constexpr float kBias4 = 1032.0f;            // offset of u4pair_raw values
-constexpr uint32_t kNegBias8 = 0xE480E480u;  // f16 pair (-1152, -1152)
-constexpr uint32_t kNegBias4 = 0xE408E408u;  // f16 pair (-1032, -1032)
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -718,25 +716,17 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                               i8pair_raw(y3, 0x4240)};
             uint32_t ao[4] = {i8pair_raw(y0, 0x4341), i8pair_raw(y1, 0x4341), i8pair_raw(y2, 0x4341),
                               i8pair_raw(y3, 0x4341)};
-            if constexpr (C::NPV == 1) {
-              // (1152 + v) P, then -1152 P: the code offset cancels in the accumulator
-              const uint32_t an[4] = {kNegBias8, kNegBias8, kNegBias8, kNegBias8};
-              mma16816<false>(o[2 * bb][0], ae, bf[0][0], bf[0][1]);
-              mma16816<false>(o[2 * bb][0], an, bf[0][0], bf[0][1]);
-              mma16816<false>(o[2 * bb + 1][0], ao, bf[0][0], bf[0][1]);
-              mma16816<false>(o[2 * bb + 1][0], an, bf[0][0], bf[0][1]);
-            } else {
-              // two n-tiles share the A operand: subtract the offset once in registers
+            // exact small integers in f16 before the product: an offset folded into the fp32
+            // accumulator instead loses its low bits there, and that error grows with the chunk
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                ae[k] = hsub2_u32(ae[k], 0x64806480u);
-                ao[k] = hsub2_u32(ao[k], 0x64806480u);
-              }
+            for (int k = 0; k < 4; ++k) {
+              ae[k] = hsub2_u32(ae[k], 0x64806480u);
+              ao[k] = hsub2_u32(ao[k], 0x64806480u);
+            }
 #pragma unroll
-              for (int n = 0; n < C::NPV; ++n) {
-                mma16816<false>(o[2 * bb][n], ae, bf[n][0], bf[n][1]);
-                mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
-              }
+            for (int n = 0; n < C::NPV; ++n) {
+              mma16816<false>(o[2 * bb][n], ae, bf[n][0], bf[n][1]);
+              mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
             }
           } else {  // q4s: matrices (tok 0-7, chunk b), (tok 8-15, chunk b) for this block
             uint32_t y0, y1, y2, y3;
@@ -745,23 +735,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             uint32_t a01[4] = {u4pair_raw(ya), u4pair_raw(ya >> 4), u4pair_raw(yb), u4pair_raw(yb >> 4)};
             uint32_t a23[4] = {u4pair_raw(ya >> 8), u4pair_raw(ya >> 12), u4pair_raw(yb >> 8),
                                u4pair_raw(yb >> 12)};
-            if constexpr (C::NPV == 1) {
-              const uint32_t an[4] = {kNegBias4, kNegBias4, kNegBias4, kNegBias4};
-              mma16816<false>(o[2 * bb][0], a01, bf[0][0], bf[0][1]);
-              mma16816<false>(o[2 * bb][0], an, bf[0][0], bf[0][1]);
-              mma16816<false>(o[2 * bb + 1][0], a23, bf[0][0], bf[0][1]);
-              mma16816<false>(o[2 * bb + 1][0], an, bf[0][0], bf[0][1]);
-            } else {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                a01[k] = hsub2_u32(a01[k], 0x64086408u);
-                a23[k] = hsub2_u32(a23[k], 0x64086408u);
-              }
+            for (int k = 0; k < 4; ++k) {
+              a01[k] = hsub2_u32(a01[k], 0x64086408u);
+              a23[k] = hsub2_u32(a23[k], 0x64086408u);
+            }
 #pragma unroll
-              for (int n = 0; n < C::NPV; ++n) {
-                mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
-                mma16816<false>(o[2 * bb + 1][n], a23, bf[n][0], bf[n][1]);
-              }
+            for (int n = 0; n < C::NPV; ++n) {
+              mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
+              mma16816<false>(o[2 * bb + 1][n], a23, bf[n][0], bf[n][1]);
             }
           }
         }
