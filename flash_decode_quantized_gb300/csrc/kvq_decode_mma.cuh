@@ -81,12 +81,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
     if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   return false;
 }
-// Bounded wait by a single thread.
-__device__ __forceinline__ bool mbar_wait_one(uint32_t bar, uint32_t parity) {
-  for (int it = 0; it < kTimeoutIters; ++it)
-    if (mbar_try(bar, parity)) return true;
-  return false;
-}
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             int c3, uint32_t bar) {
   asm volatile(
@@ -374,6 +368,19 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   // earlier kernel may write; wait for that kernel here, and let the next one launch.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int32_t* pt = a.page_table + (long long)b * a.max_pages;
+  // Page ids of this CTA's tiles, held by warp 0: lane i has tile pb + i in pg_lo and
+  // tile pb + 32 + i in pg_hi.  The first 64 are read together with seq_lens (any
+  // in-bounds table entry may be read; entries past the sequence are never used).
+  auto load_page = [&](int tile) -> int {
+    const long long pos0 = ((long long)chunk + (long long)tile * a.n_chunks) * kT;
+    return pos0 < (long long)a.max_pages * P ? __ldg(pt + pos0 / P) : -1;
+  };
+  int pg_lo = -1, pg_hi = -1, pb = 0;
+  if (warp == 0) {
+    pg_lo = load_page(lane);
+    pg_hi = load_page(32 + lane);
+  }
   const long long cap = min((long long)a.max_pages * P, (long long)a.n_chunks * a.chunk_tokens);
   long long Lraw = a.seq_lens[b];
   if (Lraw < 0 || Lraw > cap) {
@@ -396,7 +403,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     return;
   }
   const int n_tiles = (NT - chunk + a.n_chunks - 1) / a.n_chunks;
-  const int32_t* pt = a.page_table + (long long)b * a.max_pages;
 
   if (tid == 0) {
     for (int s = 0; s < C::NS; ++s) {
@@ -410,10 +416,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   // ------------------------------------------------------------ tile producer
   // Lane 0 of warp 0 issues the copies: the first NS tiles up front, then tile k + NS
   // into stage k % NS as soon as every warp has released tile k.
-  auto issue_tile = [&](int tile) {
+  auto issue_tile = [&](int tile, int page) {
     const int s = tile % C::NS;
     const int pos0 = (chunk + tile * a.n_chunks) * kT;
-    const int page = pt[pos0 / P];
     const int row0 = pos0 % P;
     const uint32_t full = bar_full + 8 * s;
     // the flag is published to the warps by the mbarrier phase that completes below
@@ -445,10 +450,24 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       bulk_load(vst + C::VROWS, src, kT * C::NB * 2, full);
     }
   };
-  const bool producer = tid == 0;
-  if (producer)
-    for (int tile = 0; tile < n_tiles && tile < C::NS; ++tile) issue_tile(tile);
-  __syncwarp();
+  // Page of tile t (t >= pb, nondecreasing over calls), by all of warp 0.  Crossing a
+  // 32-tile boundary shifts the window and starts the loads for the batch after next,
+  // 32 tiles before they are needed.
+  auto page_of = [&](int t) -> int {
+    while (t >= pb + 32) {
+      pg_lo = pg_hi;
+      pb += 32;
+      pg_hi = load_page(pb + 32 + lane);
+    }
+    return __shfl_sync(0xffffffffu, pg_lo, t - pb);
+  };
+  if (warp == 0) {
+    for (int tile = 0; tile < n_tiles && tile < C::NS; ++tile) {
+      const int page = page_of(tile);
+      if (lane == 0) issue_tile(tile, page);
+    }
+    __syncwarp();
+  }
 
   // ------------------------------------------------------------ compute warps
   const int hg = warp >> 2;          // head group
@@ -775,17 +794,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-    if (warp == 0) {
-      bool fail = false;
-      if (producer && tile + C::NS < n_tiles) {
-        if (mbar_wait_one(bar_empty + 8 * s, (tile / C::NS) & 1)) issue_tile(tile + C::NS);
-        else fail = true;
-      }
-      // reconverges warp 0 after the producer lane's branch
-      if (__shfl_sync(0xffffffffu, (int)fail, 0)) {
+    if (warp == 0 && tile + C::NS < n_tiles) {
+      // refill the stage once every warp has released it; lane 0 issues the copies
+      if (!mbar_wait_warp(bar_empty + 8 * s, (tile / C::NS) & 1)) {
         timed_out = true;
         break;
       }
+      const int page = page_of(tile + C::NS);
+      if (lane == 0) issue_tile(tile + C::NS, page);
+      __syncwarp();
     }
   }
 
