@@ -234,6 +234,23 @@ class Layer:
                                          max_len_hint=self.hint, workspace=self.ws,
                                          chunk_tokens=self.chunk, variant=self.variant)
 
+    def step(self, q=None, new_k=None, new_v=None):
+        """One decode step of the layer: append the new token's K and V rows, attend,
+        advance seq_lens.  One fused launch on the tensor-core kernel; the CUDA-core
+        variant runs kvq_append_kv + kvq_flash_decode."""
+        if self.variant == 1:
+            self.append(new_k, new_v)
+            return self.decode(q)
+        nk = self.new_k if new_k is None else new_k
+        nv = self.new_v if new_v is None else new_v
+        out = self.kvq.kvq_flash_decode_append(
+            self.q if q is None else q, nk.view(self.batch, self.hkv, self.d),
+            nv.view(self.batch, self.hkv, self.d), self.k_store, self.v_store, self.seq_lens,
+            self.page_table, advance=True, out=self.out, max_len_hint=self.hint, workspace=self.ws,
+            chunk_tokens=self.chunk, variant=self.variant)
+        self.host_lens = [L + 1 for L in self.host_lens]
+        return out
+
     def kv_bytes(self):
         return sum(self.host_lens) * self.hkv * token_head_bytes(f"{self.kc}/{self.vc}", self.d)
 
@@ -283,7 +300,7 @@ def run_mine(args, rank, world):
         seq_lens = [int(x) for x in ragged_lengths(1234 + rank, wl["batch"])]
     else:
         seq_lens = [args.kv_len or wl["kv_len"]] * wl["batch"]
-    extra = args.warmup + args.steps + 64
+    extra = args.warmup + 2 * args.steps + 96   # timed steps, e2e steps, the unfused comparison
     layer = Layer(kvq, torch, wl, codec, seq_lens, extra, seed=1000 + rank)
     layer.prepare(args.variant, args.chunk_tokens)
     flush = l2_flusher(torch)
@@ -291,14 +308,13 @@ def run_mine(args, rank, world):
 
     for _ in range(args.warmup):
         flush()
-        layer.append()
-        layer.decode()
+        layer.step()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     kv_bytes = []
     launches0 = kvq.kvq_launch_count()
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -308,17 +324,18 @@ def run_mine(args, rank, world):
             flush()
             gpu_lead(torch)
             ev[i][0].record()
-            layer.append()
+            layer.step()
             ev[i][1].record()
-            layer.decode()
-            ev[i][2].record()
             kv_bytes.append(layer.kv_bytes())
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     launches = kvq.kvq_launch_count() - launches0
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    ms_per_step = statistics.mean(step_ms)
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    # the step is the one fused kernel (the CUDA-core variant: append + decode + combine)
+    dec_ms = step_ms
+    # median over the K per-step event pairs (mean and worst step reported beside it): an
+    # nvidia-smi sample landing inside one step can stall that step by ~100 us
+    ms_per_step = statistics.median(step_ms)
     if world > 1:
         t = torch.tensor([ms_per_step], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -326,21 +343,37 @@ def run_mine(args, rank, world):
     kvb = statistics.mean(kv_bytes)
     value = world * kvb / (ms_per_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    dec_mean = statistics.mean(dec_ms)
+    dec_mean = statistics.median(dec_ms)
     achieved = kvb / (dec_mean * 1e-3) / 1e9
     sha = kernel_sources_sha()
     key = f"{args.workload}:{codec}:{seq_lens[0] if len(set(seq_lens)) == 1 else 'ragged'}"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(sha, key),
-                "kernel": "kvq_flash_decode call (decode + combine kernels)",
+                "kernel": "decode_mma_kernel with the fused append (kvq_flash_decode_append), one launch per step" if args.variant != 1 else "kvq_append_kv + decode_simt + combine",
                 "peak_source": f"{peak_kind} copy bandwidth",
                 "decode_us": round(dec_mean * 1e3, 2),
                 "decode_us_p10_p90": [round(float(np.percentile(dec_ms, 10)) * 1e3, 2),
                                       round(float(np.percentile(dec_ms, 90)) * 1e3, 2)],
-                "cv": round(statistics.pstdev(dec_ms) / dec_mean, 4)}
+                "cv": round(statistics.pstdev(dec_ms) / statistics.mean(dec_ms), 4),
+                "stat": "median of per-step CUDA-event times"}
 
     e2e = measure_e2e(torch, kvq, layer, flush, max(3, min(K, 20)))
     e2e["value"] = round(world * e2e.pop("kvb") / (e2e["ms"] * 1e-3) / 1e9, 1)
+    # the same step as two launches (kvq_append_kv, then kvq_flash_decode), for comparison
+    unfused = None
+    if args.variant != 1:
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            flush()
+            gpu_lead(torch)
+            ev2[i][0].record()
+            layer.append()
+            ev2[i][1].record()
+            layer.decode()
+            ev2[i][2].record()
+        torch.cuda.synchronize()
+        unfused = {"step_us": round(statistics.mean(a.elapsed_time(c) for a, _, c in ev2) * 1e3, 2),
+                   "decode_us": round(statistics.mean(b.elapsed_time(c) for _, b, c in ev2) * 1e3, 2)}
 
     sweep = extras = None
     if rank == 0 and not args.no_sweep and args.workload == "layer8b":
@@ -352,6 +385,8 @@ def run_mine(args, rank, world):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_layer_step": round(ms_per_step * 1e3, 2),
+        "us_per_step_mean": round(statistics.mean(step_ms) * 1e3, 2),
+        "us_per_step_max": [round(max(step_ms) * 1e3, 2), int(np.argmax(step_ms))],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, device-generated bf16 rows encoded on device)",
         "config": {"workload": f"{args.workload}: B={wl['batch']}, Hq={wl['hq']}, Hkv={wl['hkv']}, "
@@ -360,6 +395,7 @@ def run_mine(args, rank, world):
                    "chunk_tokens": args.chunk_tokens, "l2": "evicted before every timed step by reading a 2xL2 buffer (clean lines), outside its events; ~100 us GPU lead so events exclude host launch latency",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
+        "unfused_step": unfused,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
@@ -392,8 +428,7 @@ def measure_e2e(torch, kvq, layer, flush, iters):
         q_d.copy_(q_h, non_blocking=True)
         k_d.copy_(k_h, non_blocking=True)
         v_d.copy_(v_h, non_blocking=True)
-        layer.append(k_d, v_d)
-        layer.decode(q_d)
+        layer.step(q_d, k_d, v_d)
         out_h.copy_(layer.out, non_blocking=True)
         torch.cuda.synchronize()
         ms.append((time.perf_counter() - t0) * 1e3)
@@ -401,7 +436,7 @@ def measure_e2e(torch, kvq, layer, flush, iters):
     h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
     return {"ms": round(statistics.median(ms), 5), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(out_h.numel() * 4), "kvb": statistics.mean(kvb),
-            "timing": "host wall clock around H2D + append + decode + D2H, median"}
+            "timing": "host wall clock around H2D + fused append/decode step + D2H, median"}
 
 
 def run_extras(torch, kvq, args, flush, peak):
@@ -437,26 +472,47 @@ def run_extras(torch, kvq, args, flush, peak):
         del layer
         torch.cuda.empty_cache()
     for arm in ("q8_0/q8_0", "q8_0/q4s"):
-        layer = Layer(kvq, torch, WORKLOADS["resident"], arm, [65536], 160, seed=90)
+        layer = Layer(kvq, torch, WORKLOADS["resident"], arm, [65536], 3 + 3 * 128 + 32, seed=90)
         layer.prepare(args.variant, 0)
         for _ in range(3):
-            layer.append()
-            layer.decode()
+            layer.step()
         torch.cuda.synchronize()
+        tph = layer.hkv * token_head_bytes(arm, layer.d)
+
+        def loop_bytes(L0):   # KV bytes the 128 steps from length L0 read
+            return sum(L0 + i + 1 for i in range(128)) * tph
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        kvb = 0
+        L0 = int(layer.seq_lens.item())
         e0.record()
         for _ in range(128):
-            layer.append()
-            layer.decode()
-            kvb += layer.kv_bytes()
+            layer.step()
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / 128
-        gbs = kvb / 128 / (ms * 1e-3) / 1e9
-        out.append({"workload": "resident", "steps": 128, "codec": arm, "us_per_step": round(ms * 1e3, 2),
-                    "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                    "note": "back-to-back append_kv + decode, L2 not flushed between steps"})
+        gbs = loop_bytes(L0) / 128 / (ms * 1e-3) / 1e9
+        row = {"workload": "resident", "steps": 128, "codec": arm, "us_per_step": round(ms * 1e3, 2),
+               "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+               "note": "128 back-to-back fused append+decode steps, L2 not flushed between steps"}
+        # the same 128 steps captured once in a CUDA graph, timed over one replay
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(128):
+                    layer.step()
+            graph.replay()
+            torch.cuda.synchronize()
+            L0 = int(layer.seq_lens.item())
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            assert int(layer.seq_lens.item()) == L0 + 128
+            gms = e0.elapsed_time(e1) / 128
+            row["graph_us_per_step"] = round(gms * 1e3, 2)
+            row["graph_gbs"] = round(loop_bytes(L0) / 128 / (gms * 1e-3) / 1e9, 1)
+        except Exception as exc:   # report, keep the rest of the run
+            row["graph_error"] = str(exc)[:200]
+        out.append(row)
         del layer
         torch.cuda.empty_cache()
     return out

@@ -158,7 +158,8 @@ struct Plan {
   size_t ml_off;     // chunk partials: o at 0, (m, l) at ml_off
   size_t go_off;     // group partials: o at go_off, (m, l) at gml_off
   size_t gml_off;
-  size_t cnt_off;    // unit counters, then group counters
+  size_t cnt_off;    // unit counters, then group counters, then sequence counters
+  size_t seq_cnt_off;
   size_t total;
 };
 
@@ -190,7 +191,10 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
     long long c = (hint + want - 1) / want;
     c = (c + 63) / 64 * 64;
     if (c < 128) c = 128;
-    if (units > slots && c > 1024) c = 1024;
+    // With one or two CTAs per unit a long sequence among short ones would run alone
+    // (lengths are on the device): keep chunks short enough for the block scheduler to
+    // balance the batch.
+    if (units * 4 > slots && c > 1024) c = 1024;
     chunk = (int)c;
   }
   p->chunk_tokens = chunk;
@@ -203,7 +207,8 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   p->go_off = p->ml_off + round_up(heads * p->n_chunks * 2 * sizeof(float), 256);
   p->gml_off = p->go_off + round_up(heads * p->n_groups * D * sizeof(float), 256);
   p->cnt_off = p->gml_off + round_up(heads * p->n_groups * 2 * sizeof(float), 256);
-  p->total = p->cnt_off + round_up(units * (1 + p->n_groups) * sizeof(unsigned), 256);
+  p->seq_cnt_off = p->cnt_off + units * (1 + p->n_groups) * sizeof(unsigned);
+  p->total = p->cnt_off + round_up((units * (1 + p->n_groups) + (size_t)batch) * sizeof(unsigned), 256);
   return KVQ_OK;
 }
 
@@ -322,12 +327,18 @@ kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, vo
   return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
-kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_store* v_store,
-                            const int32_t* seq_lens, const int32_t* page_table, int max_pages,
-                            kvq_codec codec, float* out, int batch, int num_q_heads,
-                            float softmax_scale, int max_len_hint,
-                            const kvq_decode_opts* opts, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace kvq {
+namespace {
+
+// kvq_flash_decode, and with k_new set the fused append step (kvq_flash_decode_append).
+kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, const kvq_store* k_store,
+                       const kvq_store* v_store, const int32_t* seq_lens, int32_t* seq_lens_adv,
+                       const int32_t* page_table, int max_pages, kvq_codec codec, float* out,
+                       int batch, int num_q_heads, float softmax_scale, int max_len_hint,
+                       const kvq_decode_opts* opts, void* workspace, size_t workspace_bytes,
+                       void* stream) {
   if (!q || !k_store || !v_store || !seq_lens || !page_table || !out || !workspace)
     return KVQ_ERR_INVALID_ARG;
   if (batch < 1 || num_q_heads < 1 || max_pages < 1 || max_len_hint < 0)
@@ -341,6 +352,7 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   if (num_q_heads % kd.num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   if ((long long)max_len_hint > (long long)max_pages * kd.page_size) return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16)) return KVQ_ERR_INVALID_ARG;
+  if (k_new && (!v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   const int group = num_q_heads / kd.num_kv_heads;
   Plan p;
@@ -348,6 +360,7 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   if (st != KVQ_OK) return st;
   if (workspace_bytes < p.total) return KVQ_ERR_WORKSPACE;
   if (group > 16 || p.variant < 1 || p.variant > 2) return KVQ_ERR_UNSUPPORTED;
+  if (k_new && p.variant != 2) return KVQ_ERR_UNSUPPORTED;
   SimtFn sfn = simt_fn(kd.codec, vd.codec);
   MmaFn mfn = mma_fn(kd.codec, vd.codec);
   if (p.variant == 1 && !sfn) return KVQ_ERR_UNSUPPORTED;
@@ -376,12 +389,44 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
   a.counters = reinterpret_cast<unsigned*>(ws + p.cnt_off);
   a.grp_counter_off = (long long)batch * kd.num_kv_heads;
   a.out = out;
+  a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  a.seq_lens_adv = seq_lens_adv;
+  a.seq_counters = reinterpret_cast<unsigned*>(ws + p.seq_cnt_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.variant == 2)  // the tensor-core kernel merges the split itself (last CTA per unit)
     return from_cuda(mfn(a, kd.head_dim, k_store->rows_map, v_store->rows_map, s));
   st = from_cuda(sfn(a, kd.head_dim, s));
   if (st != KVQ_OK) return st;
   return from_cuda(launch_combine_pdl(a, kd.head_dim, s));
+}
+
+}  // namespace
+}  // namespace kvq
+
+extern "C" {
+
+kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                            const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                            kvq_codec codec, float* out, int batch, int num_q_heads,
+                            float softmax_scale, int max_len_hint,
+                            const kvq_decode_opts* opts, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return decode_impl(q, nullptr, nullptr, k_store, v_store, seq_lens, nullptr, page_table, max_pages,
+                     codec, out, batch, num_q_heads, softmax_scale, max_len_hint, opts, workspace,
+                     workspace_bytes, stream);
+}
+
+kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void* v_new,
+                                   kvq_store* k_store, kvq_store* v_store, int32_t* seq_lens,
+                                   const int32_t* page_table, int max_pages, kvq_codec codec,
+                                   float* out, int batch, int num_q_heads, float softmax_scale,
+                                   int max_len_hint, int advance, const kvq_decode_opts* opts,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!k_new || !v_new) return KVQ_ERR_INVALID_ARG;
+  return decode_impl(q, k_new, v_new, k_store, v_store, seq_lens, advance ? seq_lens : nullptr,
+                     page_table, max_pages, codec, out, batch, num_q_heads, softmax_scale,
+                     max_len_hint, opts, workspace, workspace_bytes, stream);
 }
 
 kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code) {

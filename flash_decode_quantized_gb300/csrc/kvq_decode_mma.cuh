@@ -41,6 +41,7 @@
 #include <cuda.h>
 
 #include "kvq_device.cuh"
+#include "kvq_encode.cuh"
 
 namespace kvq {
 namespace mma {
@@ -204,15 +205,22 @@ struct Cfg {
   static constexpr int KLINE = KRB >= 128 ? 128 : KRB;    // TMA box width / swizzle span
   static constexpr int VLINE = VRB >= 128 ? 128 : VRB;
   static constexpr int al1k(int x) { return (x + 1023) / 1024 * 1024; }
+  // stage: [K rows | V rows | K scales | V scales]; row regions 1024-aligned (swizzle)
   static constexpr int KROWS = al1k(kT * KRB);
-  static constexpr int KSC = KQ ? al1k(kT * NB * 2) : 0;
   static constexpr int VROWS = al1k(kT * VRB);
-  static constexpr int VSC = VQ ? al1k(kT * NB * 2) : 0;
-  static constexpr int STAGE = KROWS + KSC + VROWS + VSC;
+  static constexpr int KSC = KQ ? kT * NB * 2 : 0;        // multiples of 16 bytes
+  static constexpr int VSC = VQ ? kT * NB * 2 : 0;
+  static constexpr int V_OFF = KROWS, KSC_OFF = KROWS + VROWS, VSC_OFF = KSC_OFF + KSC;
+  static constexpr int STAGE = al1k(KROWS + VROWS + KSC + VSC);
+  // Four resident CTAs per SM (16 warps) for 4-head warps when two stages fit a quarter
+  // of the SM's shared memory: registers capped at 128 (no spills at D <= 128), else the
+  // compiler is free and register use sets the occupancy.
+  static constexpr bool FOUR = HG == 1 && GW <= 4 && D <= 128 && 2 * STAGE + 6 * 1024 <= 56 * 1024;
+  static constexpr int MINB = FOUR ? 4 : 1;
   // ring depth: as many stages (2..4) as fit the per-CTA budget that keeps the
-  // register-limited number of resident CTAs per SM
-  static constexpr int SMEM_BUDGET = HG == 2 ? 200 * 1024 : (D == 256 ? 100 * 1024 : 70 * 1024);
-  static constexpr int NS0 = (SMEM_BUDGET - 4096) / STAGE;
+  // intended number of resident CTAs per SM
+  static constexpr int SMEM_BUDGET = HG == 2 ? 200 * 1024 : D == 256 ? 100 * 1024 : FOUR ? 54 * 1024 : 70 * 1024;
+  static constexpr int NS0 = (SMEM_BUDGET - 2048) / STAGE;
   static constexpr int NS = NS0 > 4 ? 4 : (NS0 < 2 ? 2 : NS0);
   static constexpr int OBUF = NW * 8 * D * 4;             // merge buffer (reuses the ring)
   static constexpr int RING = NS * STAGE > OBUF ? NS * STAGE : OBUF;
@@ -224,6 +232,8 @@ struct Cfg {
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
   static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
+  // 233472 bytes of shared memory per SM, 1024 of them reserved per resident CTA
+  static_assert(!FOUR || 4 * (SMEM + 1024) <= 233472, "four CTAs per SM must fit");
 };
 
 // Shared-memory address of 16-byte chunk `chunk` of tile row `t` (rows as TMA wrote them).
@@ -341,10 +351,16 @@ __device__ void merge_partials(const float* ml, const float* o, long long stride
 
 // ---------------------------------------------------------------- kernel
 
+// Arrival on a per-sequence counter (release: the arriving CTA's reads of seq_lens come
+// before it); returns the ticket.
+__device__ __forceinline__ unsigned seq_arrive(unsigned* cnt) {
+  unsigned old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(cnt) : "memory");
+  return old;
+}
+
 template <int KC, int VC, int D, int GW, int HG>
-__global__ void __launch_bounds__(Cfg<KC, VC, D, GW, HG>::THREADS, 1)
-decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                  DecodeArgs a) {
+__device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeArgs& a) {
   using C = Cfg<KC, VC, D, GW, HG>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle pattern
@@ -381,24 +397,57 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     pg_lo = load_page(lane);
     pg_hi = load_page(32 + lane);
   }
+  // Fused append: the new token's K and V rows, read early by warp 0 (used only by the
+  // CTA whose tile holds the token; the reads are in bounds for every CTA).
+  constexpr int EPL = D / 32;
+  float xk[EPL], xv[EPL];
+  if (a.k_new != nullptr && warp == 0) {
+    const long long row = (long long)b * a.k.num_kv_heads + kvh;
+    load_row<EPL>(a.k_new + row * D, lane, xk);
+    load_row<EPL>(a.v_new + row * D, lane, xv);
+  }
   const long long cap = min((long long)a.max_pages * P, (long long)a.n_chunks * a.chunk_tokens);
-  long long Lraw = a.seq_lens[b];
-  if (Lraw < 0 || Lraw > cap) {
+  const bool fused = a.k_new != nullptr;
+  const long long L_old = a.seq_lens[b];
+  long long Lraw = fused ? L_old + 1 : L_old;
+  const bool len_ok = L_old >= 0 && Lraw <= cap;   // else: fault, no append, no advance
+  if (!len_ok) {
     if (tid == 0 && chunk == 0 && kvh == 0) {
       record_fault(a.k.status, KVQ_DEVICE_BAD_SEQ_LEN);
       record_fault(a.v.status, KVQ_DEVICE_BAD_SEQ_LEN);
     }
-    Lraw = Lraw < 0 ? 0 : cap;
+    Lraw = L_old < 0 ? 0 : cap;
   }
   const int L = (int)Lraw;
   // The sequence's 64-token tiles are dealt round-robin to its n_chunks CTAs: CTA c
   // takes tiles c, c + n_chunks, ... so that every CTA streams from all of the
   // sequence's pages (evens out per-CTA speed) and all finish together.
   const int NT = (L + kT - 1) / kT;                 // tiles of the sequence
+  const int nv = min(a.n_chunks, NT);   // CTAs with work for this (b, kvh)
+  // Fused advance of seq_lens[b].  Arrivals on the sequence's counter: every early-exiting
+  // CTA, and per (sequence, KV head) the one CTA that finishes the split, which arrives
+  // only after every CTA of its unit has arrived on the merge counters (so after their
+  // reads of seq_lens).  The holder of the last ticket stores the new length.  A
+  // finishing CTA takes its ticket before its final merge and checks it after, so the
+  // atomic's latency overlaps the merge.
+  const bool adv = a.seq_lens_adv != nullptr;
+  const unsigned seq_total = gridDim.y * (unsigned)(a.n_chunks - nv + (nv > 0 ? 1 : 0));
+  auto seq_finish = [&](unsigned ticket) {   // thread 0
+    if (ticket >= seq_total) record_fault(a.k.status, KVQ_DEVICE_BAD_WORKSPACE);
+    if (ticket == seq_total - 1) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");   // after every counted arrival
+      if (len_ok) a.seq_lens_adv[b] = (int32_t)(L_old + 1);
+      a.seq_counters[b] = 0u;
+    }
+  };
   if (chunk >= NT) {
     if (L == 0 && chunk == 0) {  // empty sequence: its heads' outputs are zero
       const long long h0 = (long long)b * a.num_q_heads + (long long)kvh * G;
       for (int idx = tid; idx < G * D; idx += C::THREADS) a.out[h0 * D + idx] = 0.0f;
+    }
+    if (adv) {
+      __syncthreads();   // every thread has read seq_lens
+      if (tid == 0) seq_finish(seq_arrive(a.seq_counters + b));
     }
     return;
   }
@@ -435,19 +484,19 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 #pragma unroll
     for (int seg = 0; seg < (C::KRB + 127) / 128; ++seg)
       tma_load_4d(st + seg * kT * 128, &tmk, seg * 128, row0, kvh, page, full);
-    const uint32_t vst = st + C::KROWS + C::KSC;
+    const uint32_t vst = st + C::V_OFF;
 #pragma unroll
     for (int seg = 0; seg < (C::VRB + 127) / 128; ++seg)
       tma_load_4d(vst + seg * kT * 128, &tmv, seg * 128, row0, kvh, page, full);
     if constexpr (C::KQ) {
       const uint8_t* src = a.k.buf + ((long long)page * a.k.num_kv_heads + kvh) * a.k.slab_bytes +
                            (long long)P * C::KRB + (long long)row0 * C::NB * 2;
-      bulk_load(st + C::KROWS, src, kT * C::NB * 2, full);
+      bulk_load(st + C::KSC_OFF, src, kT * C::NB * 2, full);
     }
     if constexpr (C::VQ) {
       const uint8_t* src = a.v.buf + ((long long)page * a.v.num_kv_heads + kvh) * a.v.slab_bytes +
                            (long long)P * C::VRB + (long long)row0 * C::NB * 2;
-      bulk_load(vst + C::VROWS, src, kT * C::NB * 2, full);
+      bulk_load(st + C::VSC_OFF, src, kT * C::NB * 2, full);
     }
   };
   // Page of tile t (t >= pb, nondecreasing over calls), by all of warp 0.  Crossing a
@@ -461,12 +510,32 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     return __shfl_sync(0xffffffffu, pg_lo, t - pb);
   };
+  // Fused append: the CTA holding the new token's tile (its last) encodes the token's K
+  // and V rows with warp 0 before that tile's copies are issued; the proxy fence orders
+  // the rows' generic-proxy stores before the bulk-tensor reads.
+  bool need_enc = fused && len_ok && chunk == (NT - 1) % a.n_chunks;
+  auto encode_new = [&]() {   // by all of warp 0; the token lies in this CTA's last tile
+    const int t = n_tiles - 1;   // read without moving page_of's window
+    const int lo = __shfl_sync(0xffffffffu, pg_lo, (t - pb) & 31);
+    const int hi = __shfl_sync(0xffffffffu, pg_hi, (t - pb) & 31);
+    const int page = t < pb + 32 ? lo : t < pb + 64 ? hi : load_page(t);
+    if (page >= 0 && page < a.k.num_pages && page < a.v.num_pages) {   // else the tile faults
+      const int r = (int)(L_old % P);
+      store_row<KC, EPL>(a.k, page, r, kvh, xk);
+      store_row<VC, EPL>(a.v, page, r, kvh, xv);
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncwarp();
+    need_enc = false;
+  };
   if (warp == 0) {
     for (int tile = 0; tile < n_tiles && tile < C::NS; ++tile) {
+      if (need_enc && tile == n_tiles - 1) encode_new();
       const int page = page_of(tile);
       if (lane == 0) issue_tile(tile, page);
     }
     __syncwarp();
+    if (need_enc) encode_new();   // its tile comes later, from the refill path
   }
 
   // ------------------------------------------------------------ compute warps
@@ -546,9 +615,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (n_valid > 0) {
       const bool partial = n_valid < 16;
       const uint32_t st = sbase + s * C::STAGE;
-      const uint32_t kst = st, vst = st + C::KROWS + C::KSC;
-      const uint8_t* ksc = smem + s * C::STAGE + C::KROWS;
-      const uint8_t* vsc = smem + s * C::STAGE + C::KROWS + C::KSC + C::VROWS;
+      const uint32_t kst = st, vst = st + C::V_OFF;
+      const uint8_t* ksc = smem + s * C::STAGE + C::KSC_OFF;
+      const uint8_t* vsc = smem + s * C::STAGE + C::VSC_OFF;
       const int mi = lane >> 3, mr = lane & 7;
 
       // ---------------- QK^T: S[tok r / r+8][heads 2i, 2i+1] (log2 units after scaling)
@@ -807,6 +876,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   }
 
   // ------------------------------------------------------------ merge the warps
+  unsigned seq_ticket = 0u;
+  if (adv && nv == 1 && tid == 0) seq_ticket = seq_arrive(a.seq_counters + b);   // the only CTA
 
   const int NWT = C::NW * 32;
   if (timed_out) record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
@@ -882,7 +953,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     hml[2 * h + 1] = lsum;
   }
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
-  const int nv = min(a.n_chunks, NT);   // CTAs with work for this (b, kvh)
   if (nv == 1) {
     // the whole sequence is this chunk: normalize and write the output (no split)
     for (int idx = tid; idx < gcount * D; idx += NWT) {
@@ -894,6 +964,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       const float lsum = hml[2 * h + 1];
       a.out[(head0 + h) * D + j] = lsum > 0.0f ? sum / lsum : 0.0f;
     }
+    if (adv && tid == 0) seq_finish(seq_ticket);
     return;
   }
   // ------------------------------------------------------------ partial write (a7)
@@ -927,6 +998,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   if (!arrive_last(a.counters + a.grp_counter_off + unit * a.n_groups + g, g_count, tid, NWT, last_flag,
                    a.k.status))
     return;
+  if (adv && ng == 1 && tid == 0) seq_ticket = seq_arrive(a.seq_counters + b);   // finishes the unit
   // merge this group's chunk partials
   merge_partials<D, C::NW>(
       a.part_ml + (head0 * a.n_chunks + g_first) * 2, a.part_o + (head0 * a.n_chunks + g_first) * D,
@@ -934,13 +1006,27 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       a.gpart_ml + (head0 * a.n_groups + g) * 2, a.gpart_o + (head0 * a.n_groups + g) * D,
       (long long)a.n_groups, a.out + head0 * D);
   if (tid == 0) a.counters[a.grp_counter_off + unit * a.n_groups + g] = 0u;
-  if (ng == 1) return;
+  if (ng == 1) {
+    if (adv && tid == 0) seq_finish(seq_ticket);
+    return;
+  }
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");   // group partial written before arriving
   if (!arrive_last(a.counters + unit, ng, tid, NWT, last_flag, a.k.status)) return;
+  if (adv && tid == 0) seq_ticket = seq_arrive(a.seq_counters + b);   // finishes the unit
   // the group partials were written by other CTAs before their arrivals
   merge_partials<D, C::NW>(a.gpart_ml + head0 * a.n_groups * 2, a.gpart_o + head0 * a.n_groups * D,
                            (long long)a.n_groups, ng, gcount, true, nullptr, nullptr, 0, a.out + head0 * D);
-  if (tid == 0) a.counters[unit] = 0u;
+  if (tid == 0) {
+    a.counters[unit] = 0u;
+    if (adv) seq_finish(seq_ticket);
+  }
+}
+
+template <int KC, int VC, int D, int GW, int HG>
+__global__ void __launch_bounds__(Cfg<KC, VC, D, GW, HG>::THREADS, Cfg<KC, VC, D, GW, HG>::MINB)
+decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  DecodeArgs a) {
+  decode_cta<KC, VC, D, GW, HG>(tmk, tmv, a);
 }
 
 // Sets the kernel's shared-memory attributes once per device.

@@ -86,6 +86,15 @@ struct DecodeArgs {
                                // counters at grp_counter_off (all zero between calls)
   long long grp_counter_off;
   float* out;                  // [B][Hq][D]
+  // Fused append (tensor-core kernel only): with k_new set, the token at position
+  // seq_lens[b] gets rows k_new/v_new [B][Hkv][D] (bf16) written by the CTA whose tile
+  // holds it, and attention covers seq_lens[b] + 1 tokens.  With seq_lens_adv set as
+  // well, the last of the sequence's CTAs to have read seq_lens[b] (counted in
+  // seq_counters[b], zero between calls) stores seq_lens[b] + 1 there.
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int32_t* seq_lens_adv;
+  unsigned* seq_counters;
 };
 
 // Launchers implemented in the kernel translation units.  Each returns a CUDA error.

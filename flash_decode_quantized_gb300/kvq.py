@@ -63,6 +63,8 @@ def _load():
         "kvq_decode_workspace_init": [P, Z, V],
         "kvq_flash_decode_static_ws": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
                                        ctypes.POINTER(DecodeOpts), V],
+        "kvq_flash_decode_append": [P, P, P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I, I,
+                                    ctypes.POINTER(DecodeOpts), P, Z, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -234,6 +236,39 @@ def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: 
                                 int(max_len_hint), _opts(chunk_tokens, variant),
                                 _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                 _stream(stream)), "kvq_flash_decode")
+    return out
+
+
+def kvq_flash_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                            k_store: Store, v_store: Store, seq_lens: torch.Tensor,
+                            page_table: torch.Tensor, advance: bool = True,
+                            out: torch.Tensor | None = None, softmax_scale: float = 0.0,
+                            max_len_hint: int | None = None, workspace: torch.Tensor | None = None,
+                            chunk_tokens: int = 0, variant: int = 0, stream=None) -> torch.Tensor:
+    """One decode step with the append fused in: k_new, v_new (bf16 [B, Hkv, D]) are
+    written at position seq_lens[b], q attends over seq_lens[b] + 1 tokens, and with
+    `advance` seq_lens[b] += 1 on the device."""
+    bsz, hq, dim = q.shape
+    for name, t, st in (("k_new", k_new, k_store), ("v_new", v_new, v_store)):
+        if t.dim() != 3 or t.shape[0] != bsz or t.shape[1] != st.num_kv_heads or t.shape[2] != st.head_dim:
+            raise ValueError(f"{name} must be [B, Hkv, D] = [{bsz}, {st.num_kv_heads}, {st.head_dim}]")
+    max_pages = page_table.shape[1]
+    if max_len_hint is None:
+        max_len_hint = max_pages * k_store.page_size
+    if out is None:
+        out = torch.empty((bsz, hq, dim), dtype=torch.float32, device=q.device)
+    need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq, max_len_hint, chunk_tokens, variant)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
+    _check(lib.kvq_flash_decode_append(_ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"),
+                                       _ptr(v_new, torch.bfloat16, "v_new"), k_store.handle, v_store.handle,
+                                       _ptr(seq_lens, torch.int32, "seq_lens"),
+                                       _ptr(page_table, torch.int32, "page_table"), max_pages, codec,
+                                       _ptr(out, torch.float32, "out"), bsz, hq, float(softmax_scale),
+                                       int(max_len_hint), 1 if advance else 0, _opts(chunk_tokens, variant),
+                                       _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                       _stream(stream)), "kvq_flash_decode_append")
     return out
 
 

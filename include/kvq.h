@@ -143,13 +143,17 @@ kvq_status kvq_append_kv(kvq_store* k_store, kvq_store* v_store, const void* k_r
 /* seq_lens[b] += n for b < batch, on the device (after the K and the V append). */
 kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
 
-/* Device workspace bytes a kvq_flash_decode call with the same stores, batch, head
- * count, max_len_hint and options needs (the split depends on both stores' codecs).
- * The workspace holds the split-K partials and, at its end, one arrival counter per
- * (sequence, KV head). */
+/* Device workspace bytes a kvq_flash_decode (or kvq_flash_decode_append) call with the
+ * same stores, batch, head count, max_len_hint and options needs (the split depends on
+ * both stores' codecs).  The workspace holds the split-K partials and, at its end,
+ * arrival counters: per (sequence, KV head), per group of chunks, and per sequence. */
 kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store* v_store,
                                       int batch, int num_q_heads, int max_len_hint,
                                       const kvq_decode_opts* opts, size_t* bytes);
+
+/* Zero a decode workspace (its arrival counters must be zero before its first use;
+ * every completed kvq_flash_decode leaves them zero again).  Enqueued on `stream`. */
+kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Split-K flash-decode over the quantized store (a2..a8):
  *   q          device bf16 [batch][num_q_heads][head_dim]
@@ -165,16 +169,35 @@ kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store*
  *   aligned, zeroed once before its first use (kvq_decode_workspace_init); calls that
  *   share a workspace must not overlap on the device.
  * A sequence of length 0 yields zeros. */
-/* Zero a decode workspace (its arrival counters must be zero before its first use;
- * every completed kvq_flash_decode leaves them zero again).  Enqueued on `stream`. */
-kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
-
 kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_store* v_store,
                             const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                             kvq_codec codec, float* out, int batch, int num_q_heads,
                             float softmax_scale, int max_len_hint,
                             const kvq_decode_opts* opts, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* One decode step with the append fused in (a1 followed by a2..a8, one launch of the
+ * tensor-core kernel; the on-device append of rMLX issue #295 "Fix direction" done by
+ * the decode kernel itself).  For every sequence b:
+ *   - k_new[b] and v_new[b] (device bf16 [batch][num_kv_heads][head_dim], contiguous)
+ *     are encoded into k_store and v_store at position seq_lens[b], exactly as
+ *     kvq_append would encode them;
+ *   - q attends over the seq_lens[b] + 1 tokens the stores then hold;
+ *   - with advance != 0, seq_lens[b] is set to seq_lens[b] + 1 on the device, by the
+ *     last of the sequence's CTAs once every one of them has read the old value;
+ *     with advance == 0 it is left unchanged.
+ * Arguments otherwise as for kvq_flash_decode, with seq_lens[b] + 1 <= max_len_hint.
+ * The result equals kvq_append_kv(n_new = 1, advance) followed by kvq_flash_decode.
+ * Only the tensor-core kernel implements it: opts->variant 1 gives KVQ_ERR_UNSUPPORTED.
+ * A sequence whose new length does not fit gets no append and no advance and is
+ * recorded as a device fault (KVQ_DEVICE_BAD_SEQ_LEN); a bad page of the new token is
+ * recorded as KVQ_DEVICE_BAD_PAGE. */
+kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void* v_new,
+                                   kvq_store* k_store, kvq_store* v_store, int32_t* seq_lens,
+                                   const int32_t* page_table, int max_pages, kvq_codec codec,
+                                   float* out, int batch, int num_q_heads, float softmax_scale,
+                                   int max_len_hint, int advance, const kvq_decode_opts* opts,
+                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* kvq_flash_decode without a workspace argument, for callers that cannot allocate
  * device memory where they decode (inside host callbacks, under a memory manager that
