@@ -187,18 +187,26 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
                                        : 2;
     const long long units = (long long)batch * k->desc.num_kv_heads;
     const long long slots = (long long)sms * per_sm;
-    const long long want = slots >= units ? slots / units : 1;   // chunks per unit
+    long long want = slots >= units ? slots / units : 1;   // chunks per unit
+    const long long max_chunks = (hint + 127) / 128;           // >= 128 tokens per chunk
+    if (want > max_chunks) want = max_chunks;
     long long c = (hint + want - 1) / want;
     c = (c + 63) / 64 * 64;
     if (c < 128) c = 128;
     // With one or two CTAs per unit a long sequence among short ones would run alone
     // (lengths are on the device): keep chunks short enough for the block scheduler to
     // balance the batch.
-    if (units * 4 > slots && c > 1024) c = 1024;
+    const bool capped = units * 4 > slots && c > 1024;
+    if (capped) c = 1024;
     chunk = (int)c;
+    // One full wave: `want` chunks per unit even where rounding the chunk up to whole
+    // tiles would need fewer (the tensor-core kernel deals tiles round-robin, so every
+    // resident slot gets work; chunk_tokens then only bounds the length)
+    p->n_chunks = capped ? (int)((hint + c - 1) / c) : (int)want;
+  } else {
+    p->n_chunks = (hint + chunk - 1) / chunk;
   }
   p->chunk_tokens = chunk;
-  p->n_chunks = (hint + chunk - 1) / chunk;
   p->n_groups = (p->n_chunks + kMergeGroup - 1) / kMergeGroup;
   const size_t D = (size_t)k->desc.head_dim;
   const size_t heads = (size_t)batch * num_q_heads;

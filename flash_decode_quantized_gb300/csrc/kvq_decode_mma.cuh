@@ -779,6 +779,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       // when one n-tile carries both; lo lanes feed x - f16(x) instead of x.
       const float lo_sel = (C::NPV == 1 && r >= 4) ? 1.0f : 0.0f;
       if constexpr (C::VQ) {
+        uint32_t vq4[4];   // q4s: one ldmatrix.x4 covers blocks bb and bb + 1 (bb even)
 #pragma unroll
         for (int bb = 0; bb < C::NB; ++bb) {
           float x[4];
@@ -817,9 +818,9 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
               mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
             }
           } else {  // q4s: matrices (tok 0-7, chunk b), (tok 8-15, chunk b) for this block
-            uint32_t y0, y1, y2, y3;
-            ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, (bb & ~1) + (mi >> 1)), y0, y1, y2, y3);
-            const uint32_t ya = (bb & 1) ? y2 : y0, yb = (bb & 1) ? y3 : y1;
+            if ((bb & 1) == 0)
+              ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), vq4[0], vq4[1], vq4[2], vq4[3]);
+            const uint32_t ya = (bb & 1) ? vq4[2] : vq4[0], yb = (bb & 1) ? vq4[3] : vq4[1];
             uint32_t a01[4] = {u4pair_raw(ya), u4pair_raw(ya >> 4), u4pair_raw(yb), u4pair_raw(yb >> 4)};
             uint32_t a23[4] = {u4pair_raw(ya >> 8), u4pair_raw(ya >> 12), u4pair_raw(yb >> 8),
                                u4pair_raw(yb >> 12)};
