@@ -251,6 +251,22 @@ class Layer:
         self.host_lens = [L + 1 for L in self.host_lens]
         return out
 
+    def unfused(self, target="f16"):
+        """The separate-pass arm (stock build of halobench record clm-0022): dequantize K and
+        V into 16-bit stores with kvq_dequantize, then a 16-bit kvq_flash_decode."""
+        kvq, torch = self.kvq, self.torch
+        if getattr(self, "kd", None) is None:
+            pages = self.k_store.num_pages
+            self.kd = kvq.kvq_store_create(target, self.hkv, self.d, self.page_size, pages)
+            self.vd = kvq.kvq_store_create(target, self.hkv, self.d, self.page_size, pages)
+            n = kvq.kvq_decode_workspace_bytes(self.kd, self.vd, self.batch, self.hq, self.hint, 0, 0)
+            self.ws16 = torch.empty(n, dtype=torch.uint8, device="cuda")
+            kvq.kvq_decode_workspace_init(self.ws16)
+        kvq.kvq_dequantize(self.k_store, self.kd, self.seq_lens, self.page_table)
+        kvq.kvq_dequantize(self.v_store, self.vd, self.seq_lens, self.page_table)
+        return kvq.kvq_flash_decode(self.q, self.kd, self.vd, self.seq_lens, self.page_table, out=self.out,
+                                    max_len_hint=self.hint, workspace=self.ws16)
+
     def kv_bytes(self):
         return sum(self.host_lens) * self.hkv * token_head_bytes(f"{self.kc}/{self.vc}", self.d)
 
@@ -276,13 +292,14 @@ def gpu_lead(torch):
     torch.cuda._sleep(200_000)
 
 
-def time_decode_only(torch, layer, flush, iters):
+def time_decode_only(torch, layer, flush, iters, fn=None):
+    fn = fn or layer.decode
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
     for i in range(iters):
         flush()
         gpu_lead(torch)
         ev[i][0].record()
-        layer.decode()
+        fn()
         ev[i][1].record()
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in ev]
@@ -454,9 +471,14 @@ def run_extras(torch, kvq, args, flush, peak):
             ms = statistics.median(time_decode_only(torch, layer, flush, 10))
             gbs = layer.kv_bytes() / (ms * 1e-3) / 1e9
             base = ms if arm == "f16/f16" else base
-            out.append({"workload": "longctx", "kv_len": L, "codec": arm, "us": round(ms * 1e3, 2),
-                        "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                        "vs_f16_time": round(ms / base, 3)})
+            row = {"workload": "longctx", "kv_len": L, "codec": arm, "us": round(ms * 1e3, 2),
+                   "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "vs_f16_time": round(ms / base, 3)}
+            if arm == "q8_0/q8_0":
+                time_decode_only(torch, layer, flush, 2, layer.unfused)
+                um = statistics.median(time_decode_only(torch, layer, flush, 8, layer.unfused))
+                row["unfused_f16_us"] = round(um * 1e3, 2)
+                row["unfused_vs_f16_time"] = round(um / base, 3)
+            out.append(row)
             del layer
             torch.cuda.empty_cache()
     from workloads import ragged_lengths
@@ -534,10 +556,17 @@ def run_sweep(torch, kvq, args, flush, peak):
             gbs = layer.kv_bytes() / (med * 1e-3) / 1e9
             if arm == "bf16/bf16":
                 base = med
-            rows.append({"kv_len": L, "codec": arm, "us": round(med * 1e3, 2),
-                         "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                         "vs_bf16_time": round(med / base, 3),
-                         "cv": round(statistics.pstdev(ms) / statistics.mean(ms), 4)})
+            row = {"kv_len": L, "codec": arm, "us": round(med * 1e3, 2),
+                   "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                   "vs_bf16_time": round(med / base, 3),
+                   "cv": round(statistics.pstdev(ms) / statistics.mean(ms), 4)}
+            if arm in ("q8_0/q8_0", "q4s/q4s"):
+                # the same decode with a separate dequantize-to-f16 pass first
+                time_decode_only(torch, layer, flush, 2, layer.unfused)
+                um = statistics.median(time_decode_only(torch, layer, flush, 10, layer.unfused))
+                row["unfused_f16_us"] = round(um * 1e3, 2)
+                row["fused_speedup"] = round(um / med, 3)
+            rows.append(row)
             del layer
             torch.cuda.empty_cache()
     return rows

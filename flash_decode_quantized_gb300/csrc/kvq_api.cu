@@ -437,6 +437,21 @@ kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void*
                      max_len_hint, opts, workspace, workspace_bytes, stream);
 }
 
+kvq_status kvq_dequantize(const kvq_store* src, kvq_store* dst, const int32_t* seq_lens,
+                          const int32_t* page_table, int max_pages, int batch, void* stream) {
+  if (!src || !dst || !seq_lens || !page_table || batch < 1 || max_pages < 1) return KVQ_ERR_INVALID_ARG;
+  const kvq_store_desc& sd = src->desc;
+  const kvq_store_desc& dd = dst->desc;
+  if (sd.num_kv_heads != dd.num_kv_heads || sd.head_dim != dd.head_dim || sd.page_size != dd.page_size ||
+      sd.num_pages != dd.num_pages)
+    return KVQ_ERR_INVALID_ARG;
+  if ((sd.codec != KVQ_CODEC_Q8_0 && sd.codec != KVQ_CODEC_Q4S) ||
+      (dd.codec != KVQ_CODEC_F16 && dd.codec != KVQ_CODEC_BF16))
+    return KVQ_ERR_UNSUPPORTED;
+  return from_cuda(launch_dequantize(src, dst, seq_lens, page_table, max_pages, batch,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code) {
   if (!store || !device_code) return KVQ_ERR_INVALID_ARG;
   int32_t v = 0;

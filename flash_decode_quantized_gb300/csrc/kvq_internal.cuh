@@ -102,6 +102,8 @@ cudaError_t launch_append(const kvq_store* store, const __nv_bfloat16* rows, int
                           const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                           cudaStream_t stream);
 cudaError_t launch_seq_lens_add(int32_t* seq_lens, int batch, int n, cudaStream_t stream);
+cudaError_t launch_dequantize(const kvq_store* src, kvq_store* dst, const int32_t* seq_lens,
+                              const int32_t* page_table, int max_pages, int batch, cudaStream_t stream);
 cudaError_t launch_append_kv(const kvq_store* ks, const kvq_store* vs, const __nv_bfloat16* k_rows,
                              const __nv_bfloat16* v_rows, int n_new, int batch, int32_t* seq_lens,
                              const int32_t* page_table, int max_pages, int advance, cudaStream_t stream);

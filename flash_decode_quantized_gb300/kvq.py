@@ -63,6 +63,7 @@ def _load():
         "kvq_decode_workspace_init": [P, Z, V],
         "kvq_flash_decode_static_ws": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
                                        ctypes.POINTER(DecodeOpts), V],
+        "kvq_dequantize": [P, P, P, P, I, I, V],
         "kvq_flash_decode_append": [P, P, P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I, I,
                                     ctypes.POINTER(DecodeOpts), P, Z, V],
     }
@@ -293,6 +294,15 @@ def kvq_flash_decode_static_ws(q: torch.Tensor, k_store: Store, v_store: Store,
                                           int(max_len_hint), _opts(chunk_tokens, variant), _stream(stream)),
            "kvq_flash_decode_static_ws")
     return out
+
+
+def kvq_dequantize(src: Store, dst: Store, seq_lens: torch.Tensor, page_table: torch.Tensor,
+                   stream=None) -> None:
+    """Separate dequantize pass: rows [0, seq_lens[b]) of the quantized store `src` rewritten
+    into the 16-bit store `dst` (the unfused comparison arm)."""
+    _check(lib.kvq_dequantize(src.handle, dst.handle, _ptr(seq_lens, torch.int32, "seq_lens"),
+                              _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
+                              seq_lens.shape[0], _stream(stream)), "kvq_dequantize")
 
 
 def kvq_decode_workspace_init(workspace: torch.Tensor, stream=None) -> None:

@@ -143,6 +143,18 @@ kvq_status kvq_append_kv(kvq_store* k_store, kvq_store* v_store, const void* k_r
 /* seq_lens[b] += n for b < batch, on the device (after the K and the V append). */
 kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
 
+/* Separate dequantize pass (the comparison arm of halobench record clm-0022, METHOD and
+ * depth tables: the quantized cache converted outside the attention kernel, then read
+ * by a 16-bit decode).  Rewrites rows [0, seq_lens[b]) of every sequence of `src`
+ * (q8_0 or q4s) into `dst` (f16 or bf16) at the same positions: value = d * q rounded
+ * once to the 16-bit type (d * q is exact in fp32).  The stores must share num_kv_heads,
+ * head_dim, page_size and num_pages; page_table and seq_lens as for kvq_append.
+ * A length past the table or a bad page id is recorded in dst's status word (rows of
+ * that page are skipped).  Not part of the fused path: kvq_flash_decode reads `src`
+ * directly. */
+kvq_status kvq_dequantize(const kvq_store* src, kvq_store* dst, const int32_t* seq_lens,
+                          const int32_t* page_table, int max_pages, int batch, void* stream);
+
 /* Device workspace bytes a kvq_flash_decode (or kvq_flash_decode_append) call with the
  * same stores, batch, head count, max_len_hint and options needs (the split depends on
  * both stores' codecs).  The workspace holds the split-K partials and, at its end,

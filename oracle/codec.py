@@ -57,6 +57,14 @@ def f64_to_f16_bits(x: np.ndarray) -> np.ndarray:
     return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float16).view(np.uint16)
 
 
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float64 values that are exactly representable in fp32 to bf16 (nearest even;
+    finite inputs)."""
+    u = np.asarray(x, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
 def row_bytes(codec: str, head_dim: int) -> int:
     """Bytes of one stored row (one token of one KV head), excluding scales."""
     return {"bf16": 2 * head_dim, "f16": 2 * head_dim, "q8_0": head_dim,
@@ -153,3 +161,19 @@ def dequantized(x_bits: np.ndarray, codec: str) -> np.ndarray:
     x_bits = np.asarray(x_bits, dtype=np.uint16)
     packed, scales = encode_rows(x_bits, codec)
     return decode_rows(packed, scales, codec, x_bits.shape[1])
+
+
+def dequantized_16(packed: np.ndarray, scales: np.ndarray, codec: str, head_dim: int,
+                   target: str) -> np.ndarray:
+    """The 16-bit rows a separate dequantize pass writes (the "stock" arm of halobench
+    record clm-0022, METHOD and depth tables: quantized KV converted in its own pass, then
+    read by a 16-bit decode): bits of fp16_rn(d * q) for target "f16", bf16_rn(d * q) for
+    "bf16".  d * q (11-bit scale times a code of at most 8 bits) is exact in fp32, so one
+    rounding from the exact product."""
+    x = decode_rows(packed, scales, codec, head_dim)
+    if target == "f16":
+        return f64_to_f16_bits(x)
+    if target == "bf16":
+        return f64_to_bf16_bits(x)
+    raise ValueError(target)
+

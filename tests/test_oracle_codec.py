@@ -136,3 +136,31 @@ def test_q4_error_larger_than_q8():
     e4 = np.abs(codec.dequantized(bits, "q4s") - x).mean()
     # uniform rounding error d/4 on average, d = amax/127 vs amax/7
     assert 10 < e4 / e8 < 30
+
+
+def test_dequantized_16_hand_values():
+    """The separate dequantize pass's 16-bit values, derived by hand: exact products d*q
+    rounded once to nearest even (ties included)."""
+    # one q8_0 row of 32 elements: codes at 0..3, the rest zero; scales per block below
+    cases = [
+        # (scale bits, code, f16 bits, bf16 bits, why)
+        (0x6156, 3, 0x6800, 0x4500, "683*3 = 2049: tie between 2048 and 2050 (f16) / 2048 and 2064 (bf16) -> 2048"),
+        (0x3555, 127, 0x514A, 0x4229, "0.333251953125*127 = 42.322998...: f16 step 1/32 -> 42.3125, bf16 step 1/4 -> 42.25"),
+        (0x3800, -7, 0xC300, 0xC060, "0.5*-7 = -3.5 exact in both"),
+        (0x3555, -7, 0xC0AA, 0xC015, "-2.332763671875: f16 step 1/512 -> -2.33203125, bf16 step 1/64 -> -2.328125"),
+    ]
+    for sbits, q, f16_bits, bf16_bits, why in cases:
+        packed = np.zeros((1, 32), np.uint8)
+        packed[0, 5] = np.uint8(q & 0xFF)
+        scales = np.array([[sbits]], np.uint16)
+        got16 = codec.dequantized_16(packed, scales, "q8_0", 32, "f16")
+        gotb = codec.dequantized_16(packed, scales, "q8_0", 32, "bf16")
+        assert int(got16[0, 5]) == f16_bits, why
+        assert int(gotb[0, 5]) == bf16_bits, why
+        assert int(got16[0, 0]) == 0 and int(gotb[0, 0]) == 0
+    # q4s: code -7 is nibble 1 (low nibble of byte 0 holds element 0)
+    packed = np.zeros((1, 16), np.uint8)
+    packed[0, 0] = 0x81            # element 0: u = 1 -> q = -7; element 1: u = 8 -> q = 0
+    scales = np.array([[0x3555]], np.uint16)
+    got = codec.dequantized_16(packed, scales, "q4s", 32, "f16")
+    assert int(got[0, 0]) == 0xC0AA and int(got[0, 1]) == 0
