@@ -543,7 +543,7 @@ def run_extras(torch, kvq, args, flush, peak):
 def run_sweep(torch, kvq, args, flush, peak):
     """Kernel-only decode timings for every codec arm at kv_len 4096 / 16384 / 65536."""
     wl = WORKLOADS["layer8b"]
-    arms = ["bf16/bf16", "q8_0/bf16", "q8_0/q8_0", "q4s/q4s", "q8_0/q4s"]
+    arms = ["bf16/bf16", "q8_0/bf16", "q8_0/q8_0", "q4s/q4s", "q8_0/q4s", "q4s/q8_0", "q4s/bf16"]
     rows = []
     for L in (4096, 16384, 65536):
         base = None

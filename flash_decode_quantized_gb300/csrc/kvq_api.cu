@@ -22,6 +22,8 @@ cudaError_t simt_launch_q8_0_bf16(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_q8_0_q8_0(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_q4s_q4s(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_q8_0_q4s(const DecodeArgs&, int, cudaStream_t);
+cudaError_t simt_launch_q4s_q8_0(const DecodeArgs&, int, cudaStream_t);
+cudaError_t simt_launch_q4s_bf16(const DecodeArgs&, int, cudaStream_t);
 using MmaFn = cudaError_t (*)(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t mma_launch_bf16_bf16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t mma_launch_f16_f16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
@@ -29,12 +31,16 @@ cudaError_t mma_launch_q8_0_bf16(const DecodeArgs&, int, const CUtensorMap&, con
 cudaError_t mma_launch_q8_0_q8_0(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t mma_launch_q4s_q4s(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t mma_launch_q8_0_q4s(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_q4s_q8_0(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t mma_launch_q4s_bf16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 int mma_occupancy_bf16_bf16(int, int);
 int mma_occupancy_f16_f16(int, int);
 int mma_occupancy_q8_0_bf16(int, int);
 int mma_occupancy_q8_0_q8_0(int, int);
 int mma_occupancy_q4s_q4s(int, int);
 int mma_occupancy_q8_0_q4s(int, int);
+int mma_occupancy_q4s_q8_0(int, int);
+int mma_occupancy_q4s_bf16(int, int);
 
 namespace {
 
@@ -47,6 +53,8 @@ SimtFn simt_fn(int kc, int vc) {
   if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) return simt_launch_q8_0_q8_0;
   if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) return simt_launch_q4s_q4s;
   if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) return simt_launch_q8_0_q4s;
+  if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q8_0) return simt_launch_q4s_q8_0;
+  if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_BF16) return simt_launch_q4s_bf16;
   return nullptr;
 }
 
@@ -57,6 +65,8 @@ MmaFn mma_fn(int kc, int vc) {
   if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) return mma_launch_q8_0_q8_0;
   if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) return mma_launch_q4s_q4s;
   if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) return mma_launch_q8_0_q4s;
+  if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q8_0) return mma_launch_q4s_q8_0;
+  if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_BF16) return mma_launch_q4s_bf16;
   return nullptr;
 }
 
@@ -76,6 +86,8 @@ int mma_occupancy(int kc, int vc, int head_dim, int group) {
     else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q8_0_q8_0(head_dim, group);
     else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q4s_q4s(head_dim, group);
     else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q8_0_q4s(head_dim, group);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q4s_q8_0(head_dim, group);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_BF16) n = mma_occupancy_q4s_bf16(head_dim, group);
     slot = n > 0 ? n : 1;
   }
   return slot;
@@ -344,12 +356,12 @@ namespace {
 kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, const kvq_store* k_store,
                        const kvq_store* v_store, const int32_t* seq_lens, int32_t* seq_lens_adv,
                        const int32_t* page_table, int max_pages, kvq_codec codec, float* out,
-                       int batch, int num_q_heads, float softmax_scale, int max_len_hint,
+                       int batch, int num_q_heads, int tokens, float softmax_scale, int max_len_hint,
                        const kvq_decode_opts* opts, void* workspace, size_t workspace_bytes,
                        void* stream) {
   if (!q || !k_store || !v_store || !seq_lens || !page_table || !out || !workspace)
     return KVQ_ERR_INVALID_ARG;
-  if (batch < 1 || num_q_heads < 1 || max_pages < 1 || max_len_hint < 0)
+  if (batch < 1 || num_q_heads < 1 || tokens < 1 || max_pages < 1 || max_len_hint < 0)
     return KVQ_ERR_INVALID_ARG;
   const kvq_store_desc& kd = k_store->desc;
   const kvq_store_desc& vd = v_store->desc;
@@ -362,13 +374,17 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16)) return KVQ_ERR_INVALID_ARG;
   if (k_new && (!v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
-  const int group = num_q_heads / kd.num_kv_heads;
+  if ((long long)num_q_heads * tokens > (1 << 24)) return KVQ_ERR_INVALID_ARG;
+  // the kernels see tokens x heads query rows: row (h, i) of a KV head's group is virtual
+  // head h * tokens + i, which is where [B][Hq][tokens][D] puts it
+  const int rows = num_q_heads * tokens;
+  const int group = rows / kd.num_kv_heads;
   Plan p;
-  kvq_status st = make_plan(k_store, v_store, batch, num_q_heads, max_len_hint, opts, &p);
+  kvq_status st = make_plan(k_store, v_store, batch, rows, max_len_hint, opts, &p);
   if (st != KVQ_OK) return st;
   if (workspace_bytes < p.total) return KVQ_ERR_WORKSPACE;
   if (group > 16 || p.variant < 1 || p.variant > 2) return KVQ_ERR_UNSUPPORTED;
-  if (k_new && p.variant != 2) return KVQ_ERR_UNSUPPORTED;
+  if ((k_new || tokens > 1) && p.variant != 2) return KVQ_ERR_UNSUPPORTED;
   SimtFn sfn = simt_fn(kd.codec, vd.codec);
   MmaFn mfn = mma_fn(kd.codec, vd.codec);
   if (p.variant == 1 && !sfn) return KVQ_ERR_UNSUPPORTED;
@@ -382,8 +398,9 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
   a.page_table = page_table;
   a.max_pages = max_pages;
   a.batch = batch;
-  a.num_q_heads = num_q_heads;
+  a.num_q_heads = rows;
   a.group = group;
+  a.tokens = tokens;
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt((float)kd.head_dim);
   a.qk_scale_log2 = scale * 1.4426950408889634f;
   a.chunk_tokens = p.chunk_tokens;
@@ -421,8 +438,18 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
                             const kvq_decode_opts* opts, void* workspace,
                             size_t workspace_bytes, void* stream) {
   return decode_impl(q, nullptr, nullptr, k_store, v_store, seq_lens, nullptr, page_table, max_pages,
-                     codec, out, batch, num_q_heads, softmax_scale, max_len_hint, opts, workspace,
+                     codec, out, batch, num_q_heads, 1, softmax_scale, max_len_hint, opts, workspace,
                      workspace_bytes, stream);
+}
+
+kvq_status kvq_flash_decode_multi(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                                  const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                                  kvq_codec codec, float* out, int batch, int num_q_heads, int num_tokens,
+                                  float softmax_scale, int max_len_hint, const kvq_decode_opts* opts,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, nullptr, nullptr, k_store, v_store, seq_lens, nullptr, page_table, max_pages,
+                     codec, out, batch, num_q_heads, num_tokens, softmax_scale, max_len_hint, opts,
+                     workspace, workspace_bytes, stream);
 }
 
 kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void* v_new,
@@ -433,7 +460,7 @@ kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void*
                                    void* workspace, size_t workspace_bytes, void* stream) {
   if (!k_new || !v_new) return KVQ_ERR_INVALID_ARG;
   return decode_impl(q, k_new, v_new, k_store, v_store, seq_lens, advance ? seq_lens : nullptr,
-                     page_table, max_pages, codec, out, batch, num_q_heads, softmax_scale,
+                     page_table, max_pages, codec, out, batch, num_q_heads, 1, softmax_scale,
                      max_len_hint, opts, workspace, workspace_bytes, stream);
 }
 

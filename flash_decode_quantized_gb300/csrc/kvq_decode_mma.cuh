@@ -126,8 +126,10 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t x, uint32_t y) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 // Magic-number conversion of integer codes to f16: the bits 0x64 << 8 | u encode the
-// f16 value 1024 + u exactly (u < 1024).  The constant offset is not subtracted per
-// element; the MMAs remove it (see kBias8 / kBias4).
+// f16 value 1024 + u exactly (u < 1024).  V operands subtract the constant offset in f16
+// registers (exact); K operands keep it and the QK accumulator is seeded with
+// -offset * sum(q) of the block (kBias8 / kBias4K), so the offset must stay small
+// against the dot product it rides on.
 //
 // Signed bytes packed in `u_biased` (each byte already XORed with 0x80, i.e. q + 128)
 // to the f16 pair (1152 + q) of the two bytes named by `sel` (0x4X4Y picks bytes X, Y).
@@ -138,8 +140,16 @@ __device__ __forceinline__ uint32_t i8pair_raw(uint32_t u_biased, uint32_t sel) 
 __device__ __forceinline__ uint32_t u4pair_raw(uint32_t w) {
   return (w & 0x000F000Fu) | 0x64006400u;
 }
+// Nibble pair (bits 6-9 and 22-25 of w) holding u = q + 8 -> the f16 pair 8 + u/2 =
+// 12 + q/2 (0x48 << 8 is 8.0; the nibble lands in the top mantissa bits).  The K codes of
+// the 4-bit codec use this form: with the 1024-based one the seeded accumulator carried
+// ~1000x the block's dot product and the tensor-core accumulate lost its low bits
+// (score errors ~1e-3 in log2 units for keys of magnitude ~50).
+__device__ __forceinline__ uint32_t u4pair_half(uint32_t w) {
+  return (w & 0x03C003C0u) | 0x48004800u;
+}
 constexpr float kBias8 = 1152.0f;            // offset of i8pair_raw values
-constexpr float kBias4 = 1032.0f;            // offset of u4pair_raw values
+constexpr float kBias4K = 12.0f;             // offset of u4pair_half values (which carry q/2)
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -373,7 +383,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
 
   const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = a.group;
+  const int G = a.group;         // query heads (virtual: head x query token) per KV head
+  const int T = a.tokens;        // query tokens per sequence (1: plain decode)
   const int P = a.k.page_size;
 
   if (tid == 0) {
@@ -584,7 +595,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
     }
-    const float bias = KC == KVQ_CODEC_Q4S ? kBias4 : kBias8;
+    const float bias = KC == KVQ_CODEC_Q4S ? kBias4K : kBias8;
     const float k0 = -bias * __shfl_sync(0xffffffffu, part, 4 * (2 * i4));
     const float k1 = -bias * __shfl_sync(0xffffffffu, part, 4 * (2 * i4 + 1));
     if (ws == 0 && r == 0) kbs[(hg * C::NB + bb) * 4 + i4] = make_float2(k0, k1);
@@ -600,6 +611,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       for (int k = 0; k < 4; ++k) o[mt][n][k] = 0.0f;
   // reference max (warp-uniform) and this lane's partial sum for QK columns 2*i4, 2*i4+1
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  // softmax scale in log2 units; 4-bit K fragments carry q/2
+  const float qk_mul = a.qk_scale_log2 * (KC == KVQ_CODEC_Q4S ? 2.0f : 1.0f);
   int E = -100;                                                 // running V-scale exponent bound
   bool timed_out = false;
 
@@ -668,11 +681,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
               const float2 kb = kbs[(hg * C::NB + bb + h2) * 4 + i4];
               float cb[4] = {kb.x, kb.y, kb.x, kb.y};
               uint32_t af[4];
-              af[0] = u4pair_raw(ra); af[1] = u4pair_raw(rb);
-              af[2] = u4pair_raw(ra >> 4); af[3] = u4pair_raw(rb >> 4);
+              af[0] = u4pair_half(ra << 6); af[1] = u4pair_half(rb << 6);
+              af[2] = u4pair_half(ra << 2); af[3] = u4pair_half(rb << 2);
               mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
-              af[0] = u4pair_raw(ra >> 8); af[1] = u4pair_raw(rb >> 8);
-              af[2] = u4pair_raw(ra >> 12); af[3] = u4pair_raw(rb >> 12);
+              af[0] = u4pair_half(ra >> 2); af[1] = u4pair_half(rb >> 2);
+              af[2] = u4pair_half(ra >> 6); af[3] = u4pair_half(rb >> 6);
               mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
               sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
               sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);
@@ -690,10 +703,21 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
         }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) sc[k] *= a.qk_scale_log2;
+      for (int k = 0; k < 4; ++k) sc[k] *= qk_mul;
       if (partial) {
         if (r >= n_valid) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
         if (r + 8 >= n_valid) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+      }
+      if (T > 1 && pos_w + 16 > L - T + 1) {
+        // causal limit of the query tokens (virtual head v = head * T + i sees the positions
+        // below L - T + 1 + i): only the sequence's last T - 1 positions are masked
+        const int cA = 2 * i4, cB = 2 * i4 + 1;   // this lane's QK columns
+        const int vA = hg * 8 + (GW <= 4 ? (cA & 3) : cA), vB = hg * 8 + (GW <= 4 ? (cB & 3) : cB);
+        const int limA = L - T + 1 + vA % T, limB = L - T + 1 + vB % T;
+        if (pos_w + r >= limA) sc[0] = -INFINITY;
+        if (pos_w + r >= limB) sc[1] = -INFINITY;
+        if (pos_w + r + 8 >= limA) sc[2] = -INFINITY;
+        if (pos_w + r + 8 >= limB) sc[3] = -INFINITY;
       }
 
       // ---------------- V scales of this lane's PV tokens (2i, 2i+1, 2i+8, 2i+9)
@@ -749,11 +773,18 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
         m1 = mn1;
         E = E_new;
       }
-      // m0, m1 are finite here: the warp has a valid token, whose score raised them
-      const float p0 = fast_exp2(sc[0] - m0);
-      const float p1 = fast_exp2(sc[1] - m1);
-      const float p2 = fast_exp2(sc[2] - m0);
-      const float p3 = fast_exp2(sc[3] - m1);
+      // m0, m1 are finite here unless a causal limit masked a column everywhere so far: the
+      // warp has a valid token, whose score raised them
+      float p0 = fast_exp2(sc[0] - m0);
+      float p1 = fast_exp2(sc[1] - m1);
+      float p2 = fast_exp2(sc[2] - m0);
+      float p3 = fast_exp2(sc[3] - m1);
+      if (T > 1) {
+        if (sc[0] == -INFINITY) p0 = 0.0f;
+        if (sc[1] == -INFINITY) p1 = 0.0f;
+        if (sc[2] == -INFINITY) p2 = 0.0f;
+        if (sc[3] == -INFINITY) p3 = 0.0f;
+      }
       l0 += p0 + p2;
       l1 += p1 + p3;
 

@@ -72,8 +72,10 @@ struct DecodeArgs {
   const int32_t* page_table;   // [B][max_pages]
   int max_pages;
   int batch;
-  int num_q_heads;
-  int group;                   // Hq / Hkv
+  int num_q_heads;             // query rows per sequence: Hq * tokens
+  int group;                   // query rows per KV head: (Hq / Hkv) * tokens
+  int tokens;                  // query tokens per sequence; q/out are [B][Hq][tokens][D] and
+                               // query token i attends to positions < seq_len - tokens + 1 + i
   float qk_scale_log2;         // softmax scale * log2(e)
   int chunk_tokens;            // split-K chunk length
   int n_chunks;                // chunks per (sequence, kv head)

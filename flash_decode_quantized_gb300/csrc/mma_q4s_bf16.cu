@@ -1,0 +1,12 @@
+// Tensor-core decode kernels for K=Q4S, V=BF16 (instantiations of kvq_decode_mma.cuh).
+#include "kvq_decode_mma.cuh"
+
+namespace kvq {
+cudaError_t mma_launch_q4s_bf16(const DecodeArgs& a, int head_dim, const CUtensorMap& tmk,
+                            const CUtensorMap& tmv, cudaStream_t stream) {
+  return mma::launch_pair<KVQ_CODEC_Q4S, KVQ_CODEC_BF16>(a, head_dim, tmk, tmv, stream);
+}
+int mma_occupancy_q4s_bf16(int head_dim, int group) {
+  return mma::occupancy_pair<KVQ_CODEC_Q4S, KVQ_CODEC_BF16>(head_dim, group);
+}
+}  // namespace kvq

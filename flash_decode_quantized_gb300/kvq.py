@@ -64,6 +64,8 @@ def _load():
         "kvq_flash_decode_static_ws": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
                                        ctypes.POINTER(DecodeOpts), V],
         "kvq_dequantize": [P, P, P, P, I, I, V],
+        "kvq_flash_decode_multi": [P, P, P, P, P, I, CodecPair, P, I, I, I, ctypes.c_float, I,
+                                   ctypes.POINTER(DecodeOpts), P, Z, V],
         "kvq_flash_decode_append": [P, P, P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I, I,
                                     ctypes.POINTER(DecodeOpts), P, Z, V],
     }
@@ -237,6 +239,33 @@ def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: 
                                 int(max_len_hint), _opts(chunk_tokens, variant),
                                 _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                 _stream(stream)), "kvq_flash_decode")
+    return out
+
+
+def kvq_flash_decode_multi(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: torch.Tensor,
+                           page_table: torch.Tensor, out: torch.Tensor | None = None,
+                           softmax_scale: float = 0.0, max_len_hint: int | None = None,
+                           workspace: torch.Tensor | None = None, chunk_tokens: int = 0,
+                           variant: int = 0, stream=None) -> torch.Tensor:
+    """q: bf16 [B, Hq, T, D] (T query tokens per sequence, the last T positions being the
+    drafts) -> out fp32 [B, Hq, T, D]; token i attends to positions < seq_len - T + 1 + i."""
+    bsz, hq, t, dim = q.shape
+    max_pages = page_table.shape[1]
+    if max_len_hint is None:
+        max_len_hint = max_pages * k_store.page_size
+    if out is None:
+        out = torch.empty((bsz, hq, t, dim), dtype=torch.float32, device=q.device)
+    need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq * t, max_len_hint, chunk_tokens, variant)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
+    _check(lib.kvq_flash_decode_multi(_ptr(q, torch.bfloat16, "q"), k_store.handle, v_store.handle,
+                                      _ptr(seq_lens, torch.int32, "seq_lens"),
+                                      _ptr(page_table, torch.int32, "page_table"), max_pages, codec,
+                                      _ptr(out, torch.float32, "out"), bsz, hq, t, float(softmax_scale),
+                                      int(max_len_hint), _opts(chunk_tokens, variant),
+                                      _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                      _stream(stream)), "kvq_flash_decode_multi")
     return out
 
 

@@ -90,7 +90,10 @@ typedef struct kvq_store_desc {
   int32_t num_pages;
 } kvq_store_desc;
 
-/* Codec pair a decode call expects; must equal the codecs of the stores passed. */
+/* Codec pair a decode call expects; must equal the codecs of the stores passed.
+ * Built pairs (K/V): bf16/bf16, f16/f16 (16-bit controls), q8_0/bf16 (K-only
+ * quantization), q8_0/q8_0, q4s/q4s, q8_0/q4s, q4s/q8_0, q4s/bf16 (the mixed K/V precision
+ * families of rMLX issue #292, correction table); others give KVQ_ERR_UNSUPPORTED. */
 typedef struct kvq_codec {
   int32_t k;                 /* kvq_codec_id of the K store */
   int32_t v;                 /* kvq_codec_id of the V store */
@@ -187,6 +190,27 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
                             float softmax_scale, int max_len_hint,
                             const kvq_decode_opts* opts, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* Decode of several query tokens per sequence against the same cache (speculative-draft
+ * verification: halobench record clm-0022's shipped configuration drafts several tokens
+ * per step, its --spec-draft-n-max note): the last num_tokens positions of each sequence are the
+ * drafts, and query token i attends to positions [0, seq_lens[b] - num_tokens + i]
+ * (causal among the drafts).  Every KV tile is read once for all of them.
+ *   q    device bf16 [batch][num_q_heads][num_tokens][head_dim]
+ *   out  device fp32 [batch][num_q_heads][num_tokens][head_dim]
+ *   seq_lens[b] >= num_tokens (it counts the drafts, already appended with kvq_append_kv).
+ * The workspace must hold kvq_decode_workspace_bytes(..., num_q_heads * num_tokens, ...).
+ * Needs (num_q_heads / num_kv_heads) * num_tokens <= 16 and the tensor-core kernel
+ * (opts->variant 0 or 2), else KVQ_ERR_UNSUPPORTED.  num_tokens == 1 is kvq_flash_decode.
+ * A sequence shorter than num_tokens attends as if its drafts started at position 0
+ * (query i sees positions below i + 1 - num_tokens + seq_lens[b], none if that is <= 0,
+ * giving zeros). */
+kvq_status kvq_flash_decode_multi(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                                  const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                                  kvq_codec codec, float* out, int batch, int num_q_heads,
+                                  int num_tokens, float softmax_scale, int max_len_hint,
+                                  const kvq_decode_opts* opts, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /* One decode step with the append fused in (a1 followed by a2..a8, one launch of the
  * tensor-core kernel; the on-device append of rMLX issue #295 "Fix direction" done by

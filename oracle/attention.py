@@ -86,3 +86,22 @@ def attend_one_split(q, k, v, scale, chunk: int) -> np.ndarray:
     n = k.shape[0]
     bounds = [(lo, min(lo + chunk, n)) for lo in range(0, n, chunk)]
     return combine(partials(q, k, v, scale, bounds), v.shape[1])
+
+
+def attend_tokens(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Several query tokens of one head against one sequence whose last T positions are
+    those tokens (speculative drafts, verified together): query i (of T) attends to the
+    positions [0, L - T + i], i.e. causal among the drafts.
+
+    q: float64 [T, D]; k, v: float64 [L, D] -> [T, D].  Query i is ``attend_one`` on the
+    first L - T + 1 + i positions (zeros where that count is <= 0).
+    """
+    T = q.shape[0]
+    L = k.shape[0]
+    out = np.zeros((T, v.shape[1]))
+    for i in range(T):
+        n = L - T + 1 + i
+        if n > 0:
+            out[i] = attend_one(q[i], k[:n], v[:n], scale)
+    return out
+

@@ -13,7 +13,7 @@ from workloads import make_inputs, ragged_lengths
 pytestmark = pytest.mark.gpu
 
 PAIRS = [("bf16", "bf16"), ("f16", "f16"), ("q8_0", "bf16"), ("q8_0", "q8_0"),
-         ("q4s", "q4s"), ("q8_0", "q4s")]
+         ("q4s", "q4s"), ("q8_0", "q4s"), ("q4s", "q8_0"), ("q4s", "bf16")]
 VARIANTS = [1, 2]
 
 
@@ -209,3 +209,15 @@ def test_resident_append_decode_loop(kc, vc):
         sub.v_rows[0] = inp.v_rows[0][:L]
         sub.q = inp.q
         assert_close(got, oracle_out(sub, kc, vc), f"step {step}")
+
+
+@pytest.mark.parametrize("kc,vc", PAIRS)
+def test_heavy_tailed_large_magnitude_keys(kc, vc):
+    # Student-t keys and values times per-channel scales up to 4 (blocks with amax ~ 50+):
+    # the integer-code offsets must not cost precision (a 1024-based 4-bit K fragment with
+    # a seeded accumulator missed the tolerance here)
+    inp = make_inputs([3000, 1200], 32, 8, 128, seed=97, dist="t3", channel_scaled=True)
+    ks, vs = build_store(inp, kc, "k"), build_store(inp, vc, "v")
+    q, seq, pt = device_inputs(inp)
+    got = kvq().kvq_flash_decode(q, ks, vs, seq, pt).cpu().numpy()
+    assert_close(got, oracle_out(inp, kc, vc), f"{kc}/{vc}")

@@ -12,7 +12,7 @@ from workloads import make_inputs
 pytestmark = pytest.mark.gpu
 
 PAIRS = [("q8_0", "q8_0"), ("q8_0", "q4s"), ("q4s", "q4s"), ("q8_0", "bf16"), ("bf16", "bf16"),
-         ("f16", "f16")]
+         ("f16", "f16"), ("q4s", "q8_0"), ("q4s", "bf16")]
 
 
 def prefix_stores(inp, kc, vc, prefix):

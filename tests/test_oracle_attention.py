@@ -117,3 +117,39 @@ def test_zero_length_sequence_in_batch():
     vs = [np.zeros((0, 1, 8)), rng.normal(size=(5, 1, 8))]
     out = attention.attention(q, ks, vs, 1)
     assert np.all(out[0] == 0) and np.all(np.isfinite(out[1]))
+
+
+def test_attend_tokens_hand_case():
+    # all scores equal: each draft query averages the positions it may see.  L = 3, T = 2:
+    # query 0 sees positions 0..1 (mean of 1, 3 = 2), query 1 sees 0..2 (mean of 1, 3, 8 = 4)
+    q = np.array([[0.7], [-1.2]])
+    k = np.zeros((3, 1))
+    v = np.array([[1.0], [3.0], [8.0]])
+    out = attention.attend_tokens(q, k, v, 1.0)
+    assert out[0, 0] == pytest.approx(2.0, abs=1e-15)
+    assert out[1, 0] == pytest.approx(4.0, abs=1e-15)
+
+
+def test_attend_tokens_reduces_to_attend_one():
+    rng = np.random.default_rng(7)
+    k, v = rng.standard_normal((40, 16)), rng.standard_normal((40, 16))
+    q = rng.standard_normal((5, 16))
+    out = attention.attend_tokens(q, k, v, 0.25)
+    # the last draft sees the whole sequence; T = 1 is single-token decode
+    np.testing.assert_allclose(out[4], attention.attend_one(q[4], k, v, 0.25), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(attention.attend_tokens(q[:1], k, v, 0.25)[0],
+                               attention.attend_one(q[0], k, v, 0.25), rtol=0, atol=1e-14)
+    # draft i equals a single-token decode of the sequence cut after position L - T + i
+    for i in range(5):
+        np.testing.assert_allclose(out[i], attention.attend_one(q[i], k[:36 + i], v[:36 + i], 0.25),
+                                   rtol=0, atol=1e-14)
+
+
+def test_attend_tokens_sequence_shorter_than_drafts():
+    # L = 1, T = 3: queries 0 and 1 see nothing (zeros), query 2 sees position 0
+    q = np.ones((3, 2))
+    k = np.ones((1, 2))
+    v = np.array([[5.0, -2.0]])
+    out = attention.attend_tokens(q, k, v, 1.0)
+    assert np.array_equal(out[0], [0.0, 0.0]) and np.array_equal(out[1], [0.0, 0.0])
+    np.testing.assert_array_equal(out[2], [5.0, -2.0])
