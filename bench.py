@@ -267,6 +267,23 @@ class Layer:
         return kvq.kvq_flash_decode(self.q, self.kd, self.vd, self.seq_lens, self.page_table, out=self.out,
                                     max_len_hint=self.hint, workspace=self.ws16)
 
+    def multi(self, tokens):
+        """Decode of `tokens` query tokens per sequence (the last `tokens` positions being
+        drafts) with kvq_flash_decode_multi."""
+        kvq, torch = self.kvq, self.torch
+        key = f"_multi{tokens}"
+        if not hasattr(self, key):
+            q = torch.randn((self.batch, self.hq, tokens, self.d), device="cuda").to(torch.bfloat16)
+            n = kvq.kvq_decode_workspace_bytes(self.k_store, self.v_store, self.batch, self.hq * tokens,
+                                               self.hint, 0, 0)
+            ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+            kvq.kvq_decode_workspace_init(ws)
+            out = torch.empty((self.batch, self.hq, tokens, self.d), dtype=torch.float32, device="cuda")
+            setattr(self, key, (q, ws, out))
+        q, ws, out = getattr(self, key)
+        return kvq.kvq_flash_decode_multi(q, self.k_store, self.v_store, self.seq_lens, self.page_table,
+                                          out=out, max_len_hint=self.hint, workspace=ws)
+
     def kv_bytes(self):
         return sum(self.host_lens) * self.hkv * token_head_bytes(f"{self.kc}/{self.vc}", self.d)
 
@@ -481,6 +498,22 @@ def run_extras(torch, kvq, args, flush, peak):
             out.append(row)
             del layer
             torch.cuda.empty_cache()
+    # speculative-draft verification: T query tokens per sequence in one decode, against
+    # T single-token decodes of the same cache (8B-class layer, 65536 tokens, q8_0 K+V)
+    layer = Layer(kvq, torch, WORKLOADS["layer8b"], "q8_0/q8_0", [65536], 0, seed=91)
+    layer.prepare(args.variant, 0)
+    time_decode_only(torch, layer, flush, 3)
+    one = statistics.median(time_decode_only(torch, layer, flush, 10))
+    for T in (2, 4):
+        fn = (lambda T=T: layer.multi(T))
+        time_decode_only(torch, layer, flush, 3, fn)
+        ms = statistics.median(time_decode_only(torch, layer, flush, 10, fn))
+        out.append({"workload": "spec_verify", "kv_len": 65536, "codec": "q8_0/q8_0", "query_tokens": T,
+                    "us": round(ms * 1e3, 2), "single_token_us": round(one * 1e3, 2),
+                    "vs_T_single_decodes": round(ms / (T * one), 3),
+                    "gbs": round(layer.kv_bytes() / (ms * 1e-3) / 1e9, 1)})
+    del layer
+    torch.cuda.empty_cache()
     from workloads import ragged_lengths
     lens = [int(x) for x in ragged_lengths(1234, 64)]
     for arm in ("q8_0/q8_0", "q4s/q4s"):

@@ -83,8 +83,8 @@ def test_host_argument_checks():
         k.kvq_flash_decode(q[:, :7].contiguous(), ks, vs, sl, pt, max_len_hint=64)
     assert e.value.status == k.KVQ_ERR_INVALID_ARG
     with pytest.raises(k.KvqError) as e:   # unsupported pair (no kernel built for it)
-        k4 = k.kvq_store_create("q4s", 2, 128, 256, inp.num_pages)
-        vb = k.kvq_store_create("bf16", 2, 128, 256, inp.num_pages)
+        k4 = k.kvq_store_create("bf16", 2, 128, 256, inp.num_pages)   # 16-bit K, quantized V
+        vb = k.kvq_store_create("q8_0", 2, 128, 256, inp.num_pages)
         k.kvq_flash_decode(q, k4, vb, sl, pt, max_len_hint=64)
     assert e.value.status == k.KVQ_ERR_UNSUPPORTED
     with pytest.raises(k.KvqError) as e:   # store buffer too small
