@@ -309,6 +309,21 @@ def gpu_lead(torch):
     torch.cuda._sleep(200_000)
 
 
+def max_over_ranks(torch, x: float, world: int, device) -> float:
+    """The slowest rank's value (all ranks call this; a no-op on one process)."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(kv_bytes_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job effective KV GB/s: every replica reads kv_bytes_per_rank per step, and a
+    step takes the slowest rank's time."""
+    return world * kv_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def time_decode_only(torch, layer, flush, iters, fn=None):
     fn = fn or layer.decode
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
@@ -363,19 +378,17 @@ def run_mine(args, rank, world):
             kv_bytes.append(layer.kv_bytes())
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
     launches = kvq.kvq_launch_count() - launches0
     step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     # the step is the one fused kernel (the CUDA-core variant: append + decode + combine)
     dec_ms = step_ms
     # median over the K per-step event pairs (mean and worst step reported beside it): an
     # nvidia-smi sample landing inside one step can stall that step by ~100 us
-    ms_per_step = statistics.median(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_per_step], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(torch, statistics.median(step_ms), world, "cuda")
     kvb = statistics.mean(kv_bytes)
-    value = world * kvb / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(kvb, world, ms_per_step)
     peak, peak_kind = hbm_peak()
     dec_mean = statistics.median(dec_ms)
     achieved = kvb / (dec_mean * 1e-3) / 1e9
