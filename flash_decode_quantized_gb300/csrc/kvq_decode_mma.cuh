@@ -169,19 +169,32 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     return __half22float2(*reinterpret_cast<__half2*>(&v));
   }
 }
+// y = x + k * h for the two 16-bit halves h of hp (k a 16-bit constant): one mixed-precision
+// FMA per value, exact for k = -1 when h is x rounded (Sterbenz).
+template <bool BF16>
+__device__ __forceinline__ void add_k_times(uint32_t hp, unsigned short k, float x0, float x1, float& y0, float& y1) {
+  if constexpr (BF16)
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n fma.rn.f32.bf16 %0, l, %3, %4;\n fma.rn.f32.bf16 %1, h, %3, %5;\n}"
+        : "=f"(y0), "=f"(y1) : "r"(hp), "h"(k), "f"(x0), "f"(x1));
+  else
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n fma.rn.f32.f16 %0, l, %3, %4;\n fma.rn.f32.f16 %1, h, %3, %5;\n}"
+        : "=f"(y0), "=f"(y1) : "r"(hp), "h"(k), "f"(x0), "f"(x1));
+}
 // x -> (hi, lo) pairs with hi = round(x), lo = round(x - hi), for two values.
 template <bool BF16>
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   hi = pack2<BF16>(x0, x1);
-  const float2 h = unpack2<BF16>(hi);
-  lo = pack2<BF16>(x0 - h.x, x1 - h.y);
+  float y0, y1;
+  add_k_times<BF16>(hi, BF16 ? 0xBF80 : 0xBC00, x0, x1, y0, y1);
+  lo = pack2<BF16>(y0, y1);
 }
 
-// (x0, x1) -> f16/bf16 pair of x (lo_sel = 0: the hi part) or of x - hi (lo_sel = 1).
+// (x0, x1) -> f16/bf16 pair of x (neg_sel = 0: the hi part) or of x - hi (neg_sel = -1).
 template <bool BF16>
-__device__ __forceinline__ uint32_t hi_or_lo(float x0, float x1, float lo_sel) {
-  const float2 h = unpack2<BF16>(pack2<BF16>(x0, x1));
-  return pack2<BF16>(fmaf(-lo_sel, h.x, x0), fmaf(-lo_sel, h.y, x1));
+__device__ __forceinline__ uint32_t hi_or_lo(float x0, float x1, unsigned short neg_sel) {
+  float y0, y1;
+  add_k_times<BF16>(pack2<BF16>(x0, x1), neg_sel, x0, x1, y0, y1);
+  return pack2<BF16>(y0, y1);
 }
 
 // The NB fp16 scales of tile row t (a contiguous NB*2-byte run) as NB/2 packed words.
@@ -808,7 +821,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       for (int u = 0; u < 4; ++u) pv[u] *= pscale;
       // PV column r of an 8-column tile is head r&3's hi part (r < 4) or lo part (r >= 4)
       // when one n-tile carries both; lo lanes feed x - f16(x) instead of x.
-      const float lo_sel = (C::NPV == 1 && r >= 4) ? 1.0f : 0.0f;
+      const unsigned short lo_sel = (C::NPV == 1 && r >= 4) ? (C::VBF ? 0xBF80 : 0xBC00) : 0;
       if constexpr (C::VQ) {
         uint32_t vq4[4];   // q4s: one ldmatrix.x4 covers blocks bb and bb + 1 (bb even)
 #pragma unroll
