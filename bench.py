@@ -324,6 +324,28 @@ def job_gbs(kv_bytes_per_rank: float, world: int, ms_per_step: float) -> float:
     return world * kv_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
+def read_probe_gbs(torch, kvq, flush, gib: float = 2.0) -> float:
+    """Achievable read bandwidth on this GPU now: kvq_read_probe over a `gib` GiB buffer
+    (16x the L2), median of 10 event-timed launches."""
+    buf = torch.ones(int(gib * (1 << 30)) // 16 * 16, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ms = []
+    for it in range(12):
+        flush()
+        gpu_lead(torch)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kvq.kvq_read_probe(buf, sink)
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= 2:
+            ms.append(e0.elapsed_time(e1))
+    n = buf.numel()
+    del buf
+    torch.cuda.empty_cache()
+    return n / (statistics.median(ms) * 1e-3) / 1e9
+
+
 def time_decode_only(torch, layer, flush, iters, fn=None):
     fn = fn or layer.decode
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
@@ -353,6 +375,7 @@ def run_mine(args, rank, world):
     layer = Layer(kvq, torch, wl, codec, seq_lens, extra, seed=1000 + rank)
     layer.prepare(args.variant, args.chunk_tokens)
     flush = l2_flusher(torch)
+    probe = read_probe_gbs(torch, kvq, flush)
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
@@ -402,7 +425,8 @@ def run_mine(args, rank, world):
                 "decode_us_p10_p90": [round(float(np.percentile(dec_ms, 10)) * 1e3, 2),
                                       round(float(np.percentile(dec_ms, 90)) * 1e3, 2)],
                 "cv": round(statistics.pstdev(dec_ms) / statistics.mean(dec_ms), 4),
-                "stat": "median of per-step CUDA-event times"}
+                "stat": "median of per-step CUDA-event times",
+                "read_probe_gbs": round(probe, 1), "frac_of_read_probe": round(achieved / probe, 4)}
 
     e2e = measure_e2e(torch, kvq, layer, flush, max(3, min(K, 20)))
     e2e["value"] = round(world * e2e.pop("kvb") / (e2e["ms"] * 1e-3) / 1e9, 1)
@@ -423,8 +447,9 @@ def run_mine(args, rank, world):
                    "decode_us": round(statistics.mean(b.elapsed_time(c) for _, b, c in ev2) * 1e3, 2)}
 
     sweep = extras = None
-    if rank == 0 and not args.no_sweep and args.workload == "layer8b":
-        sweep = run_sweep(torch, kvq, args, flush, peak)
+    if rank == 0 and args.workload == "layer8b":
+        if not args.no_sweep:
+            sweep = run_sweep(torch, kvq, args, flush, peak)
         if not args.no_extras:
             extras = run_extras(torch, kvq, args, flush, peak)
 
@@ -511,6 +536,36 @@ def run_extras(torch, kvq, args, flush, peak):
             out.append(row)
             del layer
             torch.cuda.empty_cache()
+    # prefill-side bulk encode: one kvq_append_kv of a 65536-token prompt's K and V rows
+    # (8B-class layer shape) into fresh q8_0 / q4s stores, bf16 read + codes and scales written
+    wl8 = WORKLOADS["layer8b"]
+    for arm in ("q8_0/q8_0", "q4s/q4s"):
+        kc, vc = arm.split("/")
+        n = 65536
+        pages = n // 256
+        ks = kvq.kvq_store_create(kc, wl8["hkv"], wl8["d"], 256, pages)
+        vs = kvq.kvq_store_create(vc, wl8["hkv"], wl8["d"], 256, pages)
+        rows_k = torch.randn((1, n, wl8["hkv"], wl8["d"]), device="cuda").to(torch.bfloat16)
+        rows_v = torch.randn((1, n, wl8["hkv"], wl8["d"]), device="cuda").to(torch.bfloat16)
+        pt = torch.arange(pages, dtype=torch.int32, device="cuda")[None]
+        seq = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ev = []
+        for it in range(6):
+            flush()
+            gpu_lead(torch)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            kvq.kvq_append_kv(ks, vs, rows_k, rows_v, seq, pt, advance=False)
+            e1.record()
+            ev.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev[1:])
+        moved = 2 * rows_k.numel() * 2 + n * wl8["hkv"] * token_head_bytes(arm, wl8["d"])
+        out.append({"workload": "prefill_encode", "tokens": n, "codec": arm, "us": round(ms * 1e3, 2),
+                    "gbs_moved": round(moved / (ms * 1e-3) / 1e9, 1),
+                    "note": "bf16 K and V rows read, codes and scales written, one launch"})
+        del ks, vs, rows_k, rows_v
+        torch.cuda.empty_cache()
     # speculative-draft verification: T query tokens per sequence in one decode, against
     # T single-token decodes of the same cache (8B-class layer, 65536 tokens, q8_0 K+V)
     layer = Layer(kvq, torch, WORKLOADS["layer8b"], "q8_0/q8_0", [65536], 0, seed=91)

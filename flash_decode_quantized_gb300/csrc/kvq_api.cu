@@ -303,7 +303,7 @@ kvq_status kvq_append(kvq_store* store, const void* rows, int n_new, int batch,
   if (!store || !seq_lens || !page_table || batch < 1 || n_new < 0 || max_pages < 1)
     return KVQ_ERR_INVALID_ARG;
   if (n_new == 0) return KVQ_OK;
-  if (!rows || !aligned(rows, 2)) return KVQ_ERR_INVALID_ARG;
+  if (!rows || !aligned(rows, 16)) return KVQ_ERR_INVALID_ARG;
   return from_cuda(launch_append(store, static_cast<const __nv_bfloat16*>(rows), n_new, batch,
                                  seq_lens, page_table, max_pages, static_cast<cudaStream_t>(stream)));
 }
@@ -318,7 +318,7 @@ kvq_status kvq_append_kv(kvq_store* k_store, kvq_store* v_store, const void* k_r
   if (kd.num_kv_heads != vd.num_kv_heads || kd.head_dim != vd.head_dim || kd.page_size != vd.page_size)
     return KVQ_ERR_INVALID_ARG;
   if (n_new == 0) return KVQ_OK;
-  if (!k_rows || !v_rows || !aligned(k_rows, 2) || !aligned(v_rows, 2)) return KVQ_ERR_INVALID_ARG;
+  if (!k_rows || !v_rows || !aligned(k_rows, 16) || !aligned(v_rows, 16)) return KVQ_ERR_INVALID_ARG;
   return from_cuda(launch_append_kv(k_store, v_store, static_cast<const __nv_bfloat16*>(k_rows),
                                     static_cast<const __nv_bfloat16*>(v_rows), n_new, batch, seq_lens, page_table,
                                     max_pages, advance ? 1 : 0, static_cast<cudaStream_t>(stream)));

@@ -7,6 +7,8 @@
 //
 // One warp encodes one row (one token of one KV head) with encode_row.
 
+#include <climits>
+
 #include "kvq_encode.cuh"
 #include "kvq_internal.cuh"
 
@@ -63,10 +65,91 @@ append_kv_kernel(StoreView ks, StoreView vs, const __nv_bfloat16* __restrict__ k
   }
 }
 
+// Bulk encode (prompt-sized appends).  A CTA takes kBulkPos consecutive new positions of
+// one sequence and encodes their rows for every KV head (for both stores with TWO).
+constexpr int kBulkPos = 16;
+constexpr int kBulkRows = 4;
+constexpr int kBulkThreads = 256;
+
+template <int KC, int VC, int EPL, bool TWO>
+__global__ void __launch_bounds__(kBulkThreads)
+append_bulk_kernel(StoreView ks, StoreView vs, const __nv_bfloat16* __restrict__ k_rows,
+                   const __nv_bfloat16* __restrict__ v_rows, int n_new, const int32_t* __restrict__ seq_lens,
+                   const int32_t* __restrict__ page_table, int max_pages) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int D = EPL * 32;
+  constexpr int NW = kBulkThreads / 32;
+  const int b = blockIdx.y, i0 = blockIdx.x * kBulkPos;
+  const int H = ks.num_kv_heads;
+  const int P = ks.page_size;
+  const int npos = min(kBulkPos, n_new - i0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long base = seq_lens[b];
+  const long long cap = min((long long)max_pages * P, (long long)INT_MAX);
+  // one warp per position: its page is looked up once, then every KV head's K and V rows
+  // are encoded, kBulkRows rows' loads in flight at a time (no integer divisions per row)
+  for (int ip = warp; ip < npos; ip += NW) {
+    const int i = i0 + ip;
+    const long long pos_ll = base + i;
+    if (base < 0 || pos_ll >= cap) {
+      if (lane == 0) {
+        record_fault(ks.status, KVQ_DEVICE_BAD_POSITION);
+        if (TWO) record_fault(vs.status, KVQ_DEVICE_BAD_POSITION);
+      }
+      continue;
+    }
+    const int pos = (int)pos_ll;
+    const int page = page_table[(long long)b * max_pages + pos / P];
+    const int r = pos % P;
+    const long long row0 = ((long long)b * n_new + i) * H;   // row of head 0 of this position
+#pragma unroll
+    for (int which = 0; which < (TWO ? 2 : 1); ++which) {
+      const StoreView& st = which ? vs : ks;
+      if (page < 0 || page >= st.num_pages) {
+        if (lane == 0) record_fault(st.status, KVQ_DEVICE_BAD_PAGE);
+        continue;
+      }
+      const __nv_bfloat16* src = (which ? v_rows : k_rows) + row0 * D;
+      for (int h0 = 0; h0 < H; h0 += kBulkRows) {
+        float x[kBulkRows][EPL];
+#pragma unroll
+        for (int u = 0; u < kBulkRows; ++u)
+          if (h0 + u < H) load_row<EPL>(src + (long long)(h0 + u) * D, lane, x[u]);
+#pragma unroll
+        for (int u = 0; u < kBulkRows; ++u) {
+          if (h0 + u >= H) break;
+          if (which) store_row<VC, EPL>(vs, page, r, h0 + u, x[u]);
+          else store_row<KC, EPL>(ks, page, r, h0 + u, x[u]);
+        }
+      }
+    }
+  }
+}
+
+template <int KC, int VC, bool TWO>
+cudaError_t launch_bulk(const kvq_store* ks, const kvq_store* vs, const __nv_bfloat16* k_rows,
+                        const __nv_bfloat16* v_rows, int n_new, int batch, const int32_t* seq_lens,
+                        const int32_t* page_table, int max_pages, cudaStream_t stream) {
+  const dim3 grid((unsigned)((n_new + kBulkPos - 1) / kBulkPos), batch);
+  const StoreView kv = view_of(ks), vv = view_of(TWO ? vs : ks);
+  cudaError_t e;
+  switch (ks->desc.head_dim) {
+    case 64: e = launch_pdl(append_bulk_kernel<KC, VC, 2, TWO>, grid, dim3(kBulkThreads), 0, stream, kv, vv, k_rows, v_rows, n_new, seq_lens, page_table, max_pages); break;
+    case 128: e = launch_pdl(append_bulk_kernel<KC, VC, 4, TWO>, grid, dim3(kBulkThreads), 0, stream, kv, vv, k_rows, v_rows, n_new, seq_lens, page_table, max_pages); break;
+    case 256: e = launch_pdl(append_bulk_kernel<KC, VC, 8, TWO>, grid, dim3(kBulkThreads), 0, stream, kv, vv, k_rows, v_rows, n_new, seq_lens, page_table, max_pages); break;
+    default: return cudaErrorNotSupported;
+  }
+  count_launch();
+  return e;
+}
+
 template <int CODEC>
 cudaError_t launch_codec(const kvq_store* s, const __nv_bfloat16* rows, int n_new, int batch,
                          const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                          cudaStream_t stream) {
+  if (n_new >= kBulkPos)   // prompt-sized: rows of a sequence's positions per CTA
+    return launch_bulk<CODEC, CODEC, false>(s, s, rows, rows, n_new, batch, seq_lens, page_table, max_pages, stream);
   const long long n_rows = (long long)batch * n_new * s->desc.num_kv_heads;
   const unsigned grid = (unsigned)((n_rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
   const StoreView v = view_of(s);
@@ -107,6 +190,12 @@ template <int KC, int VC>
 cudaError_t launch_kv_pair(const kvq_store* ks, const kvq_store* vs, const __nv_bfloat16* k_rows,
                            const __nv_bfloat16* v_rows, int n_new, int batch, int32_t* seq_lens,
                            const int32_t* page_table, int max_pages, int advance, cudaStream_t stream) {
+  if (n_new >= kBulkPos) {   // prompt-sized: the bulk kernel, then the advance
+    cudaError_t e = launch_bulk<KC, VC, true>(ks, vs, k_rows, v_rows, n_new, batch, seq_lens, page_table,
+                                              max_pages, stream);
+    if (e != cudaSuccess || !advance) return e;
+    return launch_seq_lens_add(seq_lens, batch, n_new, stream);
+  }
   const long long slots = 2LL * n_new * ks->desc.num_kv_heads;   // warps per sequence
   const int warps = (int)(slots < 16 ? slots : 16);
   const unsigned gx = (unsigned)((slots + warps - 1) / warps);

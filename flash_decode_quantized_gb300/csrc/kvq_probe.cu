@@ -1,0 +1,56 @@
+// Read-only bandwidth probe: a measurement utility, not a step of the method.  Reads every
+// 16-byte word of a buffer once (streaming loads that do not allocate in L1) with a grid
+// of resident CTAs and four loads in flight per thread; the XOR of the words reaches
+// `sink` only if it equals a constant no real buffer produces, so the loads stay live.
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kProbeThreads = 512;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__global__ void __launch_bounds__(kProbeThreads) probe_kernel(const uint4* __restrict__ buf, long long n16,
+                                                              unsigned* sink) {
+  const long long stride = (long long)gridDim.x * kProbeThreads;
+  long long i = (long long)blockIdx.x * kProbeThreads + threadIdx.x;
+  unsigned acc = 0;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = ld_stream(buf + i), b = ld_stream(buf + i + stride);
+    const uint4 c = ld_stream(buf + i + 2 * stride), d = ld_stream(buf + i + 3 * stride);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 a = ld_stream(buf + i);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+  if (acc == 0x9E3779B9u) atomicAdd(sink, 1u);
+}
+
+}  // namespace
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" kvq_status kvq_read_probe(const void* buf, size_t bytes, void* sink, void* stream) {
+  if (!buf || !sink || bytes < 16 || (reinterpret_cast<uintptr_t>(buf) & 15) != 0) return KVQ_ERR_INVALID_ARG;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, probe_kernel, kProbeThreads, 0) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  const dim3 grid((unsigned)(sms * (per_sm > 0 ? per_sm : 1)));
+  probe_kernel<<<grid, kProbeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(buf), (long long)(bytes / 16), static_cast<unsigned*>(sink));
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}

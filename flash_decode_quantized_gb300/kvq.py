@@ -64,6 +64,7 @@ def _load():
         "kvq_flash_decode_static_ws": [P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I,
                                        ctypes.POINTER(DecodeOpts), V],
         "kvq_dequantize": [P, P, P, P, I, I, V],
+        "kvq_read_probe": [P, Z, P, V],
         "kvq_flash_decode_multi": [P, P, P, P, P, I, CodecPair, P, I, I, I, ctypes.c_float, I,
                                    ctypes.POINTER(DecodeOpts), P, Z, V],
         "kvq_flash_decode_append": [P, P, P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I, I,
@@ -332,6 +333,12 @@ def kvq_dequantize(src: Store, dst: Store, seq_lens: torch.Tensor, page_table: t
     _check(lib.kvq_dequantize(src.handle, dst.handle, _ptr(seq_lens, torch.int32, "seq_lens"),
                               _ptr(page_table, torch.int32, "page_table"), page_table.shape[1],
                               seq_lens.shape[0], _stream(stream)), "kvq_dequantize")
+
+
+def kvq_read_probe(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Reads every byte of the (contiguous, 16-byte aligned) device tensor `buf` once."""
+    _check(lib.kvq_read_probe(ctypes.c_void_p(buf.data_ptr()), buf.numel() * buf.element_size(),
+                              _ptr(sink, torch.int32, "sink"), _stream(stream)), "kvq_read_probe")
 
 
 def kvq_decode_workspace_init(workspace: torch.Tensor, stream=None) -> None:

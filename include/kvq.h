@@ -125,7 +125,7 @@ kvq_status kvq_destroy(kvq_store* store);
 
 /* Encode new rows into the store, on the device (a1: on-device encode of new K/V rows;
  * rMLX issue #295 "Fix direction").
- *   rows       device bf16 [batch][n_new][num_kv_heads][head_dim], contiguous.
+ *   rows       device bf16 [batch][n_new][num_kv_heads][head_dim], contiguous, 16-byte aligned.
  *   seq_lens   device int32 [batch]: row i of sequence b is written at position
  *              seq_lens[b] + i.  Not modified (see kvq_seq_lens_add).
  *   page_table device int32 [batch][max_pages].
@@ -157,6 +157,14 @@ kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
  * directly. */
 kvq_status kvq_dequantize(const kvq_store* src, kvq_store* dst, const int32_t* seq_lens,
                           const int32_t* page_table, int max_pages, int batch, void* stream);
+
+/* Read-only bandwidth probe (a measurement utility, not a step of the method): reads the
+ * `bytes` (>= 16, 16-byte aligned start; a tail below 16 bytes is not read) of device
+ * buffer `buf` once with streaming 16-byte loads from one full wave of CTAs.  `sink` is a
+ * device uint32 the kernel may increment (never for real data).  Time it with events on
+ * `stream` to get the achievable read bandwidth that the decode's effective KV GB/s is
+ * compared with. */
+kvq_status kvq_read_probe(const void* buf, size_t bytes, void* sink, void* stream);
 
 /* Device workspace bytes a kvq_flash_decode (or kvq_flash_decode_append) call with the
  * same stores, batch, head count, max_len_hint and options needs (the split depends on

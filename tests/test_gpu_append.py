@@ -8,6 +8,7 @@ import pytest
 import torch
 
 from kvq_testutil import bf16_tensor, build_store, expected_rows, kvq, store_rows
+from oracle import codec as ocodec
 from workloads import f32_to_bf16_bits, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -116,3 +117,46 @@ def test_append_kv_matches_oracle_and_advances(kc, vc, n_new):
             ep, es = expected_rows(inp, which, codec, b, np.arange(n_new))
             assert np.array_equal(gp, ep) and np.array_equal(gs, es), (which, b)
     assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+
+
+def _tie_rows(codec, n_rows=96):
+    """Rows whose blocks put x / d exactly on rounding boundaries k + 1/2 (d a power of two,
+    x = (k + 1/2) d is a bf16), next to them (one bf16 step either side), and at subnormal
+    scales; every block also holds +-amax so that d = amax / c is the intended scale."""
+    c = 127 if codec == "q8_0" else 7
+    rng = np.random.default_rng(11)
+    rows = np.zeros((n_rows, 128), np.float32)
+    for r in range(n_rows):
+        e = int(rng.integers(-30, 6))                 # down to subnormal fp16 scales
+        d = 2.0 ** e
+        for blk in range(4):
+            k = rng.integers(0, c, size=32).astype(np.float64)
+            x = (k + 0.5) * d * rng.choice([-1.0, 1.0], size=32)
+            x[0] = c * d                                 # amax: d = fp16(amax / c) = 2^e
+            rows[r, 32 * blk:32 * blk + 32] = x
+    bits = f32_to_bf16_bits(rows)
+    # nudge a third of the elements one bf16 step up or down (near-ties)
+    nudge = rng.integers(-1, 2, size=bits.shape).astype(np.int64)
+    nudge[:, ::32] = 0
+    bits = (bits.astype(np.int64) + nudge).astype(np.uint16)
+    return bits
+
+
+@pytest.mark.parametrize("codec", ["q8_0", "q4s"])
+@pytest.mark.parametrize("n_new", [1, 96])   # one row per launch (decode path) and the bulk path
+def test_append_ties_and_subnormal_scales_bit_exact(codec, n_new):
+    bits = _tie_rows(codec)
+    k = kvq()
+    st = k.kvq_store_create(codec, 1, 128, 128, 1)
+    pt = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    seq = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rows = bf16_tensor(bits[None, :, None, :])
+    for lo in range(0, 96, n_new):
+        k.kvq_append(st, rows[:, lo:lo + n_new].contiguous(), seq, pt)
+        k.kvq_seq_lens_add(seq, n_new)
+    torch.cuda.synchronize()
+    buf = st.buf.cpu().numpy()
+    rb = 128 if codec == "q8_0" else 64
+    ep, es = ocodec.encode_rows(bits, codec)
+    assert np.array_equal(buf[:96 * rb].reshape(96, rb), ep)
+    assert np.array_equal(buf[128 * rb:128 * rb + 96 * 8].view(np.uint16).reshape(96, 4), es)

@@ -102,3 +102,15 @@ def test_zero_rows_append_is_a_no_op():
                  torch.zeros((1, 1), dtype=torch.int32, device="cuda"))
     assert k.kvq_launch_count() == before
     _ = bf16_tensor(np.zeros(4, np.uint16))
+
+
+def test_read_probe_reads_and_leaves_sink():
+    k = kvq()
+    buf = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k.kvq_read_probe(buf, sink)
+    k.kvq_read_probe(buf[:1000].clone(), sink)   # a ragged length (tail below 16 bytes unread)
+    torch.cuda.synchronize()
+    assert int(sink.item()) == 0
+    with pytest.raises(k.KvqError):
+        k.kvq_read_probe(buf[1:17], sink)          # not 16-byte aligned
