@@ -566,6 +566,41 @@ def run_extras(torch, kvq, args, flush, peak):
                     "note": "bf16 K and V rows read, codes and scales written, one launch"})
         del ks, vs, rows_k, rows_v
         torch.cuda.empty_cache()
+    # chunked prefill attention (pp512 at depth 32768, 8B-class layer shape): the 512 chunk
+    # tokens are appended, then attend causally over the 33280-token store; q8_0 against
+    # the f16 control and against a separate dequantize pass + f16 prefill
+    depth, T = 32768, 512
+    times = {}
+    for arm in ("f16/f16", "q8_0/q8_0"):
+        layer = Layer(kvq, torch, WORKLOADS["layer8b"], arm, [depth + T], 0, seed=92)
+        qp = torch.randn((1, T, layer.hq, layer.d), device="cuda").to(torch.bfloat16)
+        outp = torch.empty((1, T, layer.hq, layer.d), dtype=torch.float32, device="cuda")
+
+        def pf(layer=layer, qp=qp, outp=outp):
+            kvq.kvq_prefill_attention(qp, layer.k_store, layer.v_store, layer.seq_lens, layer.page_table, out=outp)
+        time_decode_only(torch, layer, flush, 2, pf)
+        ms = statistics.median(time_decode_only(torch, layer, flush, 6, pf))
+        times[arm] = ms
+        flops = 4.0 * layer.d * layer.hq * sum(depth + i + 1 for i in range(T))
+        row = {"workload": "prefill_attention", "depth": depth, "chunk_tokens": T, "codec": arm,
+               "us": round(ms * 1e3, 1), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+        if arm == "q8_0/q8_0":
+            row["vs_f16_time"] = round(ms / times["f16/f16"], 3)
+            # unfused arm: the quantized store dequantized to f16 first, then the f16 kernel
+            kd = kvq.kvq_store_create("f16", layer.hkv, layer.d, layer.page_size, layer.k_store.num_pages)
+            vd = kvq.kvq_store_create("f16", layer.hkv, layer.d, layer.page_size, layer.k_store.num_pages)
+
+            def unf(layer=layer, qp=qp, outp=outp, kd=kd, vd=vd):
+                kvq.kvq_dequantize(layer.k_store, kd, layer.seq_lens, layer.page_table)
+                kvq.kvq_dequantize(layer.v_store, vd, layer.seq_lens, layer.page_table)
+                kvq.kvq_prefill_attention(qp, kd, vd, layer.seq_lens, layer.page_table, out=outp)
+            time_decode_only(torch, layer, flush, 2, unf)
+            um = statistics.median(time_decode_only(torch, layer, flush, 6, unf))
+            row["unfused_f16_us"] = round(um * 1e3, 1)
+            del kd, vd
+        out.append(row)
+        del layer
+        torch.cuda.empty_cache()
     # speculative-draft verification: T query tokens per sequence in one decode, against
     # T single-token decodes of the same cache (8B-class layer, 65536 tokens, q8_0 K+V)
     layer = Layer(kvq, torch, WORKLOADS["layer8b"], "q8_0/q8_0", [65536], 0, seed=91)

@@ -33,6 +33,8 @@ cudaError_t mma_launch_q4s_q4s(const DecodeArgs&, int, const CUtensorMap&, const
 cudaError_t mma_launch_q8_0_q4s(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t mma_launch_q4s_q8_0(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t mma_launch_q4s_bf16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+cudaError_t prefill_launch(int kc, int vc, const PrefillArgs& a, int batch, int head_dim,
+                           const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream);
 int mma_occupancy_bf16_bf16(int, int);
 int mma_occupancy_f16_f16(int, int);
 int mma_occupancy_q8_0_bf16(int, int);
@@ -462,6 +464,41 @@ kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void*
   return decode_impl(q, k_new, v_new, k_store, v_store, seq_lens, advance ? seq_lens : nullptr,
                      page_table, max_pages, codec, out, batch, num_q_heads, 1, softmax_scale,
                      max_len_hint, opts, workspace, workspace_bytes, stream);
+}
+
+kvq_status kvq_prefill_attention(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                                 const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                                 kvq_codec codec, float* out, int batch, int num_q_heads,
+                                 int num_tokens, float softmax_scale, void* stream) {
+  if (!q || !k_store || !v_store || !seq_lens || !page_table || !out) return KVQ_ERR_INVALID_ARG;
+  if (batch < 1 || num_q_heads < 1 || num_tokens < 1 || max_pages < 1) return KVQ_ERR_INVALID_ARG;
+  const kvq_store_desc& kd = k_store->desc;
+  const kvq_store_desc& vd = v_store->desc;
+  if (kd.num_kv_heads != vd.num_kv_heads || kd.head_dim != vd.head_dim ||
+      kd.page_size != vd.page_size || kd.num_pages != vd.num_pages)
+    return KVQ_ERR_INVALID_ARG;
+  if (codec.k != kd.codec || codec.v != vd.codec) return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % kd.num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16)) return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if ((long long)num_tokens * num_q_heads > (1LL << 30)) return KVQ_ERR_INVALID_ARG;
+  if (!k_store->rows_map_ok || !v_store->rows_map_ok) return KVQ_ERR_UNSUPPORTED;
+  PrefillArgs a = {};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = view_of(k_store);
+  a.v = view_of(v_store);
+  a.seq_lens = seq_lens;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.num_q_heads = num_q_heads;
+  a.group = num_q_heads / kd.num_kv_heads;
+  a.tokens = num_tokens;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt((float)kd.head_dim);
+  a.qk_scale_log2 = scale * 1.4426950408889634f;
+  a.out = out;
+  const cudaError_t e = prefill_launch(kd.codec, vd.codec, a, batch, kd.head_dim, k_store->rows_map,
+                                       v_store->rows_map, static_cast<cudaStream_t>(stream));
+  return e == cudaErrorNotSupported ? KVQ_ERR_UNSUPPORTED : from_cuda(e);
 }
 
 kvq_status kvq_dequantize(const kvq_store* src, kvq_store* dst, const int32_t* seq_lens,

@@ -99,6 +99,20 @@ struct DecodeArgs {
   unsigned* seq_counters;
 };
 
+// Arguments of the prefill attention kernel (kvq_prefill.cuh).
+struct PrefillArgs {
+  const __nv_bfloat16* q;     // [B][T][Hq][D]
+  StoreView k, v;
+  const int32_t* seq_lens;    // [B], counting the T new tokens
+  const int32_t* page_table;  // [B][max_pages]
+  int max_pages;
+  int num_q_heads;
+  int group;                  // Hq / Hkv
+  int tokens;                 // T
+  float qk_scale_log2;
+  float* out;                 // [B][T][Hq][D]
+};
+
 // Launchers implemented in the kernel translation units.  Each returns a CUDA error.
 cudaError_t launch_append(const kvq_store* store, const __nv_bfloat16* rows, int n_new, int batch,
                           const int32_t* seq_lens, const int32_t* page_table, int max_pages,

@@ -65,6 +65,7 @@ def _load():
                                        ctypes.POINTER(DecodeOpts), V],
         "kvq_dequantize": [P, P, P, P, I, I, V],
         "kvq_read_probe": [P, Z, P, V],
+        "kvq_prefill_attention": [P, P, P, P, P, I, CodecPair, P, I, I, I, ctypes.c_float, V],
         "kvq_flash_decode_multi": [P, P, P, P, P, I, CodecPair, P, I, I, I, ctypes.c_float, I,
                                    ctypes.POINTER(DecodeOpts), P, Z, V],
         "kvq_flash_decode_append": [P, P, P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I, I,
@@ -267,6 +268,23 @@ def kvq_flash_decode_multi(q: torch.Tensor, k_store: Store, v_store: Store, seq_
                                       int(max_len_hint), _opts(chunk_tokens, variant),
                                       _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                       _stream(stream)), "kvq_flash_decode_multi")
+    return out
+
+
+def kvq_prefill_attention(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: torch.Tensor,
+                          page_table: torch.Tensor, out: torch.Tensor | None = None,
+                          softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """q: bf16 [B, T, Hq, D], the last T positions of each sequence (already appended) ->
+    out fp32 [B, T, Hq, D]; token i attends to positions <= seq_len - T + i."""
+    bsz, t, hq, dim = q.shape
+    if out is None:
+        out = torch.empty((bsz, t, hq, dim), dtype=torch.float32, device=q.device)
+    codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
+    _check(lib.kvq_prefill_attention(_ptr(q, torch.bfloat16, "q"), k_store.handle, v_store.handle,
+                                     _ptr(seq_lens, torch.int32, "seq_lens"),
+                                     _ptr(page_table, torch.int32, "page_table"), page_table.shape[1], codec,
+                                     _ptr(out, torch.float32, "out"), bsz, hq, t, float(softmax_scale),
+                                     _stream(stream)), "kvq_prefill_attention")
     return out
 
 

@@ -220,6 +220,22 @@ kvq_status kvq_flash_decode_multi(const void* q, const kvq_store* k_store, const
                                   const kvq_decode_opts* opts, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* Chunked prefill attention over the store (prompt processing: the pp512-at-depth arm of
+ * halobench record clm-0022's tables, where dequantize-on-load also moved q8_0 prefill):
+ * the last num_tokens positions of each sequence (already appended, e.g. with
+ * kvq_append_kv) are the chunk's tokens, and token i attends to positions
+ * [0, seq_lens[b] - num_tokens + i] (causal inside the chunk, everything before it).
+ *   q    device bf16 [batch][num_tokens][num_q_heads][head_dim] (16-byte aligned)
+ *   out  device fp32 [batch][num_tokens][num_q_heads][head_dim]
+ * One launch, no workspace: a CTA owns 64 (token, head) query rows of one KV head and
+ * streams the KV prefix once.  Built for head_dim 64 and 128 and the pairs q8_0/q8_0,
+ * q4s/q4s, q8_0/q4s, f16/f16, bf16/bf16; others give KVQ_ERR_UNSUPPORTED.  softmax_scale <= 0
+ * selects 1/sqrt(head_dim).  Device faults as for kvq_flash_decode. */
+kvq_status kvq_prefill_attention(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                                 const int32_t* seq_lens, const int32_t* page_table, int max_pages,
+                                 kvq_codec codec, float* out, int batch, int num_q_heads,
+                                 int num_tokens, float softmax_scale, void* stream);
+
 /* One decode step with the append fused in (a1 followed by a2..a8, one launch of the
  * tensor-core kernel; the on-device append of rMLX issue #295 "Fix direction" done by
  * the decode kernel itself).  For every sequence b:
