@@ -44,6 +44,13 @@ using namespace kvq;
 extern "C" kvq_status kvq_read_probe(const void* buf, size_t bytes, void* sink, void* stream) {
   if (!buf || !sink || bytes < 16 || (reinterpret_cast<uintptr_t>(buf) & 15) != 0) return KVQ_ERR_INVALID_ARG;
   int dev = 0, sms = 0, per_sm = 0;
+  // the decode kernels' shared-memory carveout, so a probe right before them leaves the
+  // SMs configured as they need (it reads through L2 only)
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    cudaFuncSetAttribute(probe_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    carveout_set = true;
+  }
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, probe_kernel, kProbeThreads, 0) != cudaSuccess)
