@@ -242,7 +242,7 @@ struct Cfg {
   static constexpr int MINB = FOUR ? 4 : 1;
   // ring depth: as many stages (2..4) as fit the per-CTA budget that keeps the
   // intended number of resident CTAs per SM
-  static constexpr int SMEM_BUDGET = HG == 2 ? 200 * 1024 : D == 256 ? 100 * 1024 : FOUR ? 54 * 1024 : 70 * 1024;
+  static constexpr int SMEM_BUDGET = HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : FOUR ? 54 * 1024 : 70 * 1024;
   static constexpr int NS0 = (SMEM_BUDGET - 2048) / STAGE;
   static constexpr int NS = NS0 > 4 ? 4 : (NS0 < 2 ? 2 : NS0);
   static constexpr int OBUF = NW * 8 * D * 4;             // merge buffer (reuses the ring)
@@ -573,7 +573,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // transpose of p every PV column (head, hi|lo) finds its head's p in its own lane.
   uint32_t qf[C::QSTEPS][2];
   {
-    const int h = hg * 8 + (GW <= 4 ? (r & 3) : r);
+    const int h = hg * GW + (GW <= 4 ? (r & 3) : r);
     const bool hv = h < G;
     const __nv_bfloat16* qrow = a.q + ((long long)b * a.num_q_heads + (long long)kvh * G + (hv ? h : 0)) * D;
 #pragma unroll
@@ -725,7 +725,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
         // causal limit of the query tokens (virtual head v = head * T + i sees the positions
         // below L - T + 1 + i): only the sequence's last T - 1 positions are masked
         const int cA = 2 * i4, cB = 2 * i4 + 1;   // this lane's QK columns
-        const int vA = hg * 8 + (GW <= 4 ? (cA & 3) : cA), vB = hg * 8 + (GW <= 4 ? (cB & 3) : cB);
+        const int vA = hg * GW + (GW <= 4 ? (cA & 3) : cA), vB = hg * GW + (GW <= 4 ? (cB & 3) : cB);
         const int limA = L - T + 1 + vA % T, limB = L - T + 1 + vB % T;
         if (pos_w + r >= limA) sc[0] = -INFINITY;
         if (pos_w + r >= limB) sc[1] = -INFINITY;
@@ -982,11 +982,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   }
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
   const long long head0 = (long long)b * a.num_q_heads + (long long)kvh * G;
-  const int gcount = G < 8 * HG ? G : 8 * HG;
+  const int gcount = G < GW * HG ? G : GW * HG;
   // per-head (M, l) of the whole CTA
   float* hml = ml_all + C::NW * 16;     // [16][2]
   for (int h = tid; h < gcount; h += NWT) {
-    const int hgi = h >> 3, hl = h & 7;
+    const int hgi = h / GW, hl = h % GW;
     float M = -INFINITY;
     for (int w = 0; w < 4; ++w) M = fmaxf(M, ml_all[(hgi * 4 + w) * 16 + hl * 2]);
     float lsum = 0.0f;
@@ -1002,7 +1002,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     // the whole sequence is this chunk: normalize and write the output (no split)
     for (int idx = tid; idx < gcount * D; idx += NWT) {
       const int h = idx / D, j = idx % D;
-      const int hgi = h >> 3, hl = h & 7;
+      const int hgi = h / GW, hl = h % GW;
       float sum = 0.0f;
 #pragma unroll
       for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
@@ -1015,7 +1015,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // ------------------------------------------------------------ partial write (a7)
   for (int idx = tid; idx < gcount * D; idx += NWT) {
     const int h = idx / D, j = idx % D;
-    const int hgi = h >> 3, hl = h & 7;
+    const int hgi = h / GW, hl = h % GW;
     float sum = 0.0f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
