@@ -230,8 +230,8 @@ def kvq_flash_decode(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: 
         max_len_hint = max_pages * k_store.page_size
     if out is None:
         out = torch.empty((bsz, hq, dim), dtype=torch.float32, device=q.device)
-    need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq, max_len_hint, chunk_tokens, variant)
-    if workspace is None:
+    if workspace is None:   # (a given workspace is checked by the library itself)
+        need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq, max_len_hint, chunk_tokens, variant)
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
     _check(lib.kvq_flash_decode(_ptr(q, torch.bfloat16, "q"), k_store.handle, v_store.handle,
@@ -271,6 +271,37 @@ def kvq_flash_decode_multi(q: torch.Tensor, k_store: Store, v_store: Store, seq_
     return out
 
 
+class DecodeAppendStep:
+    """kvq_flash_decode_append bound once to fixed device buffers (the serving pattern: each
+    step refills q / k_new / v_new in place and calls the step).  Arguments are checked and
+    marshalled here once; a call is one library call."""
+
+    def __init__(self, q, k_new, v_new, k_store, v_store, seq_lens, page_table, out, workspace,
+                 max_len_hint, advance=True, softmax_scale=0.0, chunk_tokens=0, variant=0, stream=None):
+        bsz, hq, dim = q.shape
+        for name, t, st in (("k_new", k_new, k_store), ("v_new", v_new, v_store)):
+            if t.dim() != 3 or t.shape[0] != bsz or t.shape[1] != st.num_kv_heads or t.shape[2] != st.head_dim:
+                raise ValueError(f"{name} must be [B, Hkv, D] = [{bsz}, {st.num_kv_heads}, {st.head_dim}]")
+        if out.shape != (bsz, hq, dim):
+            raise ValueError("out must be [B, Hq, D]")
+        self._keep = (q, k_new, v_new, k_store, v_store, seq_lens, page_table, out, workspace)
+        self._opts = _opts(chunk_tokens, variant)
+        self._args = (_ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"),
+                      _ptr(v_new, torch.bfloat16, "v_new"), k_store.handle, v_store.handle,
+                      _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(page_table, torch.int32, "page_table"),
+                      page_table.shape[1], CodecPair(CODECS[k_store.codec], CODECS[v_store.codec]),
+                      _ptr(out, torch.float32, "out"), bsz, hq, float(softmax_scale), int(max_len_hint),
+                      1 if advance else 0, self._opts, _ptr(workspace, torch.uint8, "workspace"),
+                      workspace.numel(), _stream(stream))
+        self.out = out
+
+    def __call__(self):
+        status = lib.kvq_flash_decode_append(*self._args)
+        if status != KVQ_OK:
+            raise KvqError(status, "kvq_flash_decode_append")
+        return self.out
+
+
 def kvq_prefill_attention(q: torch.Tensor, k_store: Store, v_store: Store, seq_lens: torch.Tensor,
                           page_table: torch.Tensor, out: torch.Tensor | None = None,
                           softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
@@ -306,8 +337,8 @@ def kvq_flash_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.T
         max_len_hint = max_pages * k_store.page_size
     if out is None:
         out = torch.empty((bsz, hq, dim), dtype=torch.float32, device=q.device)
-    need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq, max_len_hint, chunk_tokens, variant)
-    if workspace is None:
+    if workspace is None:   # (a given workspace is checked by the library itself)
+        need = kvq_decode_workspace_bytes(k_store, v_store, bsz, hq, max_len_hint, chunk_tokens, variant)
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     codec = CodecPair(CODECS[k_store.codec], CODECS[v_store.codec])
     _check(lib.kvq_flash_decode_append(_ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"),

@@ -156,3 +156,28 @@ def test_fused_cuda_core_variant_is_unsupported():
     with pytest.raises(k.KvqError):
         k.kvq_flash_decode_append(bf16_tensor(inp.q), kn, vn, ks, vs, seq, pt, variant=1)
     assert seq.cpu().tolist() == [9]
+
+
+def test_bound_step_equals_the_plain_call():
+    # kvq.DecodeAppendStep (arguments marshalled once, buffers refilled in place) gives the
+    # same stores, lengths and outputs as kvq_flash_decode_append
+    L0, steps = 600, 5
+    inp = make_inputs([L0 + steps], 32, 8, 128, seed=37)
+    k = kvq()
+    q = bf16_tensor(inp.q)
+    krows, vrows = bf16_tensor(inp.k_rows[0]), bf16_tensor(inp.v_rows[0])
+    hint = L0 + steps
+    ks, vs, seq, pt = prefix_stores(inp, "q8_0", "q8_0", [L0])
+    ws = torch.zeros(k.kvq_decode_workspace_bytes(ks, vs, 1, 32, hint), dtype=torch.uint8, device="cuda")
+    kn = torch.empty((1, 8, 128), dtype=torch.bfloat16, device="cuda")
+    vn = torch.empty_like(kn)
+    out = torch.empty((1, 32, 128), dtype=torch.float32, device="cuda")
+    bound = k.DecodeAppendStep(q, kn, vn, ks, vs, seq, pt, out, ws, hint)
+    ks2, vs2, seq2, pt2 = prefix_stores(inp, "q8_0", "q8_0", [L0])
+    for st in range(steps):
+        kn.copy_(krows[L0 + st][None]); vn.copy_(vrows[L0 + st][None])
+        bound()
+        ref = k.kvq_flash_decode_append(q, krows[L0 + st][None].contiguous(), vrows[L0 + st][None].contiguous(),
+                                        ks2, vs2, seq2, pt2, max_len_hint=hint)
+        assert torch.equal(out, ref)
+    assert torch.equal(seq, seq2) and torch.equal(ks.buf, ks2.buf) and torch.equal(vs.buf, vs2.buf)
