@@ -477,11 +477,31 @@ def run_mine(args, rank, world):
     }
     if sweep is not None:
         result["sweep"] = sweep
+        result["slopes"] = depth_slopes([(r["codec"], r["kv_len"], r["us"]) for r in sweep], "layer8b")
     if extras is not None:
         result["workloads"] = extras
+        lc = [(r["codec"], r["kv_len"], r["us"]) for r in extras if r["workload"] == "longctx"]
+        result.setdefault("slopes", {}).update(depth_slopes(lc, "longctx"))
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, wl, codec, seq_lens[0] if wl["kv_len"] else 4096)
     return result
+
+
+def depth_slopes(points, tag):
+    """Least-squares us = a + b * kv_len per codec arm (the pages' marginal cost per 1k KV
+    tokens is b * 1000): {"<tag> <codec>": {"us_per_1k_tokens": b*1000, "intercept_us": a}}."""
+    by = {}
+    for codec, L, us in points:
+        by.setdefault(codec, []).append((L, us))
+    out = {}
+    for codec, pts in by.items():
+        if len(pts) < 2:
+            continue
+        xs = np.array([p[0] for p in pts], dtype=np.float64)
+        ys = np.array([p[1] for p in pts], dtype=np.float64)
+        b, a = np.polyfit(xs, ys, 1)
+        out[f"{tag} {codec}"] = {"us_per_1k_tokens": round(float(b) * 1000, 4), "intercept_us": round(float(a), 2)}
+    return out
 
 
 def measure_e2e(torch, kvq, layer, flush, iters):
