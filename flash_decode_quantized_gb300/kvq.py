@@ -292,11 +292,13 @@ class DecodeAppendStep:
                       page_table.shape[1], CodecPair(CODECS[k_store.codec], CODECS[v_store.codec]),
                       _ptr(out, torch.float32, "out"), bsz, hq, float(softmax_scale), int(max_len_hint),
                       1 if advance else 0, self._opts, _ptr(workspace, torch.uint8, "workspace"),
-                      workspace.numel(), _stream(stream))
+                      workspace.numel())
+        self._stream = None if stream is None else _stream(stream)   # None: current at each call
         self.out = out
 
     def __call__(self):
-        status = lib.kvq_flash_decode_append(*self._args)
+        st = self._stream if self._stream is not None else torch.cuda.current_stream().cuda_stream
+        status = lib.kvq_flash_decode_append(*self._args, st)
         if status != KVQ_OK:
             raise KvqError(status, "kvq_flash_decode_append")
         return self.out

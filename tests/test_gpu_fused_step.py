@@ -181,3 +181,34 @@ def test_bound_step_equals_the_plain_call():
                                         ks2, vs2, seq2, pt2, max_len_hint=hint)
         assert torch.equal(out, ref)
     assert torch.equal(seq, seq2) and torch.equal(ks.buf, ks2.buf) and torch.equal(vs.buf, vs2.buf)
+
+
+def test_fused_steps_replay_from_a_cuda_graph():
+    # 6 fused steps captured once and replayed: the device-side length advance and the
+    # encode/decode of each step happen inside the graph, matching eager steps bit for bit
+    L0, steps = 500, 6
+    inp = make_inputs([L0 + 2 * steps], 32, 8, 128, seed=38)
+    k = kvq()
+    q = bf16_tensor(inp.q)
+    krow = bf16_tensor(inp.k_rows[0][L0:L0 + 1])
+    vrow = bf16_tensor(inp.v_rows[0][L0:L0 + 1])
+    hint = L0 + 2 * steps
+    outs = []
+    for mode in ("eager", "graph"):
+        ks, vs, seq, pt = prefix_stores(inp, "q8_0", "q8_0", [L0])
+        ws = torch.zeros(k.kvq_decode_workspace_bytes(ks, vs, 1, 32, hint), dtype=torch.uint8, device="cuda")
+        out = torch.empty((1, 32, 128), dtype=torch.float32, device="cuda")
+        step = k.DecodeAppendStep(q, krow, vrow, ks, vs, seq, pt, out, ws, hint)
+        if mode == "eager":
+            for _ in range(steps):
+                step()
+        else:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(steps):
+                    step()
+            graph.replay()
+        torch.cuda.synchronize()
+        assert int(seq.item()) == L0 + steps
+        outs.append((out.clone(), ks.buf.clone(), vs.buf.clone()))
+    assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
