@@ -125,6 +125,11 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t x, uint32_t y) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&y));
   return *reinterpret_cast<uint32_t*>(&r);
 }
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t x, uint32_t y, uint32_t z) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&y),
+                      *reinterpret_cast<__half2*>(&z));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
 // Magic-number conversion of integer codes to f16: the bits 0x64 << 8 | u encode the
 // f16 value 1024 + u exactly (u < 1024).  V operands subtract the constant offset in f16
 // registers (exact); K operands keep it and the QK accumulator is seeded with
@@ -140,6 +145,14 @@ __device__ __forceinline__ uint32_t i8pair_raw(uint32_t u_biased, uint32_t sel) 
 __device__ __forceinline__ uint32_t u4pair_raw(uint32_t w) {
   return (w & 0x000F000Fu) | 0x64006400u;
 }
+// Nibble pair (bits 4-7 and 20-23 of w) holding u = q + 8 -> the f16 pair (1024 + 16 u), with
+// no shift: hfma2_u32(x, 1/16, -72) then gives q exactly (64 + u - 72, one rounding of an
+// exact small integer).
+__device__ __forceinline__ uint32_t u4pair_hi_raw(uint32_t w) {
+  return (w & 0x00F000F0u) | 0x64006400u;
+}
+constexpr uint32_t kSixteenth2 = 0x2C002C00u;   // f16 pair (1/16, 1/16)
+constexpr uint32_t kMinus72x2 = 0xD480D480u;    // f16 pair (-72, -72)
 // Nibble pair (bits 6-9 and 22-25 of w) holding u = q + 8 -> the f16 pair 8 + u/2 =
 // 12 + q/2 (0x48 << 8 is 8.0; the nibble lands in the top mantissa bits).  The K codes of
 // the 4-bit codec use this form: with the 1024-based one the seeded accumulator carried
@@ -865,14 +878,16 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
             if ((bb & 1) == 0)
               ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), vq4[0], vq4[1], vq4[2], vq4[3]);
             const uint32_t ya = (bb & 1) ? vq4[2] : vq4[0], yb = (bb & 1) ? vq4[3] : vq4[1];
-            uint32_t a01[4] = {u4pair_raw(ya), u4pair_raw(ya >> 4), u4pair_raw(yb), u4pair_raw(yb >> 4)};
-            uint32_t a23[4] = {u4pair_raw(ya >> 8), u4pair_raw(ya >> 12), u4pair_raw(yb >> 8),
-                               u4pair_raw(yb >> 12)};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              a01[k] = hsub2_u32(a01[k], 0x64086408u);
-              a23[k] = hsub2_u32(a23[k], 0x64086408u);
-            }
+            const uint32_t ya8 = ya >> 8, yb8 = yb >> 8;
+            // even nibbles: 1024 + u, less 1032; odd nibbles in place: (1024 + 16 u) / 16 - 72
+            const uint32_t a01[4] = {hsub2_u32(u4pair_raw(ya), 0x64086408u),
+                                     hfma2_u32(u4pair_hi_raw(ya), kSixteenth2, kMinus72x2),
+                                     hsub2_u32(u4pair_raw(yb), 0x64086408u),
+                                     hfma2_u32(u4pair_hi_raw(yb), kSixteenth2, kMinus72x2)};
+            const uint32_t a23[4] = {hsub2_u32(u4pair_raw(ya8), 0x64086408u),
+                                     hfma2_u32(u4pair_hi_raw(ya8), kSixteenth2, kMinus72x2),
+                                     hsub2_u32(u4pair_raw(yb8), 0x64086408u),
+                                     hfma2_u32(u4pair_hi_raw(yb8), kSixteenth2, kMinus72x2)};
 #pragma unroll
             for (int n = 0; n < C::NPV; ++n) {
               mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
