@@ -400,7 +400,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   using C = Cfg<KC, VC, D, GW, HG>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle pattern
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // (offset from the array itself, so accesses through `smem` stay in the shared space)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + C::BAR_OFF;           // + 8*s
   const uint32_t bar_empty = sbase + C::BAR_OFF + 8 * C::NS;

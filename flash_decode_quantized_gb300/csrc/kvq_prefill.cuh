@@ -69,7 +69,8 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                    PrefillArgs a) {
   using C = PCfg<KC, VC, D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // (offset from the array itself, so accesses through `smem` stay in the shared space)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + C::BAR_OFF, bar_empty = sbase + C::BAR_OFF + 8 * C::NS;
   volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + C::OK_OFF);
@@ -417,8 +418,12 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
               // y: [t 2i: nibbles 4n..4n+3 (dims 4n+e)][t 2i+1: same dims], n = g (16-bit col g)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {   // dims 4n + e of the block
-                const uint32_t b0 = hsub2_u32(u4pair_raw(y[0] >> (4 * e)), 0x64086408u);
-                const uint32_t b1 = hsub2_u32(u4pair_raw(y[1] >> (4 * e)), 0x64086408u);
+                // even nibbles: 1024 + u, less 1032; odd nibbles in place: (1024 + 16 u) / 16 - 72
+                const int sh = 4 * (e & ~1);
+                const uint32_t b0 = (e & 1) ? hfma2_u32(u4pair_hi_raw(y[0] >> sh), kSixteenth2, kMinus72x2)
+                                            : hsub2_u32(u4pair_raw(y[0] >> sh), 0x64086408u);
+                const uint32_t b1 = (e & 1) ? hfma2_u32(u4pair_hi_raw(y[1] >> sh), kSixteenth2, kMinus72x2)
+                                            : hsub2_u32(u4pair_raw(y[1] >> sh), 0x64086408u);
                 float* acc = o[4 * bb + e];
                 mma16816<false>(acc, ah, b0, b1);
                 mma16816<false>(acc, al, b0, b1);
