@@ -505,13 +505,15 @@ def depth_slopes(points, tag):
 
 
 def measure_e2e(torch, kvq, layer, flush, iters):
-    """The same step through the public API with host buffers.  Every step copies its inputs
-    (q and the new token's K and V rows, packed in one pinned host slot per step) to the
-    device, runs kvq_flash_decode_append, and copies its output into a pinned host slot of
-    its own; the steps are enqueued back to back on one stream and the region ends with a
-    synchronize, so the time covers every transfer and launch of the K steps (L2 not
-    flushed: the serving pattern).  A one-step-at-a-time variant (synchronize after each
-    step, L2 evicted before it) is reported beside it as `sync_step`."""
+    """The same step through the public API with host buffers.  Each of the K steps has its
+    own pinned host slot for its inputs (q and the new token's K and V rows) and for its
+    output.  Default (tensor-core variant): each step is one library call bound to its slots
+    (kvq.DecodeAppendStep over pinned CPU tensors), and the kernel reads the inputs from and
+    writes the output to host memory in place, so the transfers happen inside the step.
+    `copy_engine`: the same loop with explicit pinned H2D and D2H copies around a call bound
+    to device buffers.  The steps are enqueued back to back on one stream and the region
+    ends with a synchronize (L2 not flushed: the serving pattern).  `sync_step`: one step at
+    a time (synchronize after each, L2 evicted before it), median."""
     nq, nk, nv = layer.q.numel(), layer.new_k.numel(), layer.new_v.numel()
     n_in = nq + nk + nv
     host_in = torch.empty((iters, n_in), dtype=torch.bfloat16).pin_memory()
@@ -520,55 +522,89 @@ def measure_e2e(torch, kvq, layer, flush, iters):
         host_in[i, nq:nq + nk] = layer.new_k.reshape(-1).cpu()
         host_in[i, nq + nk:] = layer.new_v.reshape(-1).cpu()
     host_out = torch.empty((iters,) + tuple(layer.out.shape), dtype=torch.float32).pin_memory()
+    bkd = (layer.batch, layer.hkv, layer.d)
+
+    def timed(run_one, sync_each=False, n=iters):
+        for i in range(3):   # warm the path
+            run_one(i)
+        torch.cuda.synchronize()
+        if sync_each:
+            out = []
+            for i in range(n):
+                flush()
+                torch.cuda.synchronize()
+                t1 = time.perf_counter()
+                run_one(i)
+                torch.cuda.synchronize()
+                out.append((time.perf_counter() - t1) * 1e3)
+            return statistics.median(out)
+        kvb = 0
+        t0 = time.perf_counter()
+        for i in range(n):
+            run_one(i)
+            kvb += layer.kv_bytes()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) * 1e3 / n, kvb / n
+
+    # explicit copies around a step bound to device buffers
     dev_in = torch.empty(n_in, dtype=torch.bfloat16, device="cuda")
     q_d = dev_in[:nq].view(layer.q.shape)
-    k_d = dev_in[nq:nq + nk].view(layer.new_k.shape)
-    v_d = dev_in[nq + nk:].view(layer.new_v.shape)
+    k_d = dev_in[nq:nq + nk].view(bkd)
+    v_d = dev_in[nq + nk:].view(bkd)
     if layer.variant == 1:
-        def run_step():
-            layer.step(q_d, k_d, v_d)
-    else:   # the step bound once to the fixed buffers (kvq.DecodeAppendStep)
-        bound = kvq.DecodeAppendStep(q_d, k_d.view(layer.batch, layer.hkv, layer.d),
-                                     v_d.view(layer.batch, layer.hkv, layer.d), layer.k_store, layer.v_store,
-                                     layer.seq_lens, layer.page_table, layer.out, layer.ws, layer.hint,
+        def dev_step():
+            layer.step(q_d, k_d.view(layer.new_k.shape), v_d.view(layer.new_v.shape))
+    else:
+        bound = kvq.DecodeAppendStep(q_d, k_d, v_d, layer.k_store, layer.v_store, layer.seq_lens,
+                                     layer.page_table, layer.out, layer.ws, layer.hint,
                                      chunk_tokens=layer.chunk, variant=layer.variant)
 
-        def run_step():
+        def dev_step():
             bound()
             layer.host_lens = [L + 1 for L in layer.host_lens]
-    for i in range(3):   # warm the path (pinned copies, binding)
+
+    def copy_one(i):
         dev_in.copy_(host_in[i], non_blocking=True)
-        run_step()
+        dev_step()
         host_out[i].copy_(layer.out, non_blocking=True)
-    torch.cuda.synchronize()
-    kvb = 0
-    t0 = time.perf_counter()
+
+    ce_ms, ce_kvb = timed(copy_one)
+    ce = {"ms": round(ce_ms, 5), "value": round(ce_kvb / (ce_ms * 1e-3) / 1e9, 1),
+          "timing": "pinned H2D copy of the step's inputs, the step (bound to device buffers), "
+                    "pinned D2H copy of its output, per step; back to back, one synchronize"}
+    if layer.variant == 1:
+        sync_ms = timed(copy_one, sync_each=True, n=min(iters, 20))
+        return {"ms": round(ce_ms, 5), "unit": "GB/s", "h2d_bytes_per_step": int(n_in * 2),
+                "d2h_bytes_per_step": int(layer.out.numel() * 4), "kvb": ce_kvb,
+                "timing": ce["timing"],
+                "sync_step": {"ms": round(sync_ms, 5), "value": round(layer.kv_bytes() / (sync_ms * 1e-3) / 1e9, 1),
+                              "timing": "one step at a time, synchronize after it, L2 evicted before, median"}}
+
+    # zero-copy: one call per step, bound to its pinned host slots
+    steps = []
     for i in range(iters):
-        dev_in.copy_(host_in[i], non_blocking=True)
-        run_step()
-        host_out[i].copy_(layer.out, non_blocking=True)
-        kvb += layer.kv_bytes()
-    torch.cuda.synchronize()
-    ms = (time.perf_counter() - t0) * 1e3 / iters
-    # one step at a time
-    sync_ms = []
-    for i in range(min(iters, 20)):
-        flush()
-        torch.cuda.synchronize()
-        t1 = time.perf_counter()
-        dev_in.copy_(host_in[i], non_blocking=True)
-        run_step()
-        host_out[i].copy_(layer.out, non_blocking=True)
-        torch.cuda.synchronize()
-        sync_ms.append((time.perf_counter() - t1) * 1e3)
-    sync_med = statistics.median(sync_ms)
+        hq = host_in[i, :nq].view(layer.q.shape)
+        hk = host_in[i, nq:nq + nk].view(bkd)
+        hv = host_in[i, nq + nk:].view(bkd)
+        steps.append(kvq.DecodeAppendStep(hq, hk, hv, layer.k_store, layer.v_store, layer.seq_lens,
+                                          layer.page_table, host_out[i], layer.ws, layer.hint,
+                                          chunk_tokens=layer.chunk, variant=layer.variant))
+
+    def zc_one(i):
+        steps[i]()
+        layer.host_lens = [L + 1 for L in layer.host_lens]
+
+    ms, kvb = timed(zc_one)
+    sync_ms = timed(zc_one, sync_each=True, n=min(iters, 20))
     return {"ms": round(ms, 5), "unit": "GB/s", "h2d_bytes_per_step": int(n_in * 2),
-            "d2h_bytes_per_step": int(layer.out.numel() * 4), "kvb": kvb / iters,
-            "timing": f"host wall clock over {iters} back-to-back steps, each with its pinned H2D of "
-                      "q + new K/V rows and D2H of the output, one synchronize at the end",
-            "sync_step": {"ms": round(sync_med, 5),
-                          "value": round(layer.kv_bytes() / (sync_med * 1e-3) / 1e9, 1),
-                          "timing": "one step at a time: H2D + step + D2H + synchronize, L2 evicted before, median"}}
+            "d2h_bytes_per_step": int(layer.out.numel() * 4), "kvb": kvb,
+            "timing": f"host wall clock over {iters} back-to-back steps, each one library call whose "
+                      "kernel reads the step's inputs from its pinned host slot and writes the output "
+                      "to its pinned host slot (zero-copy over the host link), one synchronize at the end",
+            "copy_engine": ce,
+            "sync_step": {"ms": round(sync_ms, 5),
+                          "value": round(layer.kv_bytes() / (sync_ms * 1e-3) / 1e9, 1),
+                          "timing": "one step at a time: the zero-copy step + synchronize, L2 evicted before, median"}}
 
 
 def run_extras(torch, kvq, args, flush, peak):

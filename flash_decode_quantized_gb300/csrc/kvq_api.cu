@@ -344,6 +344,20 @@ kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store*
   return KVQ_OK;
 }
 
+kvq_status kvq_pointer_kind(const void* p, int32_t* kind) {
+  if (!p || !kind) return KVQ_ERR_INVALID_ARG;
+  cudaPointerAttributes at = {};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();   // clear the sticky-free error of the query
+    *kind = -1;
+    return KVQ_OK;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) *kind = 0;
+  else if (at.type == cudaMemoryTypeHost && at.devicePointer == p) *kind = 1;
+  else *kind = -1;
+  return KVQ_OK;
+}
+
 kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes == 0) return KVQ_ERR_INVALID_ARG;
   return from_cuda(cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)));

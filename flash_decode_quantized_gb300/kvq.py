@@ -65,6 +65,7 @@ def _load():
                                        ctypes.POINTER(DecodeOpts), V],
         "kvq_dequantize": [P, P, P, P, I, I, V],
         "kvq_read_probe": [P, Z, P, V],
+        "kvq_pointer_kind": [P, ctypes.POINTER(ctypes.c_int32)],
         "kvq_prefill_attention": [P, P, P, P, P, I, CodecPair, P, I, I, I, ctypes.c_float, V],
         "kvq_flash_decode_multi": [P, P, P, P, P, I, CodecPair, P, I, I, I, ctypes.c_float, I,
                                    ctypes.POINTER(DecodeOpts), P, Z, V],
@@ -108,6 +109,30 @@ def _ptr(t: torch.Tensor, dtype, name: str) -> int:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
+
+
+def pointer_kind(ptr: int) -> int:
+    """kvq_pointer_kind: 0 device memory, 1 host memory mapped at the same address, -1 other."""
+    k = ctypes.c_int32(-1)
+    _check(lib.kvq_pointer_kind(ctypes.c_void_p(ptr), ctypes.byref(k)), "kvq_pointer_kind")
+    return k.value
+
+
+def _ptr_io(t: torch.Tensor, dtype, name: str) -> int:
+    """A step's input or output buffer: a CUDA tensor, or a pinned (page-locked) CPU tensor,
+    which the kernel reads or writes in place through its device-visible mapping (the host
+    transfer happens inside the step, with no copy-engine hand-off)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise TypeError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if pointer_kind(t.data_ptr()) != 1:
+            raise TypeError(f"{name}: pinned memory not mapped into the device's address space")
+        return t.data_ptr()
+    return _ptr(t, dtype, name)
 
 
 def _opts(chunk_tokens: int, variant: int):
@@ -272,9 +297,11 @@ def kvq_flash_decode_multi(q: torch.Tensor, k_store: Store, v_store: Store, seq_
 
 
 class DecodeAppendStep:
-    """kvq_flash_decode_append bound once to fixed device buffers (the serving pattern: each
-    step refills q / k_new / v_new in place and calls the step).  Arguments are checked and
-    marshalled here once; a call is one library call."""
+    """kvq_flash_decode_append bound once to fixed buffers (the serving pattern: each step
+    refills q / k_new / v_new in place and calls the step).  Arguments are checked and
+    marshalled here once; a call is one library call.  q, k_new, v_new and out may be pinned
+    CPU tensors: the step then reads its inputs from, and writes its output to, host memory
+    itself (zero-copy), so a serving loop needs no separate copies around the call."""
 
     def __init__(self, q, k_new, v_new, k_store, v_store, seq_lens, page_table, out, workspace,
                  max_len_hint, advance=True, softmax_scale=0.0, chunk_tokens=0, variant=0, stream=None):
@@ -286,11 +313,11 @@ class DecodeAppendStep:
             raise ValueError("out must be [B, Hq, D]")
         self._keep = (q, k_new, v_new, k_store, v_store, seq_lens, page_table, out, workspace)
         self._opts = _opts(chunk_tokens, variant)
-        self._args = (_ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"),
-                      _ptr(v_new, torch.bfloat16, "v_new"), k_store.handle, v_store.handle,
+        self._args = (_ptr_io(q, torch.bfloat16, "q"), _ptr_io(k_new, torch.bfloat16, "k_new"),
+                      _ptr_io(v_new, torch.bfloat16, "v_new"), k_store.handle, v_store.handle,
                       _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(page_table, torch.int32, "page_table"),
                       page_table.shape[1], CodecPair(CODECS[k_store.codec], CODECS[v_store.codec]),
-                      _ptr(out, torch.float32, "out"), bsz, hq, float(softmax_scale), int(max_len_hint),
+                      _ptr_io(out, torch.float32, "out"), bsz, hq, float(softmax_scale), int(max_len_hint),
                       1 if advance else 0, self._opts, _ptr(workspace, torch.uint8, "workspace"),
                       workspace.numel())
         self._stream = None if stream is None else _stream(stream)   # None: current at each call

@@ -174,6 +174,13 @@ kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store*
                                       int batch, int num_q_heads, int max_len_hint,
                                       const kvq_decode_opts* opts, size_t* bytes);
 
+/* Where `p` points, for callers deciding whether a buffer may be handed to a kernel:
+ * *kind = 0 for device (or managed) memory, 1 for page-locked host memory mapped into the
+ * current device's address space at the same address (usable in place where a call
+ * allows host buffers), -1 otherwise (pageable host memory, unknown addresses).  A host
+ * call (cudaPointerGetAttributes); KVQ_ERR_INVALID_ARG for null arguments. */
+kvq_status kvq_pointer_kind(const void* p, int32_t* kind);
+
 /* Zero a decode workspace (its arrival counters must be zero before its first use;
  * every completed kvq_flash_decode leaves them zero again).  Enqueued on `stream`. */
 kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
@@ -251,7 +258,14 @@ kvq_status kvq_prefill_attention(const void* q, const kvq_store* k_store, const 
  * Only the tensor-core kernel implements it: opts->variant 1 gives KVQ_ERR_UNSUPPORTED.
  * A sequence whose new length does not fit gets no append and no advance and is
  * recorded as a device fault (KVQ_DEVICE_BAD_SEQ_LEN); a bad page of the new token is
- * recorded as KVQ_DEVICE_BAD_PAGE. */
+ * recorded as KVQ_DEVICE_BAD_PAGE.
+ * q, k_new, v_new and out may instead point to page-locked host memory that is mapped
+ * into the device's address space (cudaHostAlloc, or a registered and mapped range; with
+ * unified addressing the host address itself): the kernel then reads the step's inputs
+ * and writes its output across the host link in place, so one call is the whole step
+ * including its transfers.  The library does not check where these four pointers point;
+ * any other host memory is undefined behaviour (as is an invalid device pointer).
+ * seq_lens, page_table, the stores and the workspace stay in device memory. */
 kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void* v_new,
                                    kvq_store* k_store, kvq_store* v_store, int32_t* seq_lens,
                                    const int32_t* page_table, int max_pages, kvq_codec codec,

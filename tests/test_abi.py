@@ -66,6 +66,7 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
                                      None, 1, 1, 0.0, 1, 1, None, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_dequantize(None, None, None, None, 1, 1, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_read_probe(None, 1024, None, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_pointer_kind(None, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_prefill_attention(None, None, None, None, None, 1, kvq.CodecPair(2, 2), None, 1, 1, 1,
                                    0.0, None) == kvq.KVQ_ERR_INVALID_ARG
     assert L.kvq_decode_workspace_bytes(None, None, 1, 1, 1, None, None) == kvq.KVQ_ERR_INVALID_ARG

@@ -212,3 +212,57 @@ def test_fused_steps_replay_from_a_cuda_graph():
         assert int(seq.item()) == L0 + steps
         outs.append((out.clone(), ks.buf.clone(), vs.buf.clone()))
     assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
+
+
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q4s", "q4s")])
+def test_step_reads_and_writes_pinned_host_buffers(kc, vc):
+    # q, k_new, v_new and out in pinned host memory (one slot per step): the kernel reads
+    # the inputs and writes the output across the host link in place, giving the same
+    # stores, lengths and outputs as the step on device buffers
+    L0, steps = 700, 4
+    inp = make_inputs([L0 + steps], 32, 8, 128, seed=39)
+    k = kvq()
+    q = bf16_tensor(inp.q)
+    krows, vrows = bf16_tensor(inp.k_rows[0]), bf16_tensor(inp.v_rows[0])
+    hint = L0 + steps
+    ks, vs, seq, pt = prefix_stores(inp, kc, vc, [L0])
+    ws = torch.zeros(k.kvq_decode_workspace_bytes(ks, vs, 1, 32, hint), dtype=torch.uint8, device="cuda")
+    hq = q.cpu().pin_memory()
+    hk = [krows[L0 + st][None].cpu().pin_memory() for st in range(steps)]
+    hv = [vrows[L0 + st][None].cpu().pin_memory() for st in range(steps)]
+    hout = [torch.empty((1, 32, 128), dtype=torch.float32).pin_memory() for _ in range(steps)]
+    bound = [k.DecodeAppendStep(hq, hk[st], hv[st], ks, vs, seq, pt, hout[st], ws, hint) for st in range(steps)]
+    for st in range(steps):
+        bound[st]()
+    torch.cuda.synchronize()
+    ks2, vs2, seq2, pt2 = prefix_stores(inp, kc, vc, [L0])
+    for st in range(steps):
+        ref = k.kvq_flash_decode_append(q, krows[L0 + st][None].contiguous(), vrows[L0 + st][None].contiguous(),
+                                        ks2, vs2, seq2, pt2, max_len_hint=hint)
+        assert torch.equal(hout[st], ref.cpu()), st
+    assert torch.equal(seq, seq2) and torch.equal(ks.buf, ks2.buf) and torch.equal(vs.buf, vs2.buf)
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+
+
+def test_pageable_host_buffers_are_rejected():
+    # only pinned CPU tensors are accepted in place of device buffers (host check, nothing
+    # is launched)
+    inp = make_inputs([300], 32, 8, 128, seed=40)
+    k = kvq()
+    ks, vs, seq, pt = prefix_stores(inp, "q8_0", "q8_0", [299])
+    ws = torch.zeros(k.kvq_decode_workspace_bytes(ks, vs, 1, 32, 300), dtype=torch.uint8, device="cuda")
+    q = torch.zeros((1, 32, 128), dtype=torch.bfloat16)           # pageable
+    kn = torch.zeros((1, 8, 128), dtype=torch.bfloat16).pin_memory()
+    out = torch.empty((1, 32, 128), dtype=torch.float32).pin_memory()
+    with pytest.raises(TypeError):
+        k.DecodeAppendStep(q, kn, kn, ks, vs, seq, pt, out, ws, 300)
+
+
+def test_pointer_kind_tells_device_mapped_host_and_pageable():
+    k = kvq()
+    d = torch.empty(64, dtype=torch.uint8, device="cuda")
+    h = torch.empty(64, dtype=torch.uint8).pin_memory()
+    p = torch.empty(64, dtype=torch.uint8)
+    assert k.pointer_kind(d.data_ptr()) == 0
+    assert k.pointer_kind(h.data_ptr()) == 1
+    assert k.pointer_kind(p.data_ptr()) == -1
