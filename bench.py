@@ -74,10 +74,12 @@ def hbm_peak():
 
 
 def kernel_sources_sha() -> str:
+    """Hash of the device-code sources the decode kernels are built from (every header of
+    the CUDA path and the tensor-core instantiation units; host-only files excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "flash_decode_quantized_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith(".cuh") or (name.startswith("mma_") and name.endswith(".cu")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]
