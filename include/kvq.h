@@ -6,8 +6,9 @@
  * the quantized KV store directly and dequantizes inside the kernel, the
  * "flash-decode-over-quant" class that rMLX issue #292 ("Root cause", correction)
  * names as the target, with the "dequantize KV on load" treatment of halobench record
- * clm-0022 (METHOD) and a 16-bit KV arm kept as the control ("THE CONTROL IS THE
- * POINT").  The prefix stays resident on the device and new rows are encoded there,
+ * clm-0022 (METHOD) and a 16-bit KV arm kept as the control (that record credits its
+ * speedup to the quantized arm because the f16 arm did not move).  The prefix stays
+ * resident on the device and new rows are encoded there,
  * so no step restages the prefix through the host (rMLX issue #295, "Root cause" and
  * "Fix direction").
  *
