@@ -864,7 +864,9 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded NumPy)", "impl": "reference",
-            "config": {"workload": f"{args.workload}", "codec": codec, "kv_len": L},
+            "config": {"workload": f"{args.workload}: B={wl['batch']}, Hq={wl['hq']}, Hkv={wl['hkv']}, "
+                                   f"D={wl['d']}, kv_len={L}",
+                       "codec": codec, "kv_len": L},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
