@@ -35,14 +35,14 @@ cudaError_t mma_launch_q4s_q8_0(const DecodeArgs&, int, const CUtensorMap&, cons
 cudaError_t mma_launch_q4s_bf16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t prefill_launch(int kc, int vc, const PrefillArgs& a, int batch, int head_dim,
                            const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream);
-int mma_occupancy_bf16_bf16(int, int);
-int mma_occupancy_f16_f16(int, int);
-int mma_occupancy_q8_0_bf16(int, int);
-int mma_occupancy_q8_0_q8_0(int, int);
-int mma_occupancy_q4s_q4s(int, int);
-int mma_occupancy_q8_0_q4s(int, int);
-int mma_occupancy_q4s_q8_0(int, int);
-int mma_occupancy_q4s_bf16(int, int);
+int mma_occupancy_bf16_bf16(int, int, int*);
+int mma_occupancy_f16_f16(int, int, int*);
+int mma_occupancy_q8_0_bf16(int, int, int*);
+int mma_occupancy_q8_0_q8_0(int, int, int*);
+int mma_occupancy_q4s_q4s(int, int, int*);
+int mma_occupancy_q8_0_q4s(int, int, int*);
+int mma_occupancy_q4s_q8_0(int, int, int*);
+int mma_occupancy_q4s_bf16(int, int, int*);
 
 namespace {
 
@@ -72,26 +72,31 @@ MmaFn mma_fn(int kc, int vc) {
   return nullptr;
 }
 
-// Resident CTAs per SM of the tensor-core kernel for this shape (cached per process).
-int mma_occupancy(int kc, int vc, int head_dim, int group) {
+// Resident CTAs per SM of the tensor-core kernel for this shape, and its pipelines per
+// CTA (cached per process).
+int mma_occupancy(int kc, int vc, int head_dim, int group, int* pipes) {
   static std::mutex mu;
   static int cache[4][4][3][3] = {};
+  static int cache_pipes[4][4][3][3] = {};
   const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
   const int gi = group <= 4 ? 0 : group <= 8 ? 1 : 2;
   std::lock_guard<std::mutex> lock(mu);
   int& slot = cache[kc & 3][vc & 3][di][gi];
+  int& pslot = cache_pipes[kc & 3][vc & 3][di][gi];
   if (slot == 0) {
-    int n = 0;
-    if (kc == KVQ_CODEC_BF16 && vc == KVQ_CODEC_BF16) n = mma_occupancy_bf16_bf16(head_dim, group);
-    else if (kc == KVQ_CODEC_F16 && vc == KVQ_CODEC_F16) n = mma_occupancy_f16_f16(head_dim, group);
-    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_BF16) n = mma_occupancy_q8_0_bf16(head_dim, group);
-    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q8_0_q8_0(head_dim, group);
-    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q4s_q4s(head_dim, group);
-    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q8_0_q4s(head_dim, group);
-    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q4s_q8_0(head_dim, group);
-    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_BF16) n = mma_occupancy_q4s_bf16(head_dim, group);
+    int n = 0, np = 1;
+    if (kc == KVQ_CODEC_BF16 && vc == KVQ_CODEC_BF16) n = mma_occupancy_bf16_bf16(head_dim, group, &np);
+    else if (kc == KVQ_CODEC_F16 && vc == KVQ_CODEC_F16) n = mma_occupancy_f16_f16(head_dim, group, &np);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_BF16) n = mma_occupancy_q8_0_bf16(head_dim, group, &np);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q8_0_q8_0(head_dim, group, &np);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q4s_q4s(head_dim, group, &np);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q8_0_q4s(head_dim, group, &np);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q4s_q8_0(head_dim, group, &np);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_BF16) n = mma_occupancy_q4s_bf16(head_dim, group, &np);
     slot = n > 0 ? n : 1;
+    pslot = np > 0 ? np : 1;
   }
+  *pipes = pslot;
   return slot;
 }
 
@@ -169,6 +174,7 @@ struct Plan {
   int n_chunks;
   int n_groups;
   int variant;
+  int records;       // record mode: records per (sequence, KV head), else 0
   size_t ml_off;     // chunk partials: o at 0, (m, l) at ml_off
   size_t go_off;     // group partials: o at go_off, (m, l) at gml_off
   size_t gml_off;
@@ -192,12 +198,16 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   int chunk = opts ? opts->chunk_tokens : 0;
   if (chunk < 0 || chunk % 64 != 0) return KVQ_ERR_INVALID_ARG;
   p->variant = (opts && opts->variant) ? opts->variant : 2;
+  const int group_all = num_q_heads / k->desc.num_kv_heads;
+  int pipes = 1;
+  if (p->variant == 2)
+    (void)mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec, k->desc.head_dim, group_all, &pipes);
   if (chunk == 0) {
     const int sms = sm_count();
     if (sms <= 0) return KVQ_ERR_CUDA;
     const int group = num_q_heads / k->desc.num_kv_heads;
     const int per_sm = p->variant == 2 ? mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec,
-                                                       k->desc.head_dim, group)
+                                                       k->desc.head_dim, group, &pipes)
                                        : 2;
     const long long units = (long long)batch * k->desc.num_kv_heads;
     const long long slots = (long long)sms * per_sm;
@@ -209,9 +219,10 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
     if (c < 128) c = 128;
     // With one or two CTAs per unit a long sequence among short ones would run alone
     // (lengths are on the device): keep chunks short enough for the block scheduler to
-    // balance the batch.
-    const bool capped = units * 4 > slots && c > 1024;
-    if (capped) c = 1024;
+    // balance the batch (1024 tokens per pipeline of the CTA).
+    const long long cap_tokens = 1024LL * pipes;
+    const bool capped = units * 4 > slots && c > cap_tokens;
+    if (capped) c = cap_tokens;
     chunk = (int)c;
     // One full wave: `want` chunks per unit even where rounding the chunk up to whole
     // tiles would need fewer (the tensor-core kernel deals tiles round-robin, so every
@@ -225,6 +236,24 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   const size_t D = (size_t)k->desc.head_dim;
   const size_t heads = (size_t)batch * num_q_heads;
   const size_t units = (size_t)batch * k->desc.num_kv_heads;
+  // Record mode (tensor-core kernel, at most 4 query rows per KV head, head_dim <= 128):
+  // every warp leaves its partial as a record ((chunk * pipes + pipe) * 4 + slice) and a
+  // separate merge kernel combines them.  Used while all records fit in 16 MiB (they stay
+  // in L2 between the two kernels and add little traffic); otherwise, and beyond 4096
+  // records per unit, the decode kernel merges in place (last-arriving CTA).
+  const long long recs = (long long)p->n_chunks * pipes * 4;
+  const long long rec_bytes = (long long)units * recs * (long long)(D * 4 + 8) * 4;
+  p->records = (p->variant == 2 && group_all <= 4 && D <= 128 && recs <= 4096 && rec_bytes <= (16LL << 20))
+                   ? (int)recs : 0;
+  if (p->records) {
+    p->ml_off = round_up(units * p->records * (D * 4) * sizeof(float), 256);
+    p->go_off = p->ml_off + round_up(units * p->records * 8 * sizeof(float), 256);
+    p->gml_off = p->go_off;
+    p->cnt_off = p->gml_off;
+    p->seq_cnt_off = p->cnt_off + units * (1 + p->n_groups) * sizeof(unsigned);
+    p->total = p->cnt_off + round_up((units * (1 + p->n_groups) + (size_t)batch) * sizeof(unsigned), 256);
+    return KVQ_OK;
+  }
   p->ml_off = round_up(heads * p->n_chunks * D * sizeof(float), 256);
   p->go_off = p->ml_off + round_up(heads * p->n_chunks * 2 * sizeof(float), 256);
   p->gml_off = p->go_off + round_up(heads * p->n_groups * D * sizeof(float), 256);
@@ -434,9 +463,15 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
   a.v_new = static_cast<const __nv_bfloat16*>(v_new);
   a.seq_lens_adv = seq_lens_adv;
   a.seq_counters = reinterpret_cast<unsigned*>(ws + p.seq_cnt_off);
+  a.warp_records = p.records;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (p.variant == 2)  // the tensor-core kernel merges the split itself (last CTA per unit)
-    return from_cuda(mfn(a, kd.head_dim, k_store->rows_map, v_store->rows_map, s));
+  if (p.variant == 2) {
+    // the tensor-core kernel merges the split itself (last CTA per unit), or in record
+    // mode leaves per-warp records for the merge kernel launched right after it
+    st = from_cuda(mfn(a, kd.head_dim, k_store->rows_map, v_store->rows_map, s));
+    if (st != KVQ_OK || !p.records) return st;
+    return from_cuda(launch_record_merge_pdl(a, kd.head_dim, vd.codec, s));
+  }
   st = from_cuda(sfn(a, kd.head_dim, s));
   if (st != KVQ_OK) return st;
   return from_cuda(launch_combine_pdl(a, kd.head_dim, s));

@@ -93,6 +93,27 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// L2 policy for data a call reads exactly once (the KV stream): evict first, so that the
+// stream does not push out of L2 what is reused (the kernel's code, the split partials,
+// the page table and lengths).
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_4d_ef(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                               int c3, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+      "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load_ef(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                             uint64_t policy) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -229,8 +250,7 @@ __device__ __forceinline__ void load_scale_words(const uint8_t* base, int t, uin
 
 template <int KC, int VC, int D, int GW, int HG>
 struct Cfg {
-  static constexpr int NW = 4 * HG;                       // warps (4 per head group)
-  static constexpr int THREADS = NW * 32;
+  static constexpr int PW = 4 * HG;                       // warps per pipeline (4 per head group)
   static constexpr int NPV = GW <= 4 ? 1 : 2;             // PV n-tiles per warp
   static constexpr bool KBF = KC == KVQ_CODEC_BF16;       // MMA type of QK^T
   static constexpr bool VBF = VC == KVQ_CODEC_BF16;       // MMA type of PV
@@ -248,28 +268,36 @@ struct Cfg {
   static constexpr int VSC = VQ ? kT * NB * 2 : 0;
   static constexpr int V_OFF = KROWS, KSC_OFF = KROWS + VROWS, VSC_OFF = KSC_OFF + KSC;
   static constexpr int STAGE = al1k(KROWS + VROWS + KSC + VSC);
-  // Four resident CTAs per SM (16 warps) for 4-head warps when two stages fit a quarter
-  // of the SM's shared memory: registers capped at 128 (no spills at D <= 128), else the
-  // compiler is free and register use sets the occupancy.
-  static constexpr bool FOUR = HG == 1 && GW <= 4 && D <= 128 && 2 * STAGE + 6 * 1024 <= 56 * 1024;
-  static constexpr int MINB = FOUR ? 4 : 1;
-  // ring depth: as many stages (2..4) as fit the per-CTA budget that keeps the
-  // intended number of resident CTAs per SM
-  static constexpr int SMEM_BUDGET = HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : FOUR ? 54 * 1024 : 70 * 1024;
+  // Four pipelines per CTA (one CTA per SM, 16 warps) for 4-head warps when two stages
+  // fit a quarter of the SM's shared memory: registers capped at 128 (no spills at
+  // D <= 128).  Each pipeline is 4 warps with its own ring of stages; the CTA merges its
+  // pipelines in shared memory, so a split has a quarter as many partials as with one
+  // pipeline per CTA.  Otherwise one pipeline per CTA and register use sets occupancy.
+  static constexpr bool PACK = HG == 1 && GW <= 4 && D <= 128 && 2 * STAGE + 6 * 1024 <= 56 * 1024;
+  static constexpr int NP = PACK ? 4 : 1;                 // pipelines per CTA
+  // the lean tile loop (see decode_cta) serves warps of at most 4 heads at D <= 128
+  static constexpr bool LEAN = HG == 1 && GW <= 4 && D <= 128;
+  static constexpr int NW = PW * NP;                      // warps per CTA
+  static constexpr int THREADS = NW * 32;
+  static constexpr int MINB = 1;
+  // ring depth per pipeline: as many stages (2..4) as fit the per-pipeline budget
+  static constexpr int SMEM_BUDGET = HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : PACK ? 54 * 1024 : 70 * 1024;
   static constexpr int NS0 = (SMEM_BUDGET - 2048) / STAGE;
   static constexpr int NS = NS0 > 4 ? 4 : (NS0 < 2 ? 2 : NS0);
-  static constexpr int OBUF = NW * 8 * D * 4;             // merge buffer (reuses the ring)
-  static constexpr int RING = NS * STAGE > OBUF ? NS * STAGE : OBUF;
-  static constexpr int BAR_OFF = RING;                    // 2*NS mbarriers
-  static constexpr int OK_OFF = BAR_OFF + 2 * NS * 8;     // per-stage "tile is valid" flags
-  static constexpr int KB_OFF = OK_OFF + 32;              // QK accumulator seeds [HG][NB][4] f32x2
-  static constexpr int ML_OFF = KB_OFF + HG * NB * 4 * 8; // per-warp m, l [8][2]
+  static constexpr int PRING = NS * STAGE;                // one pipeline's ring
+  static constexpr int OBUF = NW * 8 * D * 4;             // merge buffer (reuses the rings)
+  static constexpr int RING = NP * PRING > OBUF ? NP * PRING : OBUF;
+  static constexpr int BAR_OFF = RING;                    // [NP][full NS | empty NS] mbarriers
+  static constexpr int OK_OFF = BAR_OFF + NP * 2 * NS * 8;  // [NP][NS] "tile is valid" flags, then a flag
+  static constexpr int KB_OFF = OK_OFF + 128;             // QK accumulator seeds [HG][NB][4] f32x2
+  static constexpr int ML_OFF = KB_OFF + HG * NB * 4 * 8; // per-warp m, l [NW][8][2]
   static constexpr int SMEM = ML_OFF + (NW + 2) * 16 * 4 + 1024;  // + per-head (M, l); +1024: alignment
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
   static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
   // 233472 bytes of shared memory per SM, 1024 of them reserved per resident CTA
-  static_assert(!FOUR || 4 * (SMEM + 1024) <= 233472, "four CTAs per SM must fit");
+  static_assert(!PACK || SMEM + 1024 <= 233472, "the four pipelines must fit one SM");
+  static_assert(NP * NS <= 16, "stage flags");
 };
 
 // Shared-memory address of 16-byte chunk `chunk` of tile row `t` (rows as TMA wrote them).
@@ -327,36 +355,48 @@ __device__ __forceinline__ bool arrive_last(unsigned* counter, int expected, int
 //   M = max_c m_c, l = sum_c 2^(m_c - M) l_c, O = sum_c 2^(m_c - M) O_c.
 // Head h's partial c sits at ml[(h * stride + c) * 2] and o[(h * stride + c) * D].
 // With `final` the normalized output O / l goes to out[h * D]; otherwise (M, l, O) go
-// to out_ml[h * out_stride * 2] / out_o[h * out_stride * D].  Weights are staged in
-// shared memory when they fit; every thread of the CTA takes part.
+// to out_ml[h * out_stride * 2] / out_o[h * out_stride * D].  Every thread of the CTA
+// takes part (it contains a CTA barrier).
+//
+// Latency is what counts here (the last CTA of a split runs it after everything else):
+// the items (head, 4 consecutive elements) are spread over the CTA's threads together
+// with the partials, so that each thread loads at most kBatch partials, all at once (one
+// L2 round trip); when several threads share an item, their running results meet in
+// shared memory (`scratch`, 6 floats per thread) and one of them folds them in order.
 template <int D, int NW>
 __device__ void merge_partials(const float* ml, const float* o, long long stride, int count, int gcount,
-                               bool final, float* out_ml, float* out_o, long long out_stride, float* out) {
-  // Thread per (head, 4 consecutive elements).  One pass: each batch of up to 16 chunks
-  // loads their (m, l) and rows together (one L2 round trip per batch) and folds them in
-  // with a running maximum, in chunk order.
+                               bool final, float* out_ml, float* out_o, long long out_stride, float* out,
+                               float* scratch) {
   constexpr int D4 = D / 4;
-  constexpr int BATCH = 16;
-  for (int item = threadIdx.x; item < gcount * D4; item += NW * 32) {
+  constexpr int NT = NW * 32;
+  constexpr int kBatch = 8;
+  const int items = gcount * D4;
+  int nsplit = NT / items;                        // threads per item
+  if (nsplit > count) nsplit = count;
+  if (nsplit < 1) nsplit = 1;
+  const int per = (count + nsplit - 1) / nsplit;  // partials per thread
+  // running (M, den, acc) of partials [c0, c1) of item `item`
+  auto fold = [&](int item, int c0, int c1, float& M, float& den, float4& acc) {
     const int h = item / D4, col = item % D4;
     const float2* ml_h = reinterpret_cast<const float2*>(ml + h * stride * 2);
     const float4* o_h = reinterpret_cast<const float4*>(o + h * stride * D) + col;
-    float M = -INFINITY, den = 0.0f;
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int c0 = 0; c0 < count; c0 += BATCH) {
-      const int n = min(BATCH, count - c0);
-      float2 mlv[BATCH];
-      float4 v[BATCH];
+    M = -INFINITY;
+    den = 0.0f;
+    acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int b0 = c0; b0 < c1; b0 += kBatch) {
+      const int n = min(kBatch, c1 - b0);
+      float2 mlv[kBatch];
+      float4 v[kBatch];
 #pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         if (u < n) {
-          mlv[u] = __ldcg(ml_h + c0 + u);
-          v[u] = __ldcg(o_h + (long long)(c0 + u) * D4);
+          mlv[u] = __ldcg(ml_h + b0 + u);
+          v[u] = __ldcg(o_h + (long long)(b0 + u) * D4);
         }
       }
       float bm = M;
 #pragma unroll
-      for (int u = 0; u < BATCH; ++u)
+      for (int u = 0; u < kBatch; ++u)
         if (u < n) bm = fmaxf(bm, mlv[u].x);
       if (bm == -INFINITY) continue;
       const float f = fast_exp2(M - bm);   // 0 when M = -inf
@@ -364,7 +404,7 @@ __device__ void merge_partials(const float* ml, const float* o, long long stride
       acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
       M = bm;
 #pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         if (u < n && mlv[u].x != -INFINITY) {
           const float w = fast_exp2(mlv[u].x - M);
           den = fmaf(w, mlv[u].y, den);
@@ -375,6 +415,9 @@ __device__ void merge_partials(const float* ml, const float* o, long long stride
         }
       }
     }
+  };
+  auto emit = [&](int item, float M, float den, float4 acc) {
+    const int h = item / D4, col = item % D4;
     if (final) {
       const float inv = den > 0.0f ? 1.0f / den : 0.0f;
       reinterpret_cast<float4*>(out + h * D)[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -382,6 +425,42 @@ __device__ void merge_partials(const float* ml, const float* o, long long stride
       reinterpret_cast<float4*>(out_o + h * out_stride * D)[col] = acc;
       if (col == 0) reinterpret_cast<float2*>(out_ml + h * out_stride * 2)[0] = make_float2(M, den);
     }
+  };
+  // one (item, slice) per thread when the items are split (items * nsplit <= NT), else
+  // every thread folds whole items in turn
+  const int t = threadIdx.x;
+  for (int it = t; it < items * nsplit; it += NT) {
+    const int item = it % items, sg = it / items;
+    float M, den;
+    float4 acc;
+    fold(item, sg * per, min(count, sg * per + per), M, den, acc);
+    if (nsplit == 1) {
+      emit(item, M, den, acc);
+    } else {
+      float* sc = scratch + it * 6;
+      sc[0] = M; sc[1] = den; sc[2] = acc.x; sc[3] = acc.y; sc[4] = acc.z; sc[5] = acc.w;
+    }
+  }
+  if (nsplit == 1) return;
+  asm volatile("bar.sync 1, %0;" ::"r"(NT) : "memory");
+  for (int item = t; item < items; item += NT) {
+    float M = -INFINITY;
+    for (int sg = 0; sg < nsplit; ++sg) M = fmaxf(M, scratch[(sg * items + item) * 6]);
+    float den = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (M != -INFINITY) {
+      for (int sg = 0; sg < nsplit; ++sg) {
+        const float* sc = scratch + (sg * items + item) * 6;
+        if (sc[0] == -INFINITY) continue;
+        const float w = fast_exp2(sc[0] - M);
+        den = fmaf(w, sc[1], den);
+        acc.x = fmaf(w, sc[2], acc.x);
+        acc.y = fmaf(w, sc[3], acc.y);
+        acc.z = fmaf(w, sc[4], acc.z);
+        acc.w = fmaf(w, sc[5], acc.w);
+      }
+    }
+    emit(item, M, den, acc);
   }
 }
 
@@ -402,14 +481,22 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // 1024-byte alignment for the 128-byte swizzle pattern
   // (offset from the array itself, so accesses through `smem` stay in the shared space)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + C::BAR_OFF;           // + 8*s
-  const uint32_t bar_empty = sbase + C::BAR_OFF + 8 * C::NS;
-  float* ml_all = reinterpret_cast<float*>(smem + C::ML_OFF);
-  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + C::OK_OFF);
-
   const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Pipeline of this warp: its own ring of NS stages, barriers and stage flags.  The CTA's
+  // pipelines take the tiles of "virtual chunks" vchunk = pipe * n_chunks + chunk
+  // (pipe-major, so that the pipelines dealt one more tile than the rest spread over all
+  // the CTAs of the unit: every SM gets the same number of tiles, to within one).
+  const int pipe = warp / C::PW, pw = warp % C::PW;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sring = sbase + pipe * C::PRING;                 // this pipeline's ring
+  uint8_t* const ring = smem + pipe * C::PRING;
+  const uint32_t bar_full = sbase + C::BAR_OFF + pipe * 16 * C::NS;   // + 8*s
+  const uint32_t bar_empty = bar_full + 8 * C::NS;
+  float* ml_all = reinterpret_cast<float*>(smem + C::ML_OFF);
+  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + C::OK_OFF) + pipe * C::NS;
+  const int vchunk = pipe * a.n_chunks + chunk;
+  const int nvc = a.n_chunks * C::NP;
   const int G = a.group;         // query heads (virtual: head x query token) per KV head
   const int T = a.tokens;        // query tokens per sequence (1: plain decode)
   const int P = a.k.page_size;
@@ -427,11 +514,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // tile pb + 32 + i in pg_hi.  The first 64 are read together with seq_lens (any
   // in-bounds table entry may be read; entries past the sequence are never used).
   auto load_page = [&](int tile) -> int {
-    const long long pos0 = ((long long)chunk + (long long)tile * a.n_chunks) * kT;
+    const long long pos0 = ((long long)vchunk + (long long)tile * nvc) * kT;
     return pos0 < (long long)a.max_pages * P ? __ldg(pt + pos0 / P) : -1;
   };
   int pg_lo = -1, pg_hi = -1, pb = 0;
-  if (warp == 0) {
+  if (pw == 0) {
     pg_lo = load_page(lane);
     pg_hi = load_page(32 + lane);
   }
@@ -439,7 +526,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // CTA whose tile holds the token; the reads are in bounds for every CTA).
   constexpr int EPL = D / 32;
   float xk[EPL], xv[EPL];
-  if (a.k_new != nullptr && warp == 0) {
+  if (a.k_new != nullptr && pw == 0) {
     const long long row = (long long)b * a.k.num_kv_heads + kvh;
     load_row<EPL>(a.k_new + row * D, lane, xk);
     load_row<EPL>(a.v_new + row * D, lane, xv);
@@ -457,55 +544,61 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     Lraw = L_old < 0 ? 0 : cap;
   }
   const int L = (int)Lraw;
-  // The sequence's 64-token tiles are dealt round-robin to its n_chunks CTAs: CTA c
-  // takes tiles c, c + n_chunks, ... so that every CTA streams from all of the
-  // sequence's pages (evens out per-CTA speed) and all finish together.
+  // The sequence's 64-token tiles are dealt round-robin to the nvc pipelines of its
+  // n_chunks CTAs: pipeline v takes tiles v, v + nvc, ... so that every pipeline streams
+  // from all of the sequence's pages (evens out per-pipeline speed) and all finish together.
   const int NT = (L + kT - 1) / kT;                 // tiles of the sequence
-  const int nv = min(a.n_chunks, NT);   // CTAs with work for this (b, kvh)
-  // Fused advance of seq_lens[b].  Arrivals on the sequence's counter: every early-exiting
-  // CTA, and per (sequence, KV head) the one CTA that finishes the split, which arrives
-  // only after every CTA of its unit has arrived on the merge counters (so after their
-  // reads of seq_lens).  The holder of the last ticket stores the new length.  A
-  // finishing CTA takes its ticket before its final merge and checks it after, so the
-  // atomic's latency overlaps the merge.
+  const int nv = min(a.n_chunks, NT);   // CTAs with work for this (b, kvh): pipeline 0 has a tile
+  // Fused advance of seq_lens[b]: every CTA of the sequence takes one ticket on its
+  // counter once all its threads have read seq_lens[b] (a CTA barrier, then a release
+  // add), early in the kernel and off the tile producer's path; the holder of the last
+  // ticket stores the new length and returns the counter to zero.  Nothing of it is left
+  // for the end of the kernel.
   const bool adv = a.seq_lens_adv != nullptr;
-  const unsigned seq_total = gridDim.y * (unsigned)(a.n_chunks - nv + (nv > 0 ? 1 : 0));
-  auto seq_finish = [&](unsigned ticket) {   // thread 0
-    if (ticket >= seq_total) record_fault(a.k.status, KVQ_DEVICE_BAD_WORKSPACE);
-    if (ticket == seq_total - 1) {
+  auto seq_ticket = [&]() {   // one thread per CTA, after a CTA barrier
+    const unsigned total = gridDim.x * gridDim.y;
+    const unsigned ticket = seq_arrive(a.seq_counters + b);
+    if (ticket >= total) record_fault(a.k.status, KVQ_DEVICE_BAD_WORKSPACE);
+    if (ticket == total - 1) {
       asm volatile("fence.acq_rel.gpu;" ::: "memory");   // after every counted arrival
       if (len_ok) a.seq_lens_adv[b] = (int32_t)(L_old + 1);
       a.seq_counters[b] = 0u;
     }
   };
-  if (chunk >= NT) {
-    if (L == 0 && chunk == 0) {  // empty sequence: its heads' outputs are zero
+  if (chunk >= nv) {
+    if (C::LEAN && a.warp_records > 0) {
+      // record mode: this CTA's records are empty (m = -inf), the merge skips them
+      const long long rec0 = ((long long)b * gridDim.y + kvh) * a.warp_records + (long long)chunk * C::NW;
+      for (int i = tid; i < C::NW * 2; i += C::THREADS)
+        reinterpret_cast<float4*>(a.part_ml + (rec0 + i / 2) * 8)[i & 1] = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+    } else if (L == 0 && chunk == 0) {  // empty sequence: its heads' outputs are zero
       const long long h0 = (long long)b * a.num_q_heads + (long long)kvh * G;
       for (int idx = tid; idx < G * D; idx += C::THREADS) a.out[h0 * D + idx] = 0.0f;
     }
-    if (adv) {
+    if (adv && !(C::LEAN && a.warp_records > 0)) {
       __syncthreads();   // every thread has read seq_lens
-      if (tid == 0) seq_finish(seq_arrive(a.seq_counters + b));
+      if (tid == 0) seq_ticket();
     }
     return;
   }
-  const int n_tiles = (NT - chunk + a.n_chunks - 1) / a.n_chunks;
+  const int n_tiles = vchunk < NT ? (NT - vchunk + nvc - 1) / nvc : 0;   // this pipeline's
 
-  if (tid == 0) {
+  if (pw == 0 && lane == 0) {
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, C::NW);
+      mbar_init(bar_empty + 8 * s, C::PW);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  __syncthreads();   // also: every thread has read seq_lens
 
   // ------------------------------------------------------------ tile producer
-  // Lane 0 of warp 0 issues the copies: the first NS tiles up front, then tile k + NS
-  // into stage k % NS as soon as every warp has released tile k.
+  // Lane 0 of the pipeline's first warp issues its copies: the first NS tiles up front,
+  // then tile k + NS into stage k % NS as soon as every warp of the pipeline has released
+  // tile k.
   auto issue_tile = [&](int tile, int page) {
     const int s = tile % C::NS;
-    const int pos0 = (chunk + tile * a.n_chunks) * kT;
+    const int pos0 = (vchunk + tile * nvc) * kT;
     const int row0 = pos0 % P;
     const uint32_t full = bar_full + 8 * s;
     // the flag is published to the warps by the mbarrier phase that completes below
@@ -518,26 +611,27 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       return;
     }
     mbar_expect_tx(full, C::K_TX + C::V_TX);
-    const uint32_t st = sbase + s * C::STAGE;
+    const uint32_t st = sring + s * C::STAGE;
+    const uint64_t pol = evict_first_policy();
 #pragma unroll
     for (int seg = 0; seg < (C::KRB + 127) / 128; ++seg)
-      tma_load_4d(st + seg * kT * 128, &tmk, seg * 128, row0, kvh, page, full);
+      tma_load_4d_ef(st + seg * kT * 128, &tmk, seg * 128, row0, kvh, page, full, pol);
     const uint32_t vst = st + C::V_OFF;
 #pragma unroll
     for (int seg = 0; seg < (C::VRB + 127) / 128; ++seg)
-      tma_load_4d(vst + seg * kT * 128, &tmv, seg * 128, row0, kvh, page, full);
+      tma_load_4d_ef(vst + seg * kT * 128, &tmv, seg * 128, row0, kvh, page, full, pol);
     if constexpr (C::KQ) {
       const uint8_t* src = a.k.buf + ((long long)page * a.k.num_kv_heads + kvh) * a.k.slab_bytes +
                            (long long)P * C::KRB + (long long)row0 * C::NB * 2;
-      bulk_load(st + C::KSC_OFF, src, kT * C::NB * 2, full);
+      bulk_load_ef(st + C::KSC_OFF, src, kT * C::NB * 2, full, pol);
     }
     if constexpr (C::VQ) {
       const uint8_t* src = a.v.buf + ((long long)page * a.v.num_kv_heads + kvh) * a.v.slab_bytes +
                            (long long)P * C::VRB + (long long)row0 * C::NB * 2;
-      bulk_load(st + C::VSC_OFF, src, kT * C::NB * 2, full);
+      bulk_load_ef(st + C::VSC_OFF, src, kT * C::NB * 2, full, pol);
     }
   };
-  // Page of tile t (t >= pb, nondecreasing over calls), by all of warp 0.  Crossing a
+  // Page of tile t (t >= pb, nondecreasing over calls), by all of the producer warp.  Crossing a
   // 32-tile boundary shifts the window and starts the loads for the batch after next,
   // 32 tiles before they are needed.
   auto page_of = [&](int t) -> int {
@@ -551,8 +645,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // Fused append: the CTA holding the new token's tile (its last) encodes the token's K
   // and V rows with warp 0 before that tile's copies are issued; the proxy fence orders
   // the rows' generic-proxy stores before the bulk-tensor reads.
-  bool need_enc = fused && len_ok && chunk == (NT - 1) % a.n_chunks;
-  auto encode_new = [&]() {   // by all of warp 0; the token lies in this CTA's last tile
+  bool need_enc = fused && len_ok && vchunk == (NT - 1) % nvc;
+  auto encode_new = [&]() {   // by all of the producer warp; the token lies in its pipeline's last tile
     const int t = n_tiles - 1;   // read without moving page_of's window
     const int lo = __shfl_sync(0xffffffffu, pg_lo, (t - pb) & 31);
     const int hi = __shfl_sync(0xffffffffu, pg_hi, (t - pb) & 31);
@@ -566,7 +660,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     __syncwarp();
     need_enc = false;
   };
-  if (warp == 0) {
+  if (pw == 0) {
     for (int tile = 0; tile < n_tiles && tile < C::NS; ++tile) {
       if (need_enc && tile == n_tiles - 1) encode_new();
       const int page = page_of(tile);
@@ -577,8 +671,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   }
 
   // ------------------------------------------------------------ compute warps
-  const int hg = warp >> 2;          // head group
-  const int ws = warp & 3;           // 16-token slice of every tile
+  const int hg = pw >> 2;            // head group
+  const int ws = pw & 3;             // 16-token slice of every tile
   const int r = lane >> 2, i4 = lane & 3;
   const int t0 = ws * 16;
 
@@ -608,6 +702,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // Kept in shared memory ([head group][block][i4], float2): every lane of a head group
   // with the same i4 needs the same pair.
   float2* kbs = reinterpret_cast<float2*>(smem + C::KB_OFF);
+  float2 kbr[C::NB];   // the same seeds in registers (lean loop)
 #pragma unroll
   for (int bb = 0; bb < C::NB; ++bb) {
     float part = 0.0f;
@@ -625,9 +720,14 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     const float bias = KC == KVQ_CODEC_Q4S ? kBias4K : kBias8;
     const float k0 = -bias * __shfl_sync(0xffffffffu, part, 4 * (2 * i4));
     const float k1 = -bias * __shfl_sync(0xffffffffu, part, 4 * (2 * i4 + 1));
-    if (ws == 0 && r == 0) kbs[(hg * C::NB + bb) * 4 + i4] = make_float2(k0, k1);
+    if (!C::LEAN && pipe == 0 && ws == 0 && r == 0) kbs[(hg * C::NB + bb) * 4 + i4] = make_float2(k0, k1);
+    kbr[bb] = make_float2(k0, k1);
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(C::THREADS) : "memory");
+  if constexpr (!C::LEAN) asm volatile("bar.sync 1, %0;" ::"r"(C::THREADS) : "memory");   // seeds in smem
+  // Fused advance outside record mode (there the merge kernel stores the new length): the
+  // last warp takes the CTA's ticket, after every CTA-wide barrier before the tile loop,
+  // so that its wait holds up no other warp.
+  if (adv && !(C::LEAN && a.warp_records > 0) && warp == C::NW - 1 && lane == 0) seq_ticket();
 
   float o[C::QSTEPS][C::NPV][4];   // O^T accumulators: D/16 M-tiles x NPV n-tiles
 #pragma unroll
@@ -643,307 +743,590 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   int E = -100;                                                 // running V-scale exponent bound
   bool timed_out = false;
 
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    const int s = tile % C::NS;
-    if (!mbar_wait_warp(bar_full + 8 * s, (tile / C::NS) & 1)) {
-      timed_out = true;
-      break;
-    }
-    const int pos_w = (chunk + tile * a.n_chunks) * kT + t0;
-    const bool tile_ok = stage_ok[s] != 0;
-    const int n_valid = tile_ok ? max(0, min(16, L - pos_w)) : 0;
-    if (n_valid > 0) {
-      const bool partial = n_valid < 16;
-      const uint32_t st = sbase + s * C::STAGE;
-      const uint32_t kst = st, vst = st + C::V_OFF;
-      const uint8_t* ksc = smem + s * C::STAGE + C::KSC_OFF;
-      const uint8_t* vsc = smem + s * C::STAGE + C::VSC_OFF;
-      const int mi = lane >> 3, mr = lane & 7;
-
-      // ---------------- QK^T: S[tok r / r+8][heads 2i, 2i+1] (log2 units after scaling)
-      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if constexpr (C::KQ) {
-        // block scales of rows r and r+8
-        float dk[2][C::NB];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          uint32_t w[C::NB / 2];
-          load_scale_words<C::NB>(ksc, t0 + r + 8 * rr, w);
-#pragma unroll
-          for (int k = 0; k < C::NB / 2; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-            dk[rr][2 * k] = f.x;
-            dk[rr][2 * k + 1] = f.y;
-          }
-        }
-        if constexpr (KC == KVQ_CODEC_Q8_0) {
-#pragma unroll
-          for (int bb = 0; bb < C::NB; ++bb) {
-            uint32_t x0, x1, x2, x3;
-            ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * bb + (mi >> 1)), x0, x1, x2, x3);
-            x0 ^= 0x80808080u; x1 ^= 0x80808080u; x2 ^= 0x80808080u; x3 ^= 0x80808080u;
-            // accumulator seeded with -1152 * sum(q) of the block: removes the code offset
-            const float2 kb = kbs[(hg * C::NB + bb) * 4 + i4];
-            float cb[4] = {kb.x, kb.y, kb.x, kb.y};
-            uint32_t af[4];
-            af[0] = i8pair_raw(x0, 0x4140); af[1] = i8pair_raw(x1, 0x4140);
-            af[2] = i8pair_raw(x0, 0x4342); af[3] = i8pair_raw(x1, 0x4342);
-            mma16816<false>(cb, af, qf[2 * bb][0], qf[2 * bb][1]);
-            af[0] = i8pair_raw(x2, 0x4140); af[1] = i8pair_raw(x3, 0x4140);
-            af[2] = i8pair_raw(x2, 0x4342); af[3] = i8pair_raw(x3, 0x4342);
-            mma16816<false>(cb, af, qf[2 * bb + 1][0], qf[2 * bb + 1][1]);
-            sc[0] = fmaf(dk[0][bb], cb[0], sc[0]);
-            sc[1] = fmaf(dk[0][bb], cb[1], sc[1]);
-            sc[2] = fmaf(dk[1][bb], cb[2], sc[2]);
-            sc[3] = fmaf(dk[1][bb], cb[3], sc[3]);
-          }
-        } else {  // q4s: one ldmatrix.x4 covers two blocks
-#pragma unroll
-          for (int bb = 0; bb < C::NB; bb += 2) {
-            uint32_t x[4];
-            ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), x[0], x[1], x[2], x[3]);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const uint32_t ra = x[2 * h2], rb = x[2 * h2 + 1];  // rows r and r+8 of block bb+h2
-              const float2 kb = kbs[(hg * C::NB + bb + h2) * 4 + i4];
-              float cb[4] = {kb.x, kb.y, kb.x, kb.y};
-              uint32_t af[4];
-              af[0] = u4pair_half(ra << 6); af[1] = u4pair_half(rb << 6);
-              af[2] = u4pair_half(ra << 2); af[3] = u4pair_half(rb << 2);
-              mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
-              af[0] = u4pair_half(ra >> 2); af[1] = u4pair_half(rb >> 2);
-              af[2] = u4pair_half(ra >> 6); af[3] = u4pair_half(rb >> 6);
-              mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
-              sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
-              sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);
-              sc[2] = fmaf(dk[1][bb + h2], cb[2], sc[2]);
-              sc[3] = fmaf(dk[1][bb + h2], cb[3], sc[3]);
-            }
-          }
-        }
-      } else {  // 16-bit K: natural k order, one ldmatrix.x4 per k16 step
-#pragma unroll
-        for (int ks = 0; ks < C::QSTEPS; ++ks) {
-          uint32_t af[4];
-          ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), af[0], af[1], af[2], af[3]);
-          mma16816<C::KBF>(sc, af, qf[ks][0], qf[ks][1]);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sc[k] *= qk_mul;
-      if (partial) {
-        if (r >= n_valid) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
-        if (r + 8 >= n_valid) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
-      }
-      if (T > 1 && pos_w + 16 > L - T + 1) {
-        // causal limit of the query tokens (virtual head v = head * T + i sees the positions
-        // below L - T + 1 + i): only the sequence's last T - 1 positions are masked
-        const int cA = 2 * i4, cB = 2 * i4 + 1;   // this lane's QK columns
-        const int vA = hg * GW + (GW <= 4 ? (cA & 3) : cA), vB = hg * GW + (GW <= 4 ? (cB & 3) : cB);
-        const int limA = L - T + 1 + vA % T, limB = L - T + 1 + vB % T;
-        if (pos_w + r >= limA) sc[0] = -INFINITY;
-        if (pos_w + r >= limB) sc[1] = -INFINITY;
-        if (pos_w + r + 8 >= limA) sc[2] = -INFINITY;
-        if (pos_w + r + 8 >= limB) sc[3] = -INFINITY;
-      }
-
-      // ---------------- V scales of this lane's PV tokens (2i, 2i+1, 2i+8, 2i+9)
-      const int tk[4] = {2 * i4, 2 * i4 + 1, 2 * i4 + 8, 2 * i4 + 9};
-      uint32_t dvw[4][C::NB / 2 > 0 ? C::NB / 2 : 1];
-      int ex_lane = 0;   // every scale of this lane's tokens is < 2^ex_lane
-      if constexpr (C::VQ) {
-        uint32_t mx = 0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          load_scale_words<C::NB>(vsc, t0 + tk[u], dvw[u]);
-          if (partial && tk[u] >= n_valid) {
-#pragma unroll
-            for (int k = 0; k < C::NB / 2; ++k) dvw[u][k] = 0u;
-          }
-#pragma unroll
-          for (int k = 0; k < C::NB / 2; ++k) mx = __vmaxu2(mx, dvw[u][k]);
-        }
-        const uint32_t hmax = max(mx & 0xffffu, mx >> 16);   // scales are >= 0: bits order as values
-        const int e = (int)(hmax >> 10);
-        ex_lane = hmax ? max(e, 1) - 14 : -127;
-      }
-
-      // ---------------- lazy online softmax over the warp's 16 tokens (columns = heads)
-      const float lm0 = fmaxf(sc[0], sc[2]), lm1 = fmaxf(sc[1], sc[3]);
-      const bool over = (lm0 > m0 + kLazy) || (lm1 > m1 + kLazy) || (ex_lane > E);
-      if (__any_sync(0xffffffffu, over)) {
-        float mx0 = lm0, mx1 = lm1;
-        int ex = ex_lane;
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, 1));
-        ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, 2));
-        const int E_new = max(E, ex);
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float e2 = __uint_as_float((uint32_t)(127 + E - E_new) << 23);  // 2^(E - E_new)
-        float f0 = (mn0 == -INFINITY) ? 1.0f : fast_exp2(m0 - mn0);
-        float f1 = (mn1 == -INFINITY) ? 1.0f : fast_exp2(m1 - mn1);
-        l0 *= f0;
-        l1 *= f1;
-        f0 *= e2;
-        f1 *= e2;
-#pragma unroll
-        for (int mt = 0; mt < C::QSTEPS; ++mt)
-#pragma unroll
-          for (int n = 0; n < C::NPV; ++n) {
-            o[mt][n][0] *= f0; o[mt][n][1] *= f1; o[mt][n][2] *= f0; o[mt][n][3] *= f1;
-          }
-        m0 = mn0;
-        m1 = mn1;
-        E = E_new;
-      }
-      // m0, m1 are finite here unless a causal limit masked a column everywhere so far: the
-      // warp has a valid token, whose score raised them
-      float p0 = fast_exp2(sc[0] - m0);
-      float p1 = fast_exp2(sc[1] - m1);
-      float p2 = fast_exp2(sc[2] - m0);
-      float p3 = fast_exp2(sc[3] - m1);
-      if (T > 1) {
-        if (sc[0] == -INFINITY) p0 = 0.0f;
-        if (sc[1] == -INFINITY) p1 = 0.0f;
-        if (sc[2] == -INFINITY) p2 = 0.0f;
-        if (sc[3] == -INFINITY) p3 = 0.0f;
-      }
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-
-      // ---------------- transpose p (fp32, as two 16-bit halves) to the PV B layout:
-      // lane (r, i) receives p[tok 2i, 2i+1, 2i+8, 2i+9][column r]
-      float pv[4];
-      {
-        const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-        const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
-        const uint32_t ah = movtrans(__byte_perm(u0, u1, 0x7632)), al = movtrans(__byte_perm(u0, u1, 0x5410));
-        const uint32_t bh = movtrans(__byte_perm(u2, u3, 0x7632)), bl = movtrans(__byte_perm(u2, u3, 0x5410));
-        pv[0] = __uint_as_float(__byte_perm(al, ah, 0x5410));
-        pv[1] = __uint_as_float(__byte_perm(al, ah, 0x7632));
-        pv[2] = __uint_as_float(__byte_perm(bl, bh, 0x5410));
-        pv[3] = __uint_as_float(__byte_perm(bl, bh, 0x7632));
-      }
-
-      // ---------------- PV
-      const float pscale = __uint_as_float((uint32_t)(127 + kPScale - E) << 23);  // 2^(kPScale - E)
-#pragma unroll
-      for (int u = 0; u < 4; ++u) pv[u] *= pscale;
-      // PV column r of an 8-column tile is head r&3's hi part (r < 4) or lo part (r >= 4)
-      // when one n-tile carries both; lo lanes feed x - f16(x) instead of x.
-      const unsigned short lo_sel = (C::NPV == 1 && r >= 4) ? (C::VBF ? 0xBF80 : 0xBC00) : 0;
-      if constexpr (C::VQ) {
-        uint32_t vq4[4];   // q4s: one ldmatrix.x4 covers blocks bb and bb + 1 (bb even)
-#pragma unroll
-        for (int bb = 0; bb < C::NB; ++bb) {
-          float x[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const __half hv = __ushort_as_half((unsigned short)(dvw[u][bb >> 1] >> (16 * (bb & 1))));
-            x[u] = pv[u] * __half2float(hv);
-          }
-          uint32_t bf[C::NPV][2];
-          if constexpr (C::NPV == 1) {
-            bf[0][0] = hi_or_lo<C::VBF>(x[0], x[1], lo_sel);
-            bf[0][1] = hi_or_lo<C::VBF>(x[2], x[3], lo_sel);
-          } else {
-            split2<C::VBF>(x[0], x[1], bf[0][0], bf[1][0]);
-            split2<C::VBF>(x[2], x[3], bf[0][1], bf[1][1]);
-          }
-          if constexpr (VC == KVQ_CODEC_Q8_0) {
-            uint32_t y0, y1, y2, y3;
-            // matrices: (tok 0-7, chunk 2b), (tok 0-7, chunk 2b+1), (tok 8-15, 2b), (tok 8-15, 2b+1)
-            ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * bb + (mi & 1)), y0, y1, y2, y3);
-            y0 ^= 0x80808080u; y1 ^= 0x80808080u; y2 ^= 0x80808080u; y3 ^= 0x80808080u;
-            uint32_t ae[4] = {i8pair_raw(y0, 0x4240), i8pair_raw(y1, 0x4240), i8pair_raw(y2, 0x4240),
-                              i8pair_raw(y3, 0x4240)};
-            uint32_t ao[4] = {i8pair_raw(y0, 0x4341), i8pair_raw(y1, 0x4341), i8pair_raw(y2, 0x4341),
-                              i8pair_raw(y3, 0x4341)};
-            // exact small integers in f16 before the product: an offset folded into the fp32
-            // accumulator instead loses its low bits there, and that error grows with the chunk
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              ae[k] = hsub2_u32(ae[k], 0x64806480u);
-              ao[k] = hsub2_u32(ao[k], 0x64806480u);
-            }
-#pragma unroll
-            for (int n = 0; n < C::NPV; ++n) {
-              mma16816<false>(o[2 * bb][n], ae, bf[n][0], bf[n][1]);
-              mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
-            }
-          } else {  // q4s: matrices (tok 0-7, chunk b), (tok 8-15, chunk b) for this block
-            if ((bb & 1) == 0)
-              ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), vq4[0], vq4[1], vq4[2], vq4[3]);
-            const uint32_t ya = (bb & 1) ? vq4[2] : vq4[0], yb = (bb & 1) ? vq4[3] : vq4[1];
-            const uint32_t ya8 = ya >> 8, yb8 = yb >> 8;
-            // even nibbles: 1024 + u, less 1032; odd nibbles in place: (1024 + 16 u) / 16 - 72
-            const uint32_t a01[4] = {hsub2_u32(u4pair_raw(ya), 0x64086408u),
-                                     hfma2_u32(u4pair_hi_raw(ya), kSixteenth2, kMinus72x2),
-                                     hsub2_u32(u4pair_raw(yb), 0x64086408u),
-                                     hfma2_u32(u4pair_hi_raw(yb), kSixteenth2, kMinus72x2)};
-            const uint32_t a23[4] = {hsub2_u32(u4pair_raw(ya8), 0x64086408u),
-                                     hfma2_u32(u4pair_hi_raw(ya8), kSixteenth2, kMinus72x2),
-                                     hsub2_u32(u4pair_raw(yb8), 0x64086408u),
-                                     hfma2_u32(u4pair_hi_raw(yb8), kSixteenth2, kMinus72x2)};
-#pragma unroll
-            for (int n = 0; n < C::NPV; ++n) {
-              mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
-              mma16816<false>(o[2 * bb + 1][n], a23, bf[n][0], bf[n][1]);
-            }
-          }
-        }
-      } else {
-        // 16-bit V: one B operand for every M-tile; zero the A lanes of tokens past the end
-        uint32_t bf[C::NPV][2];
-        if constexpr (C::NPV == 1) {
-          bf[0][0] = hi_or_lo<C::VBF>(pv[0], pv[1], lo_sel);
-          bf[0][1] = hi_or_lo<C::VBF>(pv[2], pv[3], lo_sel);
-        } else {
-          split2<C::VBF>(pv[0], pv[1], bf[0][0], bf[1][0]);
-          split2<C::VBF>(pv[2], pv[3], bf[0][1], bf[1][1]);
-        }
-        uint32_t kmask_lo = 0xffffffffu, kmask_hi = 0xffffffffu;
-        if (partial) {
-          kmask_lo = (tk[0] < n_valid ? 0x0000ffffu : 0u) | (tk[1] < n_valid ? 0xffff0000u : 0u);
-          kmask_hi = (tk[2] < n_valid ? 0x0000ffffu : 0u) | (tk[3] < n_valid ? 0xffff0000u : 0u);
-        }
-#pragma unroll
-        for (int mt = 0; mt < C::QSTEPS; ++mt) {
-          uint32_t af[4];
-          // matrices: (tok 0-7, chunk 2mt), (tok 0-7, chunk 2mt+1), (tok 8-15, 2mt), (tok 8-15, 2mt+1)
-          ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * mt + (mi & 1)), af[0], af[1], af[2], af[3]);
-          af[0] &= kmask_lo; af[1] &= kmask_lo; af[2] &= kmask_hi; af[3] &= kmask_hi;
-#pragma unroll
-          for (int n = 0; n < C::NPV; ++n) mma16816<C::VBF>(o[mt][n], af, bf[n][0], bf[n][1]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-    if (warp == 0 && tile + C::NS < n_tiles) {
-      // refill the stage once every warp has released it; lane 0 issues the copies
-      if (!mbar_wait_warp(bar_empty + 8 * s, (tile / C::NS) & 1)) {
+  if constexpr (C::LEAN) {
+    // ---------------------------------------------------------- lean tile loop
+    // Warps of at most 4 heads (one 8-column MMA carries hi and lo parts of P).  Against
+    // the general loop below: the stage index and phase advance incrementally; a slice
+    // whose 16 tokens are all valid (every slice but a sequence's last) skips all
+    // masking; the QK seeds stay in registers; and the V-scaled P of each head is formed
+    // once per (token, block): lane (r, i) with r < 4 forms the hi and lo parts of tokens
+    // 2i, 2i + 1 and its partner lane (r + 4, i) those of tokens 2i + 8, 2i + 9, and one
+    // shuffle gives each its missing half (the hi lane needs the partner's hi, the lo
+    // lane the partner's lo).
+    const int mi = lane >> 3, mr = lane & 7;
+    const bool hi_lane = r < 4;
+    const int tp = hi_lane ? 2 * i4 : 2 * i4 + 8;   // this lane's two P tokens
+    int s = 0;
+    uint32_t ph = 0u;
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      if (!mbar_wait_warp(bar_full + 8 * s, ph)) {
         timed_out = true;
         break;
       }
-      const int page = page_of(tile + C::NS);
-      if (lane == 0) issue_tile(tile + C::NS, page);
+      const int pos_w = (vchunk + tile * nvc) * kT + t0;
+      const int n_valid = stage_ok[s] != 0 ? max(0, min(16, L - pos_w)) : 0;
+      if (n_valid > 0) {
+        const bool causal = T > 1 && pos_w + 16 > L - T + 1;
+        const bool slow = n_valid < 16 || causal;   // warp-uniform
+        const uint32_t st = sring + s * C::STAGE;
+        const uint32_t kst = st, vst = st + C::V_OFF;
+        const uint8_t* ksc = ring + s * C::STAGE + C::KSC_OFF;
+        const uint8_t* vsc = ring + s * C::STAGE + C::VSC_OFF;
+
+        // ---------------- QK^T: S[tok r / r+8][heads 2i, 2i+1] (log2 units after scaling)
+        float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (C::KQ) {
+          float dk[2][C::NB];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            uint32_t w[C::NB / 2];
+            load_scale_words<C::NB>(ksc, t0 + r + 8 * rr, w);
+#pragma unroll
+            for (int k = 0; k < C::NB / 2; ++k) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+              dk[rr][2 * k] = f.x;
+              dk[rr][2 * k + 1] = f.y;
+            }
+          }
+          if constexpr (KC == KVQ_CODEC_Q8_0) {
+#pragma unroll
+            for (int bb = 0; bb < C::NB; ++bb) {
+              uint32_t x0, x1, x2, x3;
+              ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * bb + (mi >> 1)), x0, x1, x2, x3);
+              x0 ^= 0x80808080u; x1 ^= 0x80808080u; x2 ^= 0x80808080u; x3 ^= 0x80808080u;
+              float cb[4] = {kbr[bb].x, kbr[bb].y, kbr[bb].x, kbr[bb].y};
+              uint32_t af[4];
+              af[0] = i8pair_raw(x0, 0x4140); af[1] = i8pair_raw(x1, 0x4140);
+              af[2] = i8pair_raw(x0, 0x4342); af[3] = i8pair_raw(x1, 0x4342);
+              mma16816<false>(cb, af, qf[2 * bb][0], qf[2 * bb][1]);
+              af[0] = i8pair_raw(x2, 0x4140); af[1] = i8pair_raw(x3, 0x4140);
+              af[2] = i8pair_raw(x2, 0x4342); af[3] = i8pair_raw(x3, 0x4342);
+              mma16816<false>(cb, af, qf[2 * bb + 1][0], qf[2 * bb + 1][1]);
+              sc[0] = fmaf(dk[0][bb], cb[0], sc[0]);
+              sc[1] = fmaf(dk[0][bb], cb[1], sc[1]);
+              sc[2] = fmaf(dk[1][bb], cb[2], sc[2]);
+              sc[3] = fmaf(dk[1][bb], cb[3], sc[3]);
+            }
+          } else {  // q4s: one ldmatrix.x4 covers two blocks
+#pragma unroll
+            for (int bb = 0; bb < C::NB; bb += 2) {
+              uint32_t x[4];
+              ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), x[0], x[1], x[2], x[3]);
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t ra = x[2 * h2], rb = x[2 * h2 + 1];  // rows r and r+8 of block bb+h2
+                float cb[4] = {kbr[bb + h2].x, kbr[bb + h2].y, kbr[bb + h2].x, kbr[bb + h2].y};
+                uint32_t af[4];
+                af[0] = u4pair_half(ra << 6); af[1] = u4pair_half(rb << 6);
+                af[2] = u4pair_half(ra << 2); af[3] = u4pair_half(rb << 2);
+                mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
+                af[0] = u4pair_half(ra >> 2); af[1] = u4pair_half(rb >> 2);
+                af[2] = u4pair_half(ra >> 6); af[3] = u4pair_half(rb >> 6);
+                mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
+                sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
+                sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);
+                sc[2] = fmaf(dk[1][bb + h2], cb[2], sc[2]);
+                sc[3] = fmaf(dk[1][bb + h2], cb[3], sc[3]);
+              }
+            }
+          }
+        } else {  // 16-bit K: natural k order, one ldmatrix.x4 per k16 step
+#pragma unroll
+          for (int ks = 0; ks < C::QSTEPS; ++ks) {
+            uint32_t af[4];
+            ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), af[0], af[1], af[2], af[3]);
+            mma16816<C::KBF>(sc, af, qf[ks][0], qf[ks][1]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[k] *= qk_mul;
+        if (slow) {
+          if (r >= n_valid) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+          if (r + 8 >= n_valid) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+          if (causal) {
+            // virtual head v = head * T + i sees the positions below L - T + 1 + i
+            const int cA = 2 * i4, cB = 2 * i4 + 1;
+            const int vA = cA & 3, vB = cB & 3;
+            const int limA = L - T + 1 + vA % T, limB = L - T + 1 + vB % T;
+            if (pos_w + r >= limA) sc[0] = -INFINITY;
+            if (pos_w + r >= limB) sc[1] = -INFINITY;
+            if (pos_w + r + 8 >= limA) sc[2] = -INFINITY;
+            if (pos_w + r + 8 >= limB) sc[3] = -INFINITY;
+          }
+        }
+
+        // ---------------- V scales of this lane's two P tokens (all blocks), their bound
+        uint32_t dw[C::VQ ? C::NB : 1];   // tokens tp (words 0..NB/2-1) and tp+1 (the rest)
+        int ex_lane = 0;   // every scale of this lane's tokens is < 2^ex_lane
+        if constexpr (C::VQ) {
+          const uint8_t* p2 = vsc + (t0 + tp) * C::NB * 2;
+          if constexpr (C::NB == 4) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p2);
+            dw[0] = v.x; dw[1] = v.y; dw[2] = v.z; dw[3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(p2);
+            dw[0] = v.x; dw[1] = v.y;
+          }
+          if (slow) {
+#pragma unroll
+            for (int k = 0; k < C::NB; ++k)
+              if (tp + (2 * k >= C::NB ? 1 : 0) >= n_valid) dw[k] = 0u;
+          }
+          uint32_t mx = dw[0];
+#pragma unroll
+          for (int k = 1; k < C::NB; ++k) mx = __vmaxu2(mx, dw[k]);
+          const uint32_t hmax = max(mx & 0xffffu, mx >> 16);   // scales are >= 0: bits order as values
+          const int e = (int)(hmax >> 10);
+          ex_lane = hmax ? max(e, 1) - 14 : -127;
+        }
+
+        // ---------------- lazy online softmax over the warp's 16 tokens (columns = heads)
+        const float lm0 = fmaxf(sc[0], sc[2]), lm1 = fmaxf(sc[1], sc[3]);
+        const bool over = (lm0 > m0 + kLazy) || (lm1 > m1 + kLazy) || (ex_lane > E);
+        if (__any_sync(0xffffffffu, over)) {
+          float mx0 = lm0, mx1 = lm1;
+          int ex = ex_lane;
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          // the scale bound over all 16 tokens: lanes 0..15 hold tokens 0..7, 16..31 tokens 8..15
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, off));
+          const int E_new = max(E, ex);
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float e2 = __uint_as_float((uint32_t)(127 + E - E_new) << 23);  // 2^(E - E_new)
+          float f0 = (mn0 == -INFINITY) ? 1.0f : fast_exp2(m0 - mn0);
+          float f1 = (mn1 == -INFINITY) ? 1.0f : fast_exp2(m1 - mn1);
+          l0 *= f0;
+          l1 *= f1;
+          f0 *= e2;
+          f1 *= e2;
+#pragma unroll
+          for (int mt = 0; mt < C::QSTEPS; ++mt) {
+            o[mt][0][0] *= f0; o[mt][0][1] *= f1; o[mt][0][2] *= f0; o[mt][0][3] *= f1;
+          }
+          m0 = mn0;
+          m1 = mn1;
+          E = E_new;
+        }
+        // m0, m1 are finite here unless a causal limit masked a column everywhere so far
+        float p0 = fast_exp2(sc[0] - m0);
+        float p1 = fast_exp2(sc[1] - m1);
+        float p2 = fast_exp2(sc[2] - m0);
+        float p3 = fast_exp2(sc[3] - m1);
+        if (causal) {
+          if (sc[0] == -INFINITY) p0 = 0.0f;
+          if (sc[1] == -INFINITY) p1 = 0.0f;
+          if (sc[2] == -INFINITY) p2 = 0.0f;
+          if (sc[3] == -INFINITY) p3 = 0.0f;
+        }
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+
+        // ---------------- transpose p to the PV B layout (fp32 as two 16-bit halves):
+        // lane (r, i) receives p[tok 2i, 2i+1, 2i+8, 2i+9][column r] and keeps its pair
+        float pa, pb;
+        {
+          const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+          const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
+          const uint32_t ah = movtrans(__byte_perm(u0, u1, 0x7632)), al = movtrans(__byte_perm(u0, u1, 0x5410));
+          const uint32_t bh = movtrans(__byte_perm(u2, u3, 0x7632)), bl = movtrans(__byte_perm(u2, u3, 0x5410));
+          const uint32_t xl = hi_lane ? al : bl, xh = hi_lane ? ah : bh;
+          pa = __uint_as_float(__byte_perm(xl, xh, 0x5410));
+          pb = __uint_as_float(__byte_perm(xl, xh, 0x7632));
+        }
+        const float pscale = __uint_as_float((uint32_t)(127 + kPScale - E) << 23);  // 2^(kPScale - E)
+        pa *= pscale;
+        pb *= pscale;
+        // (hi, lo) parts of (x0, x1) for this lane's tokens -> the B registers of its column
+        auto b_regs = [&](float x0, float x1, uint32_t& b0, uint32_t& b1) {
+          const uint32_t hi = pack2<C::VBF>(x0, x1);
+          float y0, y1;
+          add_k_times<C::VBF>(hi, C::VBF ? 0xBF80 : 0xBC00, x0, x1, y0, y1);
+          const uint32_t lo = pack2<C::VBF>(y0, y1);
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi_lane ? lo : hi, 16);
+          b0 = hi_lane ? hi : recv;
+          b1 = hi_lane ? recv : lo;
+        };
+
+        // ---------------- PV
+        if constexpr (C::VQ) {
+          uint32_t vq4[4];   // q4s: one ldmatrix.x4 covers blocks bb and bb + 1 (bb even)
+#pragma unroll
+          for (int bb = 0; bb < C::NB; ++bb) {
+            const uint32_t wa = dw[bb >> 1], wb = dw[C::NB / 2 + (bb >> 1)];
+            const float da = __half2float(__ushort_as_half((unsigned short)(wa >> (16 * (bb & 1)))));
+            const float db = __half2float(__ushort_as_half((unsigned short)(wb >> (16 * (bb & 1)))));
+            uint32_t b0, b1;
+            b_regs(pa * da, pb * db, b0, b1);
+            if constexpr (VC == KVQ_CODEC_Q8_0) {
+              uint32_t y0, y1, y2, y3;
+              // matrices: (tok 0-7, chunk 2b), (tok 0-7, chunk 2b+1), (tok 8-15, 2b), (tok 8-15, 2b+1)
+              ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * bb + (mi & 1)), y0, y1, y2, y3);
+              y0 ^= 0x80808080u; y1 ^= 0x80808080u; y2 ^= 0x80808080u; y3 ^= 0x80808080u;
+              uint32_t ae[4] = {i8pair_raw(y0, 0x4240), i8pair_raw(y1, 0x4240), i8pair_raw(y2, 0x4240),
+                                i8pair_raw(y3, 0x4240)};
+              uint32_t ao[4] = {i8pair_raw(y0, 0x4341), i8pair_raw(y1, 0x4341), i8pair_raw(y2, 0x4341),
+                                i8pair_raw(y3, 0x4341)};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                ae[k] = hsub2_u32(ae[k], 0x64806480u);
+                ao[k] = hsub2_u32(ao[k], 0x64806480u);
+              }
+              mma16816<false>(o[2 * bb][0], ae, b0, b1);
+              mma16816<false>(o[2 * bb + 1][0], ao, b0, b1);
+            } else {  // q4s: matrices (tok 0-7, chunk b), (tok 8-15, chunk b) for this block
+              if ((bb & 1) == 0)
+                ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), vq4[0], vq4[1], vq4[2], vq4[3]);
+              const uint32_t ya = (bb & 1) ? vq4[2] : vq4[0], yb = (bb & 1) ? vq4[3] : vq4[1];
+              const uint32_t ya8 = ya >> 8, yb8 = yb >> 8;
+              const uint32_t a01[4] = {hsub2_u32(u4pair_raw(ya), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(ya), kSixteenth2, kMinus72x2),
+                                       hsub2_u32(u4pair_raw(yb), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(yb), kSixteenth2, kMinus72x2)};
+              const uint32_t a23[4] = {hsub2_u32(u4pair_raw(ya8), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(ya8), kSixteenth2, kMinus72x2),
+                                       hsub2_u32(u4pair_raw(yb8), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(yb8), kSixteenth2, kMinus72x2)};
+              mma16816<false>(o[2 * bb][0], a01, b0, b1);
+              mma16816<false>(o[2 * bb + 1][0], a23, b0, b1);
+            }
+          }
+        } else {
+          // 16-bit V: one B operand for every M-tile; in a partial slice zero the A lanes of
+          // tokens past the end (their rows may hold anything)
+          uint32_t b0, b1;
+          b_regs(pa, pb, b0, b1);
+          uint32_t kmask_lo = 0xffffffffu, kmask_hi = 0xffffffffu;
+          if (slow) {
+            kmask_lo = (2 * i4 < n_valid ? 0x0000ffffu : 0u) | (2 * i4 + 1 < n_valid ? 0xffff0000u : 0u);
+            kmask_hi = (2 * i4 + 8 < n_valid ? 0x0000ffffu : 0u) | (2 * i4 + 9 < n_valid ? 0xffff0000u : 0u);
+          }
+#pragma unroll
+          for (int mt = 0; mt < C::QSTEPS; ++mt) {
+            uint32_t af[4];
+            ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * mt + (mi & 1)), af[0], af[1], af[2], af[3]);
+            if (slow) { af[0] &= kmask_lo; af[1] &= kmask_lo; af[2] &= kmask_hi; af[3] &= kmask_hi; }
+            mma16816<C::VBF>(o[mt][0], af, b0, b1);
+          }
+        }
+      }
       __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+      if (pw == 0 && tile + C::NS < n_tiles) {
+        // refill the stage once every warp has released it; lane 0 issues the copies
+        if (!mbar_wait_warp(bar_empty + 8 * s, ph)) {
+          timed_out = true;
+          break;
+        }
+        const int page = page_of(tile + C::NS);
+        if (lane == 0) issue_tile(tile + C::NS, page);
+        __syncwarp();
+      }
+      if (++s == C::NS) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  } else {
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      const int s = tile % C::NS;
+      if (!mbar_wait_warp(bar_full + 8 * s, (tile / C::NS) & 1)) {
+        timed_out = true;
+        break;
+      }
+      const int pos_w = (vchunk + tile * nvc) * kT + t0;
+      const bool tile_ok = stage_ok[s] != 0;
+      const int n_valid = tile_ok ? max(0, min(16, L - pos_w)) : 0;
+      if (n_valid > 0) {
+        const bool partial = n_valid < 16;
+        const uint32_t st = sring + s * C::STAGE;
+        const uint32_t kst = st, vst = st + C::V_OFF;
+        const uint8_t* ksc = ring + s * C::STAGE + C::KSC_OFF;
+        const uint8_t* vsc = ring + s * C::STAGE + C::VSC_OFF;
+        const int mi = lane >> 3, mr = lane & 7;
+
+        // ---------------- QK^T: S[tok r / r+8][heads 2i, 2i+1] (log2 units after scaling)
+        float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (C::KQ) {
+          // block scales of rows r and r+8
+          float dk[2][C::NB];
+  #pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            uint32_t w[C::NB / 2];
+            load_scale_words<C::NB>(ksc, t0 + r + 8 * rr, w);
+  #pragma unroll
+            for (int k = 0; k < C::NB / 2; ++k) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+              dk[rr][2 * k] = f.x;
+              dk[rr][2 * k + 1] = f.y;
+            }
+          }
+          if constexpr (KC == KVQ_CODEC_Q8_0) {
+  #pragma unroll
+            for (int bb = 0; bb < C::NB; ++bb) {
+              uint32_t x0, x1, x2, x3;
+              ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * bb + (mi >> 1)), x0, x1, x2, x3);
+              x0 ^= 0x80808080u; x1 ^= 0x80808080u; x2 ^= 0x80808080u; x3 ^= 0x80808080u;
+              // accumulator seeded with -1152 * sum(q) of the block: removes the code offset
+              const float2 kb = kbs[(hg * C::NB + bb) * 4 + i4];
+              float cb[4] = {kb.x, kb.y, kb.x, kb.y};
+              uint32_t af[4];
+              af[0] = i8pair_raw(x0, 0x4140); af[1] = i8pair_raw(x1, 0x4140);
+              af[2] = i8pair_raw(x0, 0x4342); af[3] = i8pair_raw(x1, 0x4342);
+              mma16816<false>(cb, af, qf[2 * bb][0], qf[2 * bb][1]);
+              af[0] = i8pair_raw(x2, 0x4140); af[1] = i8pair_raw(x3, 0x4140);
+              af[2] = i8pair_raw(x2, 0x4342); af[3] = i8pair_raw(x3, 0x4342);
+              mma16816<false>(cb, af, qf[2 * bb + 1][0], qf[2 * bb + 1][1]);
+              sc[0] = fmaf(dk[0][bb], cb[0], sc[0]);
+              sc[1] = fmaf(dk[0][bb], cb[1], sc[1]);
+              sc[2] = fmaf(dk[1][bb], cb[2], sc[2]);
+              sc[3] = fmaf(dk[1][bb], cb[3], sc[3]);
+            }
+          } else {  // q4s: one ldmatrix.x4 covers two blocks
+  #pragma unroll
+            for (int bb = 0; bb < C::NB; bb += 2) {
+              uint32_t x[4];
+              ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), x[0], x[1], x[2], x[3]);
+  #pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t ra = x[2 * h2], rb = x[2 * h2 + 1];  // rows r and r+8 of block bb+h2
+                const float2 kb = kbs[(hg * C::NB + bb + h2) * 4 + i4];
+                float cb[4] = {kb.x, kb.y, kb.x, kb.y};
+                uint32_t af[4];
+                af[0] = u4pair_half(ra << 6); af[1] = u4pair_half(rb << 6);
+                af[2] = u4pair_half(ra << 2); af[3] = u4pair_half(rb << 2);
+                mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
+                af[0] = u4pair_half(ra >> 2); af[1] = u4pair_half(rb >> 2);
+                af[2] = u4pair_half(ra >> 6); af[3] = u4pair_half(rb >> 6);
+                mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
+                sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
+                sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);
+                sc[2] = fmaf(dk[1][bb + h2], cb[2], sc[2]);
+                sc[3] = fmaf(dk[1][bb + h2], cb[3], sc[3]);
+              }
+            }
+          }
+        } else {  // 16-bit K: natural k order, one ldmatrix.x4 per k16 step
+  #pragma unroll
+          for (int ks = 0; ks < C::QSTEPS; ++ks) {
+            uint32_t af[4];
+            ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi & 1) * 8 + mr, 2 * ks + (mi >> 1)), af[0], af[1], af[2], af[3]);
+            mma16816<C::KBF>(sc, af, qf[ks][0], qf[ks][1]);
+          }
+        }
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) sc[k] *= qk_mul;
+        if (partial) {
+          if (r >= n_valid) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
+          if (r + 8 >= n_valid) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+        }
+        if (T > 1 && pos_w + 16 > L - T + 1) {
+          // causal limit of the query tokens (virtual head v = head * T + i sees the positions
+          // below L - T + 1 + i): only the sequence's last T - 1 positions are masked
+          const int cA = 2 * i4, cB = 2 * i4 + 1;   // this lane's QK columns
+          const int vA = hg * GW + (GW <= 4 ? (cA & 3) : cA), vB = hg * GW + (GW <= 4 ? (cB & 3) : cB);
+          const int limA = L - T + 1 + vA % T, limB = L - T + 1 + vB % T;
+          if (pos_w + r >= limA) sc[0] = -INFINITY;
+          if (pos_w + r >= limB) sc[1] = -INFINITY;
+          if (pos_w + r + 8 >= limA) sc[2] = -INFINITY;
+          if (pos_w + r + 8 >= limB) sc[3] = -INFINITY;
+        }
+
+        // ---------------- V scales of this lane's PV tokens (2i, 2i+1, 2i+8, 2i+9)
+        const int tk[4] = {2 * i4, 2 * i4 + 1, 2 * i4 + 8, 2 * i4 + 9};
+        uint32_t dvw[4][C::NB / 2 > 0 ? C::NB / 2 : 1];
+        int ex_lane = 0;   // every scale of this lane's tokens is < 2^ex_lane
+        if constexpr (C::VQ) {
+          uint32_t mx = 0;
+  #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            load_scale_words<C::NB>(vsc, t0 + tk[u], dvw[u]);
+            if (partial && tk[u] >= n_valid) {
+  #pragma unroll
+              for (int k = 0; k < C::NB / 2; ++k) dvw[u][k] = 0u;
+            }
+  #pragma unroll
+            for (int k = 0; k < C::NB / 2; ++k) mx = __vmaxu2(mx, dvw[u][k]);
+          }
+          const uint32_t hmax = max(mx & 0xffffu, mx >> 16);   // scales are >= 0: bits order as values
+          const int e = (int)(hmax >> 10);
+          ex_lane = hmax ? max(e, 1) - 14 : -127;
+        }
+
+        // ---------------- lazy online softmax over the warp's 16 tokens (columns = heads)
+        const float lm0 = fmaxf(sc[0], sc[2]), lm1 = fmaxf(sc[1], sc[3]);
+        const bool over = (lm0 > m0 + kLazy) || (lm1 > m1 + kLazy) || (ex_lane > E);
+        if (__any_sync(0xffffffffu, over)) {
+          float mx0 = lm0, mx1 = lm1;
+          int ex = ex_lane;
+  #pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, 1));
+          ex = max(ex, __shfl_xor_sync(0xffffffffu, ex, 2));
+          const int E_new = max(E, ex);
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float e2 = __uint_as_float((uint32_t)(127 + E - E_new) << 23);  // 2^(E - E_new)
+          float f0 = (mn0 == -INFINITY) ? 1.0f : fast_exp2(m0 - mn0);
+          float f1 = (mn1 == -INFINITY) ? 1.0f : fast_exp2(m1 - mn1);
+          l0 *= f0;
+          l1 *= f1;
+          f0 *= e2;
+          f1 *= e2;
+  #pragma unroll
+          for (int mt = 0; mt < C::QSTEPS; ++mt)
+  #pragma unroll
+            for (int n = 0; n < C::NPV; ++n) {
+              o[mt][n][0] *= f0; o[mt][n][1] *= f1; o[mt][n][2] *= f0; o[mt][n][3] *= f1;
+            }
+          m0 = mn0;
+          m1 = mn1;
+          E = E_new;
+        }
+        // m0, m1 are finite here unless a causal limit masked a column everywhere so far: the
+        // warp has a valid token, whose score raised them
+        float p0 = fast_exp2(sc[0] - m0);
+        float p1 = fast_exp2(sc[1] - m1);
+        float p2 = fast_exp2(sc[2] - m0);
+        float p3 = fast_exp2(sc[3] - m1);
+        if (T > 1) {
+          if (sc[0] == -INFINITY) p0 = 0.0f;
+          if (sc[1] == -INFINITY) p1 = 0.0f;
+          if (sc[2] == -INFINITY) p2 = 0.0f;
+          if (sc[3] == -INFINITY) p3 = 0.0f;
+        }
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+
+        // ---------------- transpose p (fp32, as two 16-bit halves) to the PV B layout:
+        // lane (r, i) receives p[tok 2i, 2i+1, 2i+8, 2i+9][column r]
+        float pv[4];
+        {
+          const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+          const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
+          const uint32_t ah = movtrans(__byte_perm(u0, u1, 0x7632)), al = movtrans(__byte_perm(u0, u1, 0x5410));
+          const uint32_t bh = movtrans(__byte_perm(u2, u3, 0x7632)), bl = movtrans(__byte_perm(u2, u3, 0x5410));
+          pv[0] = __uint_as_float(__byte_perm(al, ah, 0x5410));
+          pv[1] = __uint_as_float(__byte_perm(al, ah, 0x7632));
+          pv[2] = __uint_as_float(__byte_perm(bl, bh, 0x5410));
+          pv[3] = __uint_as_float(__byte_perm(bl, bh, 0x7632));
+        }
+
+        // ---------------- PV
+        const float pscale = __uint_as_float((uint32_t)(127 + kPScale - E) << 23);  // 2^(kPScale - E)
+  #pragma unroll
+        for (int u = 0; u < 4; ++u) pv[u] *= pscale;
+        // PV column r of an 8-column tile is head r&3's hi part (r < 4) or lo part (r >= 4)
+        // when one n-tile carries both; lo lanes feed x - f16(x) instead of x.
+        const unsigned short lo_sel = (C::NPV == 1 && r >= 4) ? (C::VBF ? 0xBF80 : 0xBC00) : 0;
+        if constexpr (C::VQ) {
+          uint32_t vq4[4];   // q4s: one ldmatrix.x4 covers blocks bb and bb + 1 (bb even)
+  #pragma unroll
+          for (int bb = 0; bb < C::NB; ++bb) {
+            float x[4];
+  #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const __half hv = __ushort_as_half((unsigned short)(dvw[u][bb >> 1] >> (16 * (bb & 1))));
+              x[u] = pv[u] * __half2float(hv);
+            }
+            uint32_t bf[C::NPV][2];
+            if constexpr (C::NPV == 1) {
+              bf[0][0] = hi_or_lo<C::VBF>(x[0], x[1], lo_sel);
+              bf[0][1] = hi_or_lo<C::VBF>(x[2], x[3], lo_sel);
+            } else {
+              split2<C::VBF>(x[0], x[1], bf[0][0], bf[1][0]);
+              split2<C::VBF>(x[2], x[3], bf[0][1], bf[1][1]);
+            }
+            if constexpr (VC == KVQ_CODEC_Q8_0) {
+              uint32_t y0, y1, y2, y3;
+              // matrices: (tok 0-7, chunk 2b), (tok 0-7, chunk 2b+1), (tok 8-15, 2b), (tok 8-15, 2b+1)
+              ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * bb + (mi & 1)), y0, y1, y2, y3);
+              y0 ^= 0x80808080u; y1 ^= 0x80808080u; y2 ^= 0x80808080u; y3 ^= 0x80808080u;
+              uint32_t ae[4] = {i8pair_raw(y0, 0x4240), i8pair_raw(y1, 0x4240), i8pair_raw(y2, 0x4240),
+                                i8pair_raw(y3, 0x4240)};
+              uint32_t ao[4] = {i8pair_raw(y0, 0x4341), i8pair_raw(y1, 0x4341), i8pair_raw(y2, 0x4341),
+                                i8pair_raw(y3, 0x4341)};
+              // exact small integers in f16 before the product: an offset folded into the fp32
+              // accumulator instead loses its low bits there, and that error grows with the chunk
+  #pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                ae[k] = hsub2_u32(ae[k], 0x64806480u);
+                ao[k] = hsub2_u32(ao[k], 0x64806480u);
+              }
+  #pragma unroll
+              for (int n = 0; n < C::NPV; ++n) {
+                mma16816<false>(o[2 * bb][n], ae, bf[n][0], bf[n][1]);
+                mma16816<false>(o[2 * bb + 1][n], ao, bf[n][0], bf[n][1]);
+              }
+            } else {  // q4s: matrices (tok 0-7, chunk b), (tok 8-15, chunk b) for this block
+              if ((bb & 1) == 0)
+                ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi & 1) * 8 + mr, bb + (mi >> 1)), vq4[0], vq4[1], vq4[2], vq4[3]);
+              const uint32_t ya = (bb & 1) ? vq4[2] : vq4[0], yb = (bb & 1) ? vq4[3] : vq4[1];
+              const uint32_t ya8 = ya >> 8, yb8 = yb >> 8;
+              // even nibbles: 1024 + u, less 1032; odd nibbles in place: (1024 + 16 u) / 16 - 72
+              const uint32_t a01[4] = {hsub2_u32(u4pair_raw(ya), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(ya), kSixteenth2, kMinus72x2),
+                                       hsub2_u32(u4pair_raw(yb), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(yb), kSixteenth2, kMinus72x2)};
+              const uint32_t a23[4] = {hsub2_u32(u4pair_raw(ya8), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(ya8), kSixteenth2, kMinus72x2),
+                                       hsub2_u32(u4pair_raw(yb8), 0x64086408u),
+                                       hfma2_u32(u4pair_hi_raw(yb8), kSixteenth2, kMinus72x2)};
+  #pragma unroll
+              for (int n = 0; n < C::NPV; ++n) {
+                mma16816<false>(o[2 * bb][n], a01, bf[n][0], bf[n][1]);
+                mma16816<false>(o[2 * bb + 1][n], a23, bf[n][0], bf[n][1]);
+              }
+            }
+          }
+        } else {
+          // 16-bit V: one B operand for every M-tile; zero the A lanes of tokens past the end
+          uint32_t bf[C::NPV][2];
+          if constexpr (C::NPV == 1) {
+            bf[0][0] = hi_or_lo<C::VBF>(pv[0], pv[1], lo_sel);
+            bf[0][1] = hi_or_lo<C::VBF>(pv[2], pv[3], lo_sel);
+          } else {
+            split2<C::VBF>(pv[0], pv[1], bf[0][0], bf[1][0]);
+            split2<C::VBF>(pv[2], pv[3], bf[0][1], bf[1][1]);
+          }
+          uint32_t kmask_lo = 0xffffffffu, kmask_hi = 0xffffffffu;
+          if (partial) {
+            kmask_lo = (tk[0] < n_valid ? 0x0000ffffu : 0u) | (tk[1] < n_valid ? 0xffff0000u : 0u);
+            kmask_hi = (tk[2] < n_valid ? 0x0000ffffu : 0u) | (tk[3] < n_valid ? 0xffff0000u : 0u);
+          }
+  #pragma unroll
+          for (int mt = 0; mt < C::QSTEPS; ++mt) {
+            uint32_t af[4];
+            // matrices: (tok 0-7, chunk 2mt), (tok 0-7, chunk 2mt+1), (tok 8-15, 2mt), (tok 8-15, 2mt+1)
+            ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * mt + (mi & 1)), af[0], af[1], af[2], af[3]);
+            af[0] &= kmask_lo; af[1] &= kmask_lo; af[2] &= kmask_hi; af[3] &= kmask_hi;
+  #pragma unroll
+            for (int n = 0; n < C::NPV; ++n) mma16816<C::VBF>(o[mt][n], af, bf[n][0], bf[n][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+      if (pw == 0 && tile + C::NS < n_tiles) {
+        // refill the stage once every warp has released it; lane 0 issues the copies
+        if (!mbar_wait_warp(bar_empty + 8 * s, (tile / C::NS) & 1)) {
+          timed_out = true;
+          break;
+        }
+        const int page = page_of(tile + C::NS);
+        if (lane == 0) issue_tile(tile + C::NS, page);
+        __syncwarp();
+      }
     }
   }
-
   // ------------------------------------------------------------ merge the warps
-  unsigned seq_ticket = 0u;
-  if (adv && nv == 1 && tid == 0) seq_ticket = seq_arrive(a.seq_counters + b);   // the only CTA
-
   const int NWT = C::NW * 32;
   if (timed_out) record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
-  // every warp reaches the barriers below (a timed-out warp skips only its tiles)
-  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
   // per-head sums of the lanes' partials; O true scale: O * 2^(E - kPScale)
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
@@ -951,97 +1334,198 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
   }
   const float oscale = __uint_as_float((uint32_t)(127 + E - kPScale) << 23);
-  float* ml = ml_all + warp * 16;
-  if (r == 0) {
-    ml[(2 * i4) * 2] = m0;
-    ml[(2 * i4) * 2 + 1] = l0;
-    ml[(2 * i4 + 1) * 2] = m1;
-    ml[(2 * i4 + 1) * 2 + 1] = l1;
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
-  float* obuf = reinterpret_cast<float*>(smem);  // the ring is idle now
-  {
-    // heads of this lane's O columns after folding: 2*i4, 2*i4+1 (lanes i4 < GW/2 only)
-    const int hA = 2 * i4, hB = 2 * i4 + 1;
-    float fA = 0.0f, fB = 0.0f;
-    {
-      float MA = -INFINITY, MB = -INFINITY;
-      const int wg0 = hg * 4;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        MA = fmaxf(MA, ml_all[(wg0 + w) * 16 + (hA & 7) * 2]);
-        MB = fmaxf(MB, ml_all[(wg0 + w) * 16 + (hB & 7) * 2]);
-      }
-      const float mA = __shfl_sync(0xffffffffu, m0, (lane & ~3) | (i4 & (GW <= 4 ? 1 : 3)));
-      const float mB = __shfl_sync(0xffffffffu, m1, (lane & ~3) | (i4 & (GW <= 4 ? 1 : 3)));
-      fA = (mA == -INFINITY) ? 0.0f : fast_exp2(mA - MA) * oscale;
-      fB = (mB == -INFINITY) ? 0.0f : fast_exp2(mB - MB) * oscale;
-    }
+  const long long head0 = (long long)b * a.num_q_heads + (long long)kvh * G;
+  const int gcount = G < GW * HG ? G : GW * HG;
+  if (C::LEAN && a.warp_records > 0) {
+    // ---- record mode: this warp's partial, in register order (one float2 per lane and
+    // M-tile: lanes i < 2 rows r, lanes i >= 2 rows r + 8 after adding the lo columns),
+    // and its (m, l) per head; the record merge kernel combines the records
+    const long long rec = ((long long)b * gridDim.y + kvh) * a.warp_records + (long long)chunk * C::NW + warp;
+    if (r == 0 && i4 < 2) reinterpret_cast<float4*>(a.part_ml + rec * 8)[i4] = make_float4(m0, l0, m1, l1);
+    float2* ro = reinterpret_cast<float2*>(a.part_o + rec * (C::QSTEPS * 64)) + lane;
 #pragma unroll
     for (int mt = 0; mt < C::QSTEPS; ++mt) {
       float v[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float x = o[mt][0][k];
-        if constexpr (C::NPV == 2) x += o[mt][1][k];
-        else x += __shfl_xor_sync(0xffffffffu, x, 2);  // add the lo columns (lanes i4 ^ 2)
-        v[k] = x;
-      }
-      if (GW > 4 || i4 < 2) {
-        const int d0 = pv_dim<VC>(mt, r), d1 = pv_dim<VC>(mt, r + 8);
-        obuf[(warp * 8 + hA) * D + d0] = v[0] * fA;
-        obuf[(warp * 8 + hB) * D + d0] = v[1] * fB;
-        obuf[(warp * 8 + hA) * D + d1] = v[2] * fA;
-        obuf[(warp * 8 + hB) * D + d1] = v[3] * fB;
+      for (int k = 0; k < 4; ++k) v[k] = o[mt][0][k] + __shfl_xor_sync(0xffffffffu, o[mt][0][k], 2);
+      ro[mt * 32] = i4 < 2 ? make_float2(v[0] * oscale, v[1] * oscale) : make_float2(v[2] * oscale, v[3] * oscale);
+    }
+    return;
+  }
+  if constexpr (C::NPV == 1 && HG == 1 && C::NW <= 16) {
+    // ---- warps of at most 4 heads: every warp's accumulators have the same lane layout
+    // (lane (r, i) holds rows r, r + 8 of each M-tile for columns 2i, 2i + 1, i.e. heads
+    // 2(i & 1), 2(i & 1) + 1, hi parts for i < 2 and lo parts for i >= 2), so the warps
+    // are summed position by position: each warp stores its scaled values in register
+    // order (one float2 per lane and M-tile, no bank conflicts) and thread t adds up
+    // position t of every warp.
+    float* hml = ml_all + C::NW * 16;        // per-head (M, l) of the whole CTA [4][2]
+    float* obuf = reinterpret_cast<float*>(smem);
+    if (r == 0) *reinterpret_cast<float4*>(ml_all + warp * 16 + i4 * 4) = make_float4(m0, l0, m1, l1);
+    // every warp reaches this barrier (a timed-out warp skips only its tiles); after it
+    // all loops are done, so the rings are idle
+    asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+    // (M, l) of heads 2hp, 2hp + 1 over the CTA's warps: lane (hp, w) reads warp w's pair
+    const int hp = lane >> 4, wr = lane & 15;
+    const float4 mlw = wr < C::NW ? *reinterpret_cast<const float4*>(ml_all + wr * 16 + hp * 4)
+                                  : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+    float Ma = mlw.x, Mb = mlw.z;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) {
+      Ma = fmaxf(Ma, __shfl_xor_sync(0xffffffffu, Ma, off));
+      Mb = fmaxf(Mb, __shfl_xor_sync(0xffffffffu, Mb, off));
+    }
+    float la = mlw.x == -INFINITY ? 0.0f : fast_exp2(mlw.x - Ma) * mlw.y;
+    float lb = mlw.z == -INFINITY ? 0.0f : fast_exp2(mlw.z - Mb) * mlw.w;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) {
+      la += __shfl_xor_sync(0xffffffffu, la, off);
+      lb += __shfl_xor_sync(0xffffffffu, lb, off);
+    }
+    if (warp == 0 && wr == 0) *reinterpret_cast<float4*>(hml + hp * 4) = make_float4(Ma, la, Mb, lb);
+    {
+      const int src = (i4 & 1) * 16;          // the lane holding this lane's head pair
+      const float MA = __shfl_sync(0xffffffffu, Ma, src), MB = __shfl_sync(0xffffffffu, Mb, src);
+      const float mA = __shfl_sync(0xffffffffu, m0, (lane & ~3) | (i4 & 1));
+      const float mB = __shfl_sync(0xffffffffu, m1, (lane & ~3) | (i4 & 1));
+      const float fA = (mA == -INFINITY) ? 0.0f : fast_exp2(mA - MA) * oscale;
+      const float fB = (mB == -INFINITY) ? 0.0f : fast_exp2(mB - MB) * oscale;
+#pragma unroll
+      for (int mt = 0; mt < C::QSTEPS; ++mt) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = o[mt][0][k] + __shfl_xor_sync(0xffffffffu, o[mt][0][k], 2);
+        // lanes i < 2 keep rows r (d0), lanes i >= 2 rows r + 8 (d1)
+        const float2 w2 = i4 < 2 ? make_float2(v[0] * fA, v[1] * fB) : make_float2(v[2] * fA, v[3] * fB);
+        *reinterpret_cast<float2*>(obuf + (warp * C::QSTEPS + mt) * 64 + lane * 2) = w2;
       }
     }
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
-  const long long head0 = (long long)b * a.num_q_heads + (long long)kvh * G;
-  const int gcount = G < GW * HG ? G : GW * HG;
-  // per-head (M, l) of the whole CTA
-  float* hml = ml_all + C::NW * 16;     // [16][2]
-  for (int h = tid; h < gcount; h += NWT) {
-    const int hgi = h / GW, hl = h % GW;
-    float M = -INFINITY;
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, ml_all[(hgi * 4 + w) * 16 + hl * 2]);
-    float lsum = 0.0f;
-    for (int w = 0; w < 4; ++w) {
-      const float mw = ml_all[(hgi * 4 + w) * 16 + hl * 2];
-      if (mw != -INFINITY) lsum += fast_exp2(mw - M) * ml_all[(hgi * 4 + w) * 16 + hl * 2 + 1];
+    asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+    // position t = (M-tile, lane, k) -> (head, element of head_dim)
+    for (int t = tid; t < C::QSTEPS * 64; t += NWT) {
+      const int mt = t >> 6, ln = (t >> 1) & 31, k = t & 1;
+      const int rr = ln >> 2, ii = ln & 3;
+      const int dim = pv_dim<VC>(mt, ii < 2 ? rr : rr + 8);
+      const int h = 2 * (ii & 1) + k;
+      if (h >= gcount) continue;
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < C::NW; ++w) sum += obuf[(w * C::QSTEPS + mt) * 64 + (t & 63)];
+      if (nv == 1) {
+        // the whole sequence is this chunk: normalize and write the output (no split)
+        const float lsum = hml[2 * h + 1];
+        a.out[(head0 + h) * D + dim] = lsum > 0.0f ? sum / lsum : 0.0f;
+      } else {
+        a.part_o[((head0 + h) * a.n_chunks + chunk) * D + dim] = sum;   // partial write (a7)
+      }
     }
-    hml[2 * h] = M;
-    hml[2 * h + 1] = lsum;
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
-  if (nv == 1) {
-    // the whole sequence is this chunk: normalize and write the output (no split)
+    if (nv == 1) {
+      return;
+    }
+    if (tid < gcount) {
+      a.part_ml[((head0 + tid) * a.n_chunks + chunk) * 2] = hml[2 * tid];
+      a.part_ml[((head0 + tid) * a.n_chunks + chunk) * 2 + 1] = hml[2 * tid + 1];
+    }
+  } else {
+    float* ml = ml_all + warp * 16;   // its own region (not part of the rings)
+    if (r == 0) {
+      ml[(2 * i4) * 2] = m0;
+      ml[(2 * i4) * 2 + 1] = l0;
+      ml[(2 * i4 + 1) * 2] = m1;
+      ml[(2 * i4 + 1) * 2 + 1] = l1;
+    }
+    // every warp reaches this barrier (a timed-out warp skips only its tiles); after it all
+    // loops are done, so the rings are idle
+    asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+    float* obuf = reinterpret_cast<float*>(smem);
+    // warp index of member w of head group hgi in pipeline pp
+    auto wix = [&](int pp, int hgi, int w) { return pp * C::PW + hgi * 4 + w; };
+    float* hml = ml_all + C::NW * 16;     // per-head (M, l) of the whole CTA [16][2]
+    if (warp == 0 && lane < gcount) {
+      const int h = lane, hgi = h / GW, hl = h % GW;
+      float M = -INFINITY;
+      for (int pp = 0; pp < C::NP; ++pp)
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, ml_all[wix(pp, hgi, w) * 16 + hl * 2]);
+      float lsum = 0.0f;
+      for (int pp = 0; pp < C::NP; ++pp)
+        for (int w = 0; w < 4; ++w) {
+          const float mw = ml_all[wix(pp, hgi, w) * 16 + hl * 2];
+          if (mw != -INFINITY) lsum += fast_exp2(mw - M) * ml_all[wix(pp, hgi, w) * 16 + hl * 2 + 1];
+        }
+      hml[2 * h] = M;
+      hml[2 * h + 1] = lsum;
+    }
+    {
+      // heads of this lane's O columns after folding: 2*i4, 2*i4+1 (lanes i4 < GW/2 only)
+      const int hA = 2 * i4, hB = 2 * i4 + 1;
+      float fA = 0.0f, fB = 0.0f;
+      {
+        // over the warps of this head group in every pipeline
+        float MA = -INFINITY, MB = -INFINITY;
+  #pragma unroll
+        for (int pp = 0; pp < C::NP; ++pp)
+  #pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int wi = wix(pp, hg, w);
+            MA = fmaxf(MA, ml_all[wi * 16 + (hA & 7) * 2]);
+            MB = fmaxf(MB, ml_all[wi * 16 + (hB & 7) * 2]);
+          }
+        const float mA = __shfl_sync(0xffffffffu, m0, (lane & ~3) | (i4 & (GW <= 4 ? 1 : 3)));
+        const float mB = __shfl_sync(0xffffffffu, m1, (lane & ~3) | (i4 & (GW <= 4 ? 1 : 3)));
+        fA = (mA == -INFINITY) ? 0.0f : fast_exp2(mA - MA) * oscale;
+        fB = (mB == -INFINITY) ? 0.0f : fast_exp2(mB - MB) * oscale;
+      }
+  #pragma unroll
+      for (int mt = 0; mt < C::QSTEPS; ++mt) {
+        float v[4];
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float x = o[mt][0][k];
+          if constexpr (C::NPV == 2) x += o[mt][1][k];
+          else x += __shfl_xor_sync(0xffffffffu, x, 2);  // add the lo columns (lanes i4 ^ 2)
+          v[k] = x;
+        }
+        if (GW > 4 || i4 < 2) {
+          const int d0 = pv_dim<VC>(mt, r), d1 = pv_dim<VC>(mt, r + 8);
+          obuf[(warp * 8 + hA) * D + d0] = v[0] * fA;
+          obuf[(warp * 8 + hB) * D + d0] = v[1] * fB;
+          obuf[(warp * 8 + hA) * D + d1] = v[2] * fA;
+          obuf[(warp * 8 + hB) * D + d1] = v[3] * fB;
+        }
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
+    if (nv == 1) {
+      // the whole sequence is this chunk: normalize and write the output (no split)
+      for (int idx = tid; idx < gcount * D; idx += NWT) {
+        const int h = idx / D, j = idx % D;
+        const int hgi = h / GW, hl = h % GW;
+        float sum = 0.0f;
+  #pragma unroll
+        for (int pp = 0; pp < C::NP; ++pp)
+  #pragma unroll
+          for (int w = 0; w < 4; ++w) sum += obuf[(wix(pp, hgi, w) * 8 + hl) * D + j];
+        const float lsum = hml[2 * h + 1];
+        a.out[(head0 + h) * D + j] = lsum > 0.0f ? sum / lsum : 0.0f;
+      }
+      return;
+    }
+    // ------------------------------------------------------------ partial write (a7)
     for (int idx = tid; idx < gcount * D; idx += NWT) {
       const int h = idx / D, j = idx % D;
       const int hgi = h / GW, hl = h % GW;
       float sum = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
-      const float lsum = hml[2 * h + 1];
-      a.out[(head0 + h) * D + j] = lsum > 0.0f ? sum / lsum : 0.0f;
+  #pragma unroll
+      for (int pp = 0; pp < C::NP; ++pp)
+  #pragma unroll
+        for (int w = 0; w < 4; ++w) sum += obuf[(wix(pp, hgi, w) * 8 + hl) * D + j];
+      a.part_o[((head0 + h) * a.n_chunks + chunk) * D + j] = sum;
     }
-    if (adv && tid == 0) seq_finish(seq_ticket);
-    return;
+    for (int h = tid; h < gcount; h += NWT) {
+      a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2] = hml[2 * h];
+      a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2 + 1] = hml[2 * h + 1];
+    }
   }
-  // ------------------------------------------------------------ partial write (a7)
-  for (int idx = tid; idx < gcount * D; idx += NWT) {
-    const int h = idx / D, j = idx % D;
-    const int hgi = h / GW, hl = h % GW;
-    float sum = 0.0f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) sum += obuf[((hgi * 4 + w) * 8 + hl) * D + j];
-    a.part_o[((head0 + h) * a.n_chunks + chunk) * D + j] = sum;
-  }
-  for (int h = tid; h < gcount; h += NWT) {
-    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2] = hml[2 * h];
-    a.part_ml[((head0 + h) * a.n_chunks + chunk) * 2 + 1] = hml[2 * h + 1];
-  }
-
   // ------------------------------------------------------------ split-K combine (a8)
   // Two levels, both done by whichever CTA arrives last (atomic counters in the
   // workspace, returned to zero by that CTA):
@@ -1055,32 +1539,27 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   const int g = chunk / gsz;
   const int g_first = g * gsz;
   const int g_count = min(gsz, nv - g_first);
-  volatile int* last_flag = stage_ok + 4;
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OK_OFF) + 16;
   if (!arrive_last(a.counters + a.grp_counter_off + unit * a.n_groups + g, g_count, tid, NWT, last_flag,
                    a.k.status))
     return;
-  if (adv && ng == 1 && tid == 0) seq_ticket = seq_arrive(a.seq_counters + b);   // finishes the unit
   // merge this group's chunk partials
   merge_partials<D, C::NW>(
       a.part_ml + (head0 * a.n_chunks + g_first) * 2, a.part_o + (head0 * a.n_chunks + g_first) * D,
       (long long)a.n_chunks, g_count, gcount, ng == 1,
       a.gpart_ml + (head0 * a.n_groups + g) * 2, a.gpart_o + (head0 * a.n_groups + g) * D,
-      (long long)a.n_groups, a.out + head0 * D);
+      (long long)a.n_groups, a.out + head0 * D, reinterpret_cast<float*>(smem));
   if (tid == 0) a.counters[a.grp_counter_off + unit * a.n_groups + g] = 0u;
   if (ng == 1) {
-    if (adv && tid == 0) seq_finish(seq_ticket);
     return;
   }
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");   // group partial written before arriving
   if (!arrive_last(a.counters + unit, ng, tid, NWT, last_flag, a.k.status)) return;
-  if (adv && tid == 0) seq_ticket = seq_arrive(a.seq_counters + b);   // finishes the unit
   // the group partials were written by other CTAs before their arrivals
   merge_partials<D, C::NW>(a.gpart_ml + head0 * a.n_groups * 2, a.gpart_o + head0 * a.n_groups * D,
-                           (long long)a.n_groups, ng, gcount, true, nullptr, nullptr, 0, a.out + head0 * D);
-  if (tid == 0) {
-    a.counters[unit] = 0u;
-    if (adv) seq_finish(seq_ticket);
-  }
+                           (long long)a.n_groups, ng, gcount, true, nullptr, nullptr, 0, a.out + head0 * D,
+                           reinterpret_cast<float*>(smem));
+  if (tid == 0) a.counters[unit] = 0u;
 }
 
 template <int KC, int VC, int D, int GW, int HG>
@@ -1119,11 +1598,12 @@ cudaError_t launch(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMa
   return e;
 }
 
-// Resident CTAs per SM of one instantiation (0 on error).
+// Resident CTAs per SM of one instantiation (0 on error); *pipes = its pipelines per CTA.
 template <int KC, int VC, int D, int GW, int HG>
-int occupancy() {
+int occupancy(int* pipes) {
   using C = Cfg<KC, VC, D, GW, HG>;
   auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
+  *pipes = C::NP;
   if (prepare<KC, VC, D, GW, HG>() != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM) != cudaSuccess) return 0;
@@ -1131,11 +1611,11 @@ int occupancy() {
 }
 
 template <int KC, int VC>
-int occupancy_pair(int head_dim, int g) {
+int occupancy_pair(int head_dim, int g, int* pipes) {
 #define KVQ_MMA_O(D)                                         \
-  if (g <= 4) return occupancy<KC, VC, D, 4, 1>();           \
-  if (g <= 8) return occupancy<KC, VC, D, 8, 1>();           \
-  if (g <= 16) return occupancy<KC, VC, D, 8, 2>();          \
+  if (g <= 4) return occupancy<KC, VC, D, 4, 1>(pipes);      \
+  if (g <= 8) return occupancy<KC, VC, D, 8, 1>(pipes);      \
+  if (g <= 16) return occupancy<KC, VC, D, 8, 2>(pipes);     \
   return 0;
   switch (head_dim) {
     case 64: { KVQ_MMA_O(64) }

@@ -97,6 +97,13 @@ struct DecodeArgs {
   const __nv_bfloat16* v_new;
   int32_t* seq_lens_adv;
   unsigned* seq_counters;
+  // Record mode (warps of at most 4 heads, D <= 128): with warp_records > 0 the decode
+  // kernel merges nothing; every warp writes its own partial as record
+  // (chunk * pipes + pipe) * 4 + slice of its (sequence, KV head) unit:
+  //   part_ml [unit][record][8]: (m, l) of heads 0, 1, 2, 3 (base-2 max, sum)
+  //   part_o  [unit][record][D * 4]: unnormalized O in the accumulator's register order
+  // and the record merge kernel (launched right after it) forms the output.
+  int warp_records;
 };
 
 // Arguments of the prefill attention kernel (kvq_prefill.cuh).
@@ -143,6 +150,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 cudaError_t launch_combine_pdl(const DecodeArgs& a, int head_dim, cudaStream_t stream);
+cudaError_t launch_record_merge_pdl(const DecodeArgs& a, int head_dim, int v_codec, cudaStream_t stream);
 
 void count_launch();
 kvq_status decode_workspace_layout(const kvq_store* k_store, const kvq_store* v_store, int batch,

@@ -110,18 +110,27 @@ typedef struct kvq_decode_opts {
 typedef struct kvq_store kvq_store;  /* opaque handle: host metadata + a device status word */
 
 /* Bytes of device memory a store with this shape needs (num_pages * num_kv_heads *
- * page_size * (row_bytes + 2*head_dim/32 for quantized codecs)).  Pure host call. */
+ * page_size * (row_bytes + 2*head_dim/32 for quantized codecs)).  Pure host call.
+ * Source: the resident packed store of rMLX issue #295 ("Fix direction": keep the prefix
+ * on the device across decode steps and read the quant store directly).  The pages give
+ * no API for it; sizing, wrapping caller memory and releasing the handle is the plainest
+ * lifecycle that lets the caller (torch) own every byte of device memory. */
 kvq_status kvq_store_bytes(const kvq_store_desc* desc, size_t* bytes);
 
 /* Wrap caller-owned device memory `buf` (at least kvq_store_bytes bytes, 256-byte
- * aligned) as a store.  The buffer's previous contents are kept; rows that were never
- * appended hold whatever the buffer held.  Allocates the handle on the host and a
- * 4-byte status word on the current device.  `*out` is valid until kvq_destroy. */
+ * aligned) as a store (the resident store of rMLX issue #295, "Fix direction").  The
+ * buffer's previous contents are kept; rows that were never appended hold whatever the
+ * buffer held.  Allocates the handle on the host and a 4-byte status word on the current
+ * device.  `*out` is valid until kvq_destroy.  Errors: KVQ_ERR_INVALID_ARG for a bad
+ * descriptor or a null, unaligned or too small buffer; KVQ_ERR_CUDA when the status word
+ * cannot be allocated or cleared (nothing is kept, *out stays NULL). */
 kvq_status kvq_store_create(const kvq_store_desc* desc, void* buf, size_t buf_bytes,
                             kvq_store** out);
 
-/* Free the handle and its status word.  Does not touch `buf`.  The caller must make
- * sure no enqueued work still uses the store.  NULL is accepted. */
+/* Free the handle and its status word (end of the resident store's life, rMLX issue
+ * #295 "Fix direction").  Does not touch `buf`.  The caller must make sure no enqueued
+ * work still uses the store.  NULL is accepted.  KVQ_ERR_CUDA if cudaFree fails (the
+ * host handle is freed regardless). */
 kvq_status kvq_destroy(kvq_store* store);
 
 /* Encode new rows into the store, on the device (a1: on-device encode of new K/V rows;
@@ -144,7 +153,11 @@ kvq_status kvq_append_kv(kvq_store* k_store, kvq_store* v_store, const void* k_r
                          const void* v_rows, int n_new, int batch, int32_t* seq_lens,
                          const int32_t* page_table, int max_pages, int advance, void* stream);
 
-/* seq_lens[b] += n for b < batch, on the device (after the K and the V append). */
+/* seq_lens[b] += n for b < batch, on the device (after the K and the V append).  Source:
+ * rMLX issue #295 ("Fix direction": no per-step host restage), so the lengths that
+ * locate the new rows advance on the device too, in stream order, without a host round
+ * trip.  seq_lens: device int32 [batch], caller-owned.  KVQ_ERR_INVALID_ARG for a null
+ * pointer or batch < 1; KVQ_ERR_CUDA for a failed launch. */
 kvq_status kvq_seq_lens_add(int32_t* seq_lens, int batch, int n, void* stream);
 
 /* Separate dequantize pass (the comparison arm of halobench record clm-0022, METHOD and
@@ -169,7 +182,11 @@ kvq_status kvq_read_probe(const void* buf, size_t bytes, void* sink, void* strea
 
 /* Device workspace bytes a kvq_flash_decode (or kvq_flash_decode_append) call with the
  * same stores, batch, head count, max_len_hint and options needs (the split depends on
- * both stores' codecs).  The workspace holds the split-K partials and, at its end,
+ * both stores' codecs).  Source: the split-K form of the flash-decode-over-quant kernel
+ * class (rMLX issue #292, "Root cause" and its correction): each chunk of the KV length
+ * leaves a partial (running max m, sum l, accumulator) that the combine step merges,
+ * and those partials live here.  Pure host call; KVQ_ERR_INVALID_ARG for null pointers,
+ * batch or head counts < 1, a negative hint or heads not divisible by num_kv_heads.  The workspace holds the split-K partials and, at its end,
  * arrival counters: per (sequence, KV head), per group of chunks, and per sequence. */
 kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store* v_store,
                                       int batch, int num_q_heads, int max_len_hint,
@@ -183,7 +200,10 @@ kvq_status kvq_decode_workspace_bytes(const kvq_store* k_store, const kvq_store*
 kvq_status kvq_pointer_kind(const void* p, int32_t* kind);
 
 /* Zero a decode workspace (its arrival counters must be zero before its first use;
- * every completed kvq_flash_decode leaves them zero again).  Enqueued on `stream`. */
+ * every completed kvq_flash_decode leaves them zero again).  Enqueued on `stream`.
+ * Source: the split-K partials of rMLX issue #292 (see kvq_decode_workspace_bytes); the
+ * counters are how the last CTA of a split finds out it is last.  workspace: device
+ * memory, caller-owned.  KVQ_ERR_INVALID_ARG for a null pointer or zero size. */
 kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Split-K flash-decode over the quantized store (a2..a8):
@@ -296,14 +316,17 @@ kvq_status kvq_flash_decode_static_ws(const void* q, const kvq_store* k_store,
 
 /* Wait for the device, read and clear the store's status word.  *device_code receives
  * the first recorded fault (KVQ_DEVICE_*), or 0.  Returns KVQ_ERR_DEVICE_FAULT when a
- * fault was recorded, KVQ_OK otherwise.  The only call that synchronizes. */
+ * fault was recorded, KVQ_OK otherwise.  The only call that synchronizes.  The pages have
+ * no counterpart: it is how kernels that never trap report bad device data. */
 kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code);
 
 /* Number of decode/append/combine kernels this library has launched in this process
- * (a dispatch counter for benchmarks and tests). */
+ * (a dispatch counter for benchmarks and tests: the pages prove their kernels ran by
+ * counting dispatches, rMLX issue #295 "Finding" table and rMLX issue #292 "Symptom"). */
 uint64_t kvq_launch_count(void);
 
-/* Static string naming a status code. */
+/* Static string naming a status code (plumbing; the pages have no counterpart).  Never
+ * NULL: unknown codes give "KVQ_UNKNOWN_STATUS". */
 const char* kvq_status_string(kvq_status status);
 
 #ifdef __cplusplus

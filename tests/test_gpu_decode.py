@@ -162,12 +162,15 @@ def test_workspace_counters_return_to_zero():
 
 
 def test_dirty_workspace_is_reported():
-    inp = make_inputs([3000], 8, 2, 128, seed=22)
+    # 16 query heads on 2 KV heads (8 per KV head): the
+    # kernel merges the split in place with arrival counters, so counters that are not zero
+    # at the start are reported
+    inp = make_inputs([3000], 16, 2, 128, seed=22)
     k = kvq()
     ks = build_store(inp, "q8_0", "k")
     vs = build_store(inp, "q8_0", "v")
     q, sl, pt = device_inputs(inp)
-    need = k.kvq_decode_workspace_bytes(ks, vs, 1, 8, 3000, chunk_tokens=256)
+    need = k.kvq_decode_workspace_bytes(ks, vs, 1, 16, 3000, chunk_tokens=256)
     ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
     k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=3000, workspace=ws, chunk_tokens=256)
     assert k.kvq_store_get_error(ks) == 5
@@ -175,6 +178,24 @@ def test_dirty_workspace_is_reported():
     out = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=3000, workspace=ws, chunk_tokens=256)
     assert k.kvq_store_get_error(ks) == 0
     assert_close(out.cpu().numpy(), oracle_out(inp, "q8_0", "q8_0"), "after re-init")
+
+
+def test_dirty_workspace_record_mode_keeps_no_state():
+    # at most 4 query heads per KV head: every warp rewrites its record on every call and
+    # a separate kernel merges them, so a workspace full of garbage gives the same output
+    inp = make_inputs([3000], 8, 2, 128, seed=22)
+    k = kvq()
+    ks = build_store(inp, "q8_0", "k")
+    vs = build_store(inp, "q8_0", "v")
+    q, sl, pt = device_inputs(inp)
+    need = k.kvq_decode_workspace_bytes(ks, vs, 1, 8, 3000, chunk_tokens=256)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    dirty = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=3000, workspace=ws, chunk_tokens=256)
+    assert k.kvq_store_get_error(ks) == 0
+    ws.zero_()
+    clean = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=3000, workspace=ws, chunk_tokens=256)
+    assert torch.equal(dirty, clean)
+    assert_close(clean.cpu().numpy(), oracle_out(inp, "q8_0", "q8_0"), "record mode")
 
 
 @pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q8_0", "q4s")])

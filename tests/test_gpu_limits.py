@@ -38,16 +38,27 @@ def test_largest_head_dim_and_group_at_the_largest_page(kc, vc):
     assert_close(decode(inp, kc, vc), oracle_out(inp, kc, vc), f"D256 G16 P1024 {kc}/{vc}")
 
 
-def test_many_chunks_two_level_merge():
-    # 64-token chunks over 16384 tokens: 256 partials per (sequence, KV head), merged in 16
-    # groups and then across the groups
-    inp = make_inputs([16384], 32, 8, 128, seed=71)
+@pytest.mark.parametrize("hkv", [8, 4])
+def test_many_chunks_two_level_merge(hkv):
+    # 64-token chunks over 16384 tokens: 256 partials per (sequence, KV head).  With 4 query
+    # heads per KV head they are 4096 per-warp records for the merge kernel; with 8 the
+    # kernel merges them in place, in 16 groups and then across the groups
+    inp = make_inputs([16384], 32, hkv, 128, seed=71)
     got = decode(inp, "q8_0", "q8_0", chunk_tokens=64)
     want = oracle_out(inp, "q8_0", "q8_0", heads=[0, 5, 13, 31])
-    assert_close(got, want, "256 chunks")
+    assert_close(got, want, f"256 chunks, {32 // hkv} heads per KV head")
     # the default split and the 64-token split agree to rounding
     ref = decode(inp, "q8_0", "q8_0")
     assert np.max(np.abs(got - ref)) < 1e-4
+
+
+def test_in_place_merge_beyond_the_record_limit():
+    # 64-token chunks over 65536 tokens at 4 query heads per KV head: 16384 per-warp records
+    # would exceed the record limit, so the kernel merges in place (1024 partials, 64 groups)
+    inp = make_inputs([65536], 8, 2, 128, seed=73)
+    got = decode(inp, "q8_0", "q8_0", chunk_tokens=64)
+    want = oracle_out(inp, "q8_0", "q8_0", heads=[0, 3, 6])
+    assert_close(got, want, "1024 chunks in place")
 
 
 def test_more_units_than_resident_ctas_and_single_token_sequences():
