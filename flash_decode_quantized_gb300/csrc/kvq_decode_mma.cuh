@@ -291,7 +291,9 @@ struct Cfg {
   static constexpr int OK_OFF = BAR_OFF + NP * 2 * NS * 8;  // [NP][NS] "tile is valid" flags, then a flag
   static constexpr int KB_OFF = OK_OFF + 128;             // QK accumulator seeds [HG][NB][4] f32x2
   static constexpr int ML_OFF = KB_OFF + HG * NB * 4 * 8; // per-warp m, l [NW][8][2]
-  static constexpr int SMEM = ML_OFF + (NW + 2) * 16 * 4 + 1024;  // + per-head (M, l); +1024: alignment
+  static constexpr int PG_OFF = ML_OFF + (NW + 2) * 16 * 4;   // + per-head (M, l); then [NP][64] page ids
+  static constexpr int RC_OFF = PG_OFF + NP * 64 * 4;     // [NP][NS] releases counted per stage
+  static constexpr int SMEM = RC_OFF + 16 * 4 + 1024;     // +1024: alignment
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
   static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
@@ -589,6 +591,15 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       mbar_init(bar_empty + 8 * s, C::PW);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // lean loop: the page ids of the pipeline's first 64 tiles and the release counters live
+  // in shared memory, where whichever warp refills a stage finds them
+  int* const pgs = reinterpret_cast<int*>(smem + C::PG_OFF) + pipe * 64;
+  unsigned* const rcnt = reinterpret_cast<unsigned*>(smem + C::RC_OFF) + pipe * C::NS;
+  if (C::LEAN && pw == 0) {
+    pgs[lane] = pg_lo;
+    pgs[32 + lane] = pg_hi;
+    if (lane < C::NS) rcnt[lane] = 0u;
   }
   __syncthreads();   // also: every thread has read seq_lens
 
@@ -1014,15 +1025,24 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-      if (pw == 0 && tile + C::NS < n_tiles) {
-        // refill the stage once every warp has released it; lane 0 issues the copies
-        if (!mbar_wait_warp(bar_empty + 8 * s, ph)) {
+      // Release the stage; the warp that releases it last (counted in shared memory)
+      // refills it at once, so that no warp waits for the others and a stage is never
+      // left empty while its refiller finishes other work.
+      uint32_t last = 0u;
+      if (lane == 0) {
+        mbar_arrive(bar_empty + 8 * s);
+        last = atomicAdd(rcnt + s, 1u) == (unsigned)(C::PW - 1) ? 1u : 0u;
+        if (last) atomicExch(rcnt + s, 0u);
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last && tile + C::NS < n_tiles) {
+        if (!mbar_wait_warp(bar_empty + 8 * s, ph)) {   // every release is in: no wait
           timed_out = true;
           break;
         }
-        const int page = page_of(tile + C::NS);
-        if (lane == 0) issue_tile(tile + C::NS, page);
+        const int t2 = tile + C::NS;
+        const int page = t2 < 64 ? pgs[t2] : load_page(t2);
+        if (lane == 0) issue_tile(t2, page);
         __syncwarp();
       }
       if (++s == C::NS) {
