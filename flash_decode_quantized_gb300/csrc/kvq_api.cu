@@ -16,6 +16,14 @@ namespace kvq {
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::atomic<int> g_wait_limit{0};   // 0: the default limit
+static std::atomic<int> g_skip_tile{-1};
+void fault_injection(int* wait_limit, int* skip_tile) {
+  const int w = g_wait_limit.load(std::memory_order_relaxed);
+  *wait_limit = w > 0 ? w : (1 << 22);   // the kernels' default wait limit
+  *skip_tile = g_skip_tile.load(std::memory_order_relaxed);
+}
+
 cudaError_t simt_launch_bf16_bf16(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_f16_f16(const DecodeArgs&, int, cudaStream_t);
 cudaError_t simt_launch_q8_0_bf16(const DecodeArgs&, int, cudaStream_t);
@@ -398,12 +406,15 @@ namespace kvq {
 namespace {
 
 // kvq_flash_decode, and with k_new set the fused append step (kvq_flash_decode_append).
+// With reset_counters the workspace's counters are zeroed on the stream right before the
+// launch, after every check has passed (the fixed-array entry point's workspace keeps the
+// previous call's contents).
 kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, const kvq_store* k_store,
                        const kvq_store* v_store, const int32_t* seq_lens, int32_t* seq_lens_adv,
                        const int32_t* page_table, int max_pages, kvq_codec codec, float* out,
                        int batch, int num_q_heads, int tokens, float softmax_scale, int max_len_hint,
                        const kvq_decode_opts* opts, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+                       void* stream, bool reset_counters = false) {
   if (!q || !k_store || !v_store || !seq_lens || !page_table || !out || !workspace)
     return KVQ_ERR_INVALID_ARG;
   if (batch < 1 || num_q_heads < 1 || tokens < 1 || max_pages < 1 || max_len_hint < 0)
@@ -464,7 +475,10 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
   a.seq_lens_adv = seq_lens_adv;
   a.seq_counters = reinterpret_cast<unsigned*>(ws + p.seq_cnt_off);
   a.warp_records = p.records;
+  fault_injection(&a.wait_limit, &a.skip_tile);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (reset_counters && cudaMemsetAsync(ws + p.cnt_off, 0, p.total - p.cnt_off, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
   if (p.variant == 2) {
     // the tensor-core kernel merges the split itself (last CTA per unit), or in record
     // mode leaves per-warp records for the merge kernel launched right after it
@@ -478,6 +492,16 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
 }
 
 }  // namespace
+
+kvq_status decode_reset(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                        const int32_t* seq_lens, const int32_t* page_table, int max_pages, kvq_codec codec,
+                        float* out, int batch, int num_q_heads, float softmax_scale, int max_len_hint,
+                        const kvq_decode_opts* opts, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, nullptr, nullptr, k_store, v_store, seq_lens, nullptr, page_table, max_pages, codec,
+                     out, batch, num_q_heads, 1, softmax_scale, max_len_hint, opts, workspace, workspace_bytes,
+                     stream, true);
+}
+
 }  // namespace kvq
 
 extern "C" {
@@ -577,6 +601,13 @@ kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code) {
 }
 
 uint64_t kvq_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+kvq_status kvq_set_fault_injection(int32_t wait_limit, int32_t skip_tile) {
+  if (wait_limit < 0 || skip_tile < -1) return KVQ_ERR_INVALID_ARG;
+  kvq::g_wait_limit.store(wait_limit, std::memory_order_relaxed);
+  kvq::g_skip_tile.store(skip_tile, std::memory_order_relaxed);
+  return KVQ_OK;
+}
 
 const char* kvq_status_string(kvq_status status) {
   switch (status) {

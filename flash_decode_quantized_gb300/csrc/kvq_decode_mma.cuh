@@ -77,8 +77,8 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait, by every lane of a warp, for the phase of parity `parity` to complete.
 // Each lane observes the completion itself (acquire); the result is warp-uniform, so
 // the warp leaves together.  False on timeout.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
-  for (int it = 0; it < kTimeoutIters; ++it)
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int limit = kTimeoutIters) {
+  for (int it = 0; it < limit; ++it)
     if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   return false;
 }
@@ -293,7 +293,8 @@ struct Cfg {
   static constexpr int ML_OFF = KB_OFF + HG * NB * 4 * 8; // per-warp m, l [NW][8][2]
   static constexpr int PG_OFF = ML_OFF + (NW + 2) * 16 * 4;   // + per-head (M, l); then [NP][64] page ids
   static constexpr int RC_OFF = PG_OFF + NP * 64 * 4;     // [NP][NS] releases counted per stage
-  static constexpr int SMEM = RC_OFF + 16 * 4 + 1024;     // +1024: alignment
+  static constexpr int LI_OFF = RC_OFF + 16 * 4;          // [NP][NS] last tile issued into each stage
+  static constexpr int SMEM = LI_OFF + 16 * 4 + 1024;     // +1024: alignment
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
   static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
@@ -596,6 +597,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // in shared memory, where whichever warp refills a stage finds them
   int* const pgs = reinterpret_cast<int*>(smem + C::PG_OFF) + pipe * 64;
   unsigned* const rcnt = reinterpret_cast<unsigned*>(smem + C::RC_OFF) + pipe * C::NS;
+  volatile int* const last_issued = reinterpret_cast<volatile int*>(smem + C::LI_OFF) + pipe * C::NS;
+  if (pw == 0 && lane < C::NS) last_issued[lane] = -1;
   if (C::LEAN && pw == 0) {
     pgs[lane] = pg_lo;
     pgs[32 + lane] = pg_hi;
@@ -609,6 +612,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // tile k.
   auto issue_tile = [&](int tile, int page) {
     const int s = tile % C::NS;
+    // fault injection (tests of the timeout path): the first pipeline never issues this
+    // tile, neither its copies nor an arrival, so its consumers' bounded waits run out on a
+    // stage with nothing in flight
+    if (vchunk == 0 && tile == a.skip_tile) return;
+    last_issued[s] = tile;
     const int pos0 = (vchunk + tile * nvc) * kT;
     const int row0 = pos0 % P;
     const uint32_t full = bar_full + 8 * s;
@@ -753,6 +761,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   const float qk_mul = a.qk_scale_log2 * (KC == KVQ_CODEC_Q4S ? 2.0f : 1.0f);
   int E = -100;                                                 // running V-scale exponent bound
   bool timed_out = false;
+  const int wlim = a.wait_limit;   // tries of mbarrier.try_wait before a wait gives up
 
   if constexpr (C::LEAN) {
     // ---------------------------------------------------------- lean tile loop
@@ -770,7 +779,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     int s = 0;
     uint32_t ph = 0u;
     for (int tile = 0; tile < n_tiles; ++tile) {
-      if (!mbar_wait_warp(bar_full + 8 * s, ph)) {
+      if (!mbar_wait_warp(bar_full + 8 * s, ph, wlim)) {
         timed_out = true;
         break;
       }
@@ -1036,7 +1045,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last && tile + C::NS < n_tiles) {
-        if (!mbar_wait_warp(bar_empty + 8 * s, ph)) {   // every release is in: no wait
+        if (!mbar_wait_warp(bar_empty + 8 * s, ph, wlim)) {   // every release is in: no wait
           timed_out = true;
           break;
         }
@@ -1053,7 +1062,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   } else {
     for (int tile = 0; tile < n_tiles; ++tile) {
       const int s = tile % C::NS;
-      if (!mbar_wait_warp(bar_full + 8 * s, (tile / C::NS) & 1)) {
+      if (!mbar_wait_warp(bar_full + 8 * s, (tile / C::NS) & 1, wlim)) {
         timed_out = true;
         break;
       }
@@ -1334,7 +1343,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
       if (pw == 0 && tile + C::NS < n_tiles) {
         // refill the stage once every warp has released it; lane 0 issues the copies
-        if (!mbar_wait_warp(bar_empty + 8 * s, (tile / C::NS) & 1)) {
+        if (!mbar_wait_warp(bar_empty + 8 * s, (tile / C::NS) & 1, wlim)) {
           timed_out = true;
           break;
         }
@@ -1346,7 +1355,18 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   }
   // ------------------------------------------------------------ merge the warps
   const int NWT = C::NW * 32;
-  if (timed_out) record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
+  if (timed_out) {
+    record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
+    // Leave no bulk copy in flight into this CTA's shared memory: wait for the phase of the
+    // last tile issued into each stage of the pipeline (copies that were issued complete).
+    // A stage never issued has nothing in flight and is not waited on.  Every warp that
+    // issues a copy records it before its own drain, so each copy is drained by its issuer
+    // at least.
+    for (int st = 0; st < C::NS; ++st) {
+      const int t = last_issued[st];
+      if (t >= 0) (void)mbar_wait_warp(bar_full + 8 * st, (t / C::NS) & 1);
+    }
+  }
   // per-head sums of the lanes' partials; O true scale: O * 2^(E - kPScale)
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {

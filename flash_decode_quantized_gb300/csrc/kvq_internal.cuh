@@ -104,6 +104,8 @@ struct DecodeArgs {
   //   part_o  [unit][record][D * 4]: unnormalized O in the accumulator's register order
   // and the record merge kernel (launched right after it) forms the output.
   int warp_records;
+  int wait_limit;              // tries of each bounded mbarrier wait before it gives up
+  int skip_tile;               // fault injection: tile the first pipeline never issues (-1: none)
 };
 
 // Arguments of the prefill attention kernel (kvq_prefill.cuh).
@@ -153,8 +155,17 @@ cudaError_t launch_combine_pdl(const DecodeArgs& a, int head_dim, cudaStream_t s
 cudaError_t launch_record_merge_pdl(const DecodeArgs& a, int head_dim, int v_codec, cudaStream_t stream);
 
 void count_launch();
+// Fault injection for tests of the timeout path (kvq_set_fault_injection): the wait limit
+// and the skipped tile that the next decode launches use.
+void fault_injection(int* wait_limit, int* skip_tile);
 kvq_status decode_workspace_layout(const kvq_store* k_store, const kvq_store* v_store, int batch,
                                    int num_q_heads, int max_len_hint, const kvq_decode_opts* opts,
                                    size_t* total, size_t* counters_off);
+// kvq_flash_decode that zeroes the workspace's counters on the stream right before its
+// launch, once every argument check has passed (nothing is enqueued on a failed check).
+kvq_status decode_reset(const void* q, const kvq_store* k_store, const kvq_store* v_store,
+                        const int32_t* seq_lens, const int32_t* page_table, int max_pages, kvq_codec codec,
+                        float* out, int batch, int num_q_heads, float softmax_scale, int max_len_hint,
+                        const kvq_decode_opts* opts, void* workspace, size_t workspace_bytes, void* stream);
 
 }  // namespace kvq

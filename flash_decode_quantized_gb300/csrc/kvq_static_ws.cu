@@ -48,16 +48,15 @@ extern "C" kvq_status kvq_flash_decode_static_ws(const void* q, const kvq_store*
   size_t need = 0, counters_off = 0;
   kvq_status st = kvq::decode_workspace_layout(k_store, v_store, batch, num_q_heads, max_len_hint, opts,
                                                &need, &counters_off);
+  (void)counters_off;
   if (st != KVQ_OK) return st;
   if (need > kStaticWorkspaceBytes) return KVQ_ERR_WORKSPACE;
   void* ws = nullptr;
   st = static_workspace(&ws);
   if (st != KVQ_OK) return st;
-  // The array keeps the previous call's contents: zero the merge counters this call
-  // relies on (the partials are fully written before they are read).
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(static_cast<unsigned char*>(ws) + counters_off, 0, need - counters_off, s) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  return kvq_flash_decode(q, k_store, v_store, seq_lens, page_table, max_pages, codec, out, batch, num_q_heads,
-                          softmax_scale, max_len_hint, opts, ws, kStaticWorkspaceBytes, stream);
+  // The array keeps the previous call's contents: the merge counters this call relies on
+  // are zeroed on `stream` right before the launch, after every argument check (a rejected
+  // call enqueues nothing); the partials are fully written before they are read.
+  return kvq::decode_reset(q, k_store, v_store, seq_lens, page_table, max_pages, codec, out, batch,
+                           num_q_heads, softmax_scale, max_len_hint, opts, ws, kStaticWorkspaceBytes, stream);
 }

@@ -71,6 +71,7 @@ def _load():
                                    ctypes.POINTER(DecodeOpts), P, Z, V],
         "kvq_flash_decode_append": [P, P, P, P, P, P, P, I, CodecPair, P, I, I, ctypes.c_float, I, I,
                                     ctypes.POINTER(DecodeOpts), P, Z, V],
+        "kvq_set_fault_injection": [ctypes.c_int32, ctypes.c_int32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -436,6 +437,11 @@ def kvq_store_get_error(store: Store) -> int:
 
 def kvq_launch_count() -> int:
     return int(lib.kvq_launch_count())
+
+
+def kvq_set_fault_injection(wait_limit: int, skip_tile: int) -> None:
+    """Test hook for the device-timeout path; (0, -1) restores normal operation."""
+    _check(lib.kvq_set_fault_injection(int(wait_limit), int(skip_tile)), "kvq_set_fault_injection")
 
 
 def kvq_status_string(status: int) -> str:

@@ -304,7 +304,8 @@ kvq_status kvq_flash_decode_append(const void* q, const void* k_new, const void*
  * nothing.  The first call on a device looks up the array's address (set-up, a
  * synchronous runtime query); make that first call before any stream capture.  Every
  * call zeroes the array's merge counters with an asynchronous memset on `stream`
- * (no allocation).  All calls share the one array, so calls that overlap on the device
+ * (no allocation), after every argument check has passed: a call that fails a check
+ * returns its error and enqueues nothing.  All calls share the one array, so calls that overlap on the device
  * (other streams, concurrent graphs) race; serialize them.  Other arguments, results
  * and errors are those of kvq_flash_decode. */
 kvq_status kvq_flash_decode_static_ws(const void* q, const kvq_store* k_store,
@@ -324,6 +325,22 @@ kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code);
  * (a dispatch counter for benchmarks and tests: the pages prove their kernels ran by
  * counting dispatches, rMLX issue #295 "Finding" table and rMLX issue #292 "Symptom"). */
 uint64_t kvq_launch_count(void);
+
+/* Fault injection for tests of the device-timeout path (plumbing; the pages have no
+ * counterpart: bounded waits are how this library's kernels avoid hanging on a stage that
+ * never fills).  Applies to the tensor-core decode launches that follow in this process,
+ * until reset with (0, -1):
+ *   wait_limit  tries of each bounded mbarrier wait before it gives up (0 = the default,
+ *               about four million);
+ *   skip_tile   a tile of the first pipeline of every (sequence, KV head) unit that is
+ *               never issued (neither its copies nor an arrival), or -1 for none.
+ * With a tile skipped, that pipeline's waits run out: the kernel records
+ * KVQ_DEVICE_TIMEOUT in the K store's status word and the call's output is invalid.  No
+ * copy is left in flight (the skipped stage has none; every issued one is waited for
+ * before the CTA exits), so the next call runs normally.  Process-wide, not synchronized
+ * with launches from other threads.  KVQ_ERR_INVALID_ARG for wait_limit < 0 or
+ * skip_tile < -1. */
+kvq_status kvq_set_fault_injection(int32_t wait_limit, int32_t skip_tile);
 
 /* Static string naming a status code (plumbing; the pages have no counterpart).  Never
  * NULL: unknown codes give "KVQ_UNKNOWN_STATUS". */

@@ -77,3 +77,6 @@ def test_null_arguments_rejected_before_any_cuda_call(lib):
     assert L.kvq_store_create(ctypes.byref(d), None, 0, ctypes.byref(h)) == kvq.KVQ_ERR_INVALID_ARG
     assert h.value is None
     assert isinstance(kvq.kvq_launch_count(), int)
+    for bad in [(-1, -1), (0, -2)]:
+        assert L.kvq_set_fault_injection(*bad) == kvq.KVQ_ERR_INVALID_ARG
+    assert L.kvq_set_fault_injection(0, -1) == kvq.KVQ_OK   # the default: no injection

@@ -114,3 +114,32 @@ def test_read_probe_reads_and_leaves_sink():
     assert int(sink.item()) == 0
     with pytest.raises(k.KvqError):
         k.kvq_read_probe(buf[1:17], sink)          # not 16-byte aligned
+
+
+@pytest.mark.parametrize("hq,hkv,d,kc,skip", [
+    (32, 8, 128, "q8_0", 1),     # lean tile loop, per-warp records merged by a second kernel
+    (32, 8, 128, "q4s", 0),      # the very first tile never issued: nothing to drain in that stage
+    (16, 2, 128, "q8_0", 1),     # 8 heads per KV head: generic loop, in-place merge
+    (64, 4, 256, "q8_0", 1),     # GQA 16:1, head dim 256
+])
+def test_device_timeout_is_recorded_and_the_next_call_runs(hq, hkv, d, kc, skip):
+    # A tile that the producer never issues (no copy, no arrival) leaves its consumers waiting
+    # on a stage with nothing in flight; their bounded waits run out, the kernel records
+    # KVQ_DEVICE_TIMEOUT, drains every copy it did issue and exits.  The context stays usable.
+    inp = make_inputs([8000, 1700], hq, hkv, d, seed=43)
+    k = kvq()
+    ks = build_store(inp, kc, "k")
+    vs = build_store(inp, kc, "v")
+    q, sl, pt = device_inputs(inp)
+    want = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=8000, variant=2)
+    assert k.kvq_store_get_error(ks) == 0
+    try:
+        k.kvq_set_fault_injection(4096, skip)
+        k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=8000, variant=2)
+        assert k.kvq_store_get_error(ks) == 4   # KVQ_DEVICE_TIMEOUT
+    finally:
+        k.kvq_set_fault_injection(0, -1)
+    got = k.kvq_flash_decode(q, ks, vs, sl, pt, max_len_hint=8000, variant=2)
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+    assert torch.equal(got, want)
+
