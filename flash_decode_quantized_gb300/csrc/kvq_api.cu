@@ -84,10 +84,10 @@ MmaFn mma_fn(int kc, int vc) {
 // CTA (cached per process).
 int mma_occupancy(int kc, int vc, int head_dim, int group, int* pipes) {
   static std::mutex mu;
-  static int cache[4][4][3][3] = {};
-  static int cache_pipes[4][4][3][3] = {};
+  static int cache[4][4][3][4] = {};
+  static int cache_pipes[4][4][3][4] = {};
   const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
-  const int gi = group <= 4 ? 0 : group <= 8 ? 1 : 2;
+  const int gi = group <= 4 ? 0 : group <= 8 ? 1 : group <= 16 ? 2 : 3;
   std::lock_guard<std::mutex> lock(mu);
   int& slot = cache[kc & 3][vc & 3][di][gi];
   int& pslot = cache_pipes[kc & 3][vc & 3][di][gi];
@@ -439,7 +439,10 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
   kvq_status st = make_plan(k_store, v_store, batch, rows, max_len_hint, opts, &p);
   if (st != KVQ_OK) return st;
   if (workspace_bytes < p.total) return KVQ_ERR_WORKSPACE;
-  if (group > 16 || p.variant < 1 || p.variant > 2) return KVQ_ERR_UNSUPPORTED;
+  // query rows per KV head: up to 16, or 32 for q8_0 K and V at head_dim >= 128 (the
+  // tensor-core kernel's heads-on-M loop)
+  const bool rows32 = kd.codec == KVQ_CODEC_Q8_0 && vd.codec == KVQ_CODEC_Q8_0 && kd.head_dim >= 128;
+  if (group > (rows32 && p.variant == 2 ? 32 : 16) || p.variant < 1 || p.variant > 2) return KVQ_ERR_UNSUPPORTED;
   if ((k_new || tokens > 1) && p.variant != 2) return KVQ_ERR_UNSUPPORTED;
   SimtFn sfn = simt_fn(kd.codec, vd.codec);
   MmaFn mfn = mma_fn(kd.codec, vd.codec);
@@ -475,15 +478,22 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
   a.seq_lens_adv = seq_lens_adv;
   a.seq_counters = reinterpret_cast<unsigned*>(ws + p.seq_cnt_off);
   a.warp_records = p.records;
+  // the heads-on-M loop (q8_0 K and V, head_dim 128 or 256, 9..32 query rows per KV head)
+  // leaves its chunk partials to the chunk merge kernel
+  a.chunk_merge = (p.variant == 2 && kd.codec == KVQ_CODEC_Q8_0 && vd.codec == KVQ_CODEC_Q8_0 &&
+                   (kd.head_dim == 128 || kd.head_dim == 256) && group > 8 && p.n_chunks > 1)
+                      ? 1 : 0;
   fault_injection(&a.wait_limit, &a.skip_tile);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (reset_counters && cudaMemsetAsync(ws + p.cnt_off, 0, p.total - p.cnt_off, s) != cudaSuccess)
     return KVQ_ERR_CUDA;
   if (p.variant == 2) {
-    // the tensor-core kernel merges the split itself (last CTA per unit), or in record
-    // mode leaves per-warp records for the merge kernel launched right after it
+    // the tensor-core kernel merges the split itself (last CTA per unit), or leaves its
+    // partials to a merge kernel launched right after it (record and chunk-merge modes)
     st = from_cuda(mfn(a, kd.head_dim, k_store->rows_map, v_store->rows_map, s));
-    if (st != KVQ_OK || !p.records) return st;
+    if (st != KVQ_OK) return st;
+    if (a.chunk_merge) return from_cuda(launch_chunk_merge_pdl(a, kd.head_dim, s));
+    if (!p.records) return st;
     return from_cuda(launch_record_merge_pdl(a, kd.head_dim, vd.codec, s));
   }
   st = from_cuda(sfn(a, kd.head_dim, s));

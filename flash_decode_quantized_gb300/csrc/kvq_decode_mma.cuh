@@ -250,7 +250,12 @@ __device__ __forceinline__ void load_scale_words(const uint8_t* base, int t, uin
 
 template <int KC, int VC, int D, int GW, int HG>
 struct Cfg {
-  static constexpr int PW = 4 * HG;                       // warps per pipeline (4 per head group)
+  // Heads on M (GW == 16, kvq_decode_hm.cuh): warps of 16 query rows x 16 tokens, HG row
+  // groups per pipeline; at head_dim 256 the two warps of a slice pair split head_dim
+  // (DS = 2) so that a warp's O accumulators take 64 registers and 16 warps fit an SM.
+  static constexpr bool HM = GW == 16;
+  static constexpr int DS = HM && D == 256 ? 2 : 1;
+  static constexpr int PW = 4 * HG * DS;                  // warps per pipeline (4 per head group)
   static constexpr int NPV = GW <= 4 ? 1 : 2;             // PV n-tiles per warp
   static constexpr bool KBF = KC == KVQ_CODEC_BF16;       // MMA type of QK^T
   static constexpr bool VBF = VC == KVQ_CODEC_BF16;       // MMA type of PV
@@ -274,33 +279,48 @@ struct Cfg {
   // pipelines in shared memory, so a split has a quarter as many partials as with one
   // pipeline per CTA.  Otherwise one pipeline per CTA and register use sets occupancy.
   static constexpr bool PACK = HG == 1 && GW <= 4 && D <= 128 && 2 * STAGE + 6 * 1024 <= 56 * 1024;
-  static constexpr int NP = PACK ? 4 : 1;                 // pipelines per CTA
+  // HM: two pipelines per CTA for one row group, one for two
+  static constexpr int NP = PACK ? 4 : (HM && HG == 1) ? 2 : 1;   // pipelines per CTA
   // the lean tile loop (see decode_cta) serves warps of at most 4 heads at D <= 128
   static constexpr bool LEAN = HG == 1 && GW <= 4 && D <= 128;
   static constexpr int NW = PW * NP;                      // warps per CTA
   static constexpr int THREADS = NW * 32;
   static constexpr int MINB = 1;
   // ring depth per pipeline: as many stages (2..4) as fit the per-pipeline budget
-  static constexpr int SMEM_BUDGET = HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : PACK ? 54 * 1024 : 70 * 1024;
+  static constexpr int SMEM_BUDGET = HM ? (DS > 1 ? (HG > 1 ? 140 * 1024 : 70 * 1024) : HG > 1 ? 204 * 1024 : 104 * 1024 + 2048)
+                                     : HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : PACK ? 54 * 1024 : 70 * 1024;
   static constexpr int NS0 = (SMEM_BUDGET - 2048) / STAGE;
   static constexpr int NS = NS0 > 4 ? 4 : (NS0 < 2 ? 2 : NS0);
   static constexpr int PRING = NS * STAGE;                // one pipeline's ring
-  static constexpr int OBUF = NW * 8 * D * 4;             // merge buffer (reuses the rings)
+  static constexpr int OBUF = NW * (HM ? 16 * D / DS : 8 * D) * 4;   // merge buffer (reuses the rings)
   static constexpr int RING = NP * PRING > OBUF ? NP * PRING : OBUF;
   static constexpr int BAR_OFF = RING;                    // [NP][full NS | empty NS] mbarriers
   static constexpr int OK_OFF = BAR_OFF + NP * 2 * NS * 8;  // [NP][NS] "tile is valid" flags, then a flag
   static constexpr int KB_OFF = OK_OFF + 128;             // QK accumulator seeds [HG][NB][4] f32x2
-  static constexpr int ML_OFF = KB_OFF + HG * NB * 4 * 8; // per-warp m, l [NW][8][2]
-  static constexpr int PG_OFF = ML_OFF + (NW + 2) * 16 * 4;   // + per-head (M, l); then [NP][64] page ids
+  static constexpr int ML_OFF = KB_OFF + HG * NB * 4 * 8; // per-warp m, l [NW][8][2] (HM: [NW][16][2])
+  static constexpr int ML_BYTES = HM ? (NW + HG) * 16 * 8 : (NW + 2) * 16 * 4;
+  static constexpr int PG_OFF = ML_OFF + ML_BYTES;        // + per-head (M, l); then [NP][64] page ids
   static constexpr int RC_OFF = PG_OFF + NP * 64 * 4;     // [NP][NS] releases counted per stage
   static constexpr int LI_OFF = RC_OFF + 16 * 4;          // [NP][NS] last tile issued into each stage
-  static constexpr int SMEM = LI_OFF + 16 * 4 + 1024;     // +1024: alignment
+  // HM: q in MMA fragment order [HG][D/16][32 lanes] x 16 bytes, then the QK seeds
+  // [HG][NB][8] f32x2 (rows r, r + 8)
+  static constexpr int QF_OFF = LI_OFF + 16 * 4;
+  static constexpr int SD_OFF = QF_OFF + (HM ? HG * (D / 16) * 512 : 0);
+  // HM: per warp, the f32 block scales of its 16-token slice, K [NB][16] then V [NB/DS][16];
+  // with DS = 2 the score exchange of each slice pair, [pair][2 buffers][2 halves][32 lanes]
+  // float4, and its mbarriers [pair][2]
+  static constexpr int SC_OFF = SD_OFF + (HM ? HG * NB * 64 : 0);
+  static constexpr int XS_OFF = SC_OFF + (HM ? NW * (NB + NB / DS) * 16 * 4 : 0);
+  static constexpr int NPAIRS = HM && DS > 1 ? NP * HG * 4 : 0;
+  static constexpr int XB_OFF = XS_OFF + NPAIRS * 2 * 2 * 32 * 16;
+  static constexpr int SMEM = XB_OFF + NPAIRS * 16 + 1024;   // +1024: alignment
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
   static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
   // 233472 bytes of shared memory per SM, 1024 of them reserved per resident CTA
   static_assert(!PACK || SMEM + 1024 <= 233472, "the four pipelines must fit one SM");
   static_assert(NP * NS <= 16, "stage flags");
+  static_assert(!HM || SMEM <= 232448, "heads-on-M configuration exceeds shared memory");
 };
 
 // Shared-memory address of 16-byte chunk `chunk` of tile row `t` (rows as TMA wrote them).
@@ -467,6 +487,53 @@ __device__ void merge_partials(const float* ml, const float* o, long long stride
   }
 }
 
+// Split-K combine (a8) after a CTA wrote its chunk partial.  Two levels, both done by
+// whichever CTA arrives last (atomic counters in the workspace, returned to zero by that
+// CTA):
+//   group: the last of the <= kGroup chunks of a group merges their partials into a
+//          group partial while the rest of the grid is still streaming;
+//   unit:  the last group of a (sequence, KV head) merges the group partials into the
+//          output.  A single group (up to 64 chunks form one) writes the output directly.
+template <int D, int NW>
+__device__ __forceinline__ void split_k_combine(const DecodeArgs& a, uint8_t* smem, volatile int* last_flag, int b,
+                                                int kvh, int chunk, int nv, long long head0, int gcount) {
+  const int tid = threadIdx.x, NWT = NW * 32;
+  const long long unit = (long long)b * a.k.num_kv_heads + kvh;
+  const int gsz = nv <= 4 * kGroup ? nv : kGroup;   // up to 64 partials: one level
+  const int ng = (nv + gsz - 1) / gsz;
+  const int g = chunk / gsz;
+  const int g_first = g * gsz;
+  const int g_count = min(gsz, nv - g_first);
+  if (!arrive_last(a.counters + a.grp_counter_off + unit * a.n_groups + g, g_count, tid, NWT, last_flag,
+                   a.k.status))
+    return;
+  // merge this group's chunk partials
+  merge_partials<D, NW>(
+      a.part_ml + (head0 * a.n_chunks + g_first) * 2, a.part_o + (head0 * a.n_chunks + g_first) * D,
+      (long long)a.n_chunks, g_count, gcount, ng == 1,
+      a.gpart_ml + (head0 * a.n_groups + g) * 2, a.gpart_o + (head0 * a.n_groups + g) * D,
+      (long long)a.n_groups, a.out + head0 * D, reinterpret_cast<float*>(smem));
+  if (tid == 0) a.counters[a.grp_counter_off + unit * a.n_groups + g] = 0u;
+  if (ng == 1) {
+    return;
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");   // group partial written before arriving
+  if (!arrive_last(a.counters + unit, ng, tid, NWT, last_flag, a.k.status)) return;
+  // the group partials were written by other CTAs before their arrivals
+  merge_partials<D, NW>(a.gpart_ml + head0 * a.n_groups * 2, a.gpart_o + head0 * a.n_groups * D,
+                        (long long)a.n_groups, ng, gcount, true, nullptr, nullptr, 0, a.out + head0 * D,
+                        reinterpret_cast<float*>(smem));
+  if (tid == 0) a.counters[unit] = 0u;
+}
+
+}  // namespace mma
+}  // namespace kvq
+
+#include "kvq_decode_hm.cuh"
+
+namespace kvq {
+namespace mma {
+
 // ---------------------------------------------------------------- kernel
 
 // Arrival on a per-sequence counter (release: the arriving CTA's reads of seq_lens come
@@ -513,6 +580,9 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t* pt = a.page_table + (long long)b * a.max_pages;
+  // heads-on-M loop: this thread's q loads, in flight with the reads below
+  HmQ<KC, D, HG, C::THREADS, C::HM> hmq;
+  hmq.load(a, (long long)b * a.num_q_heads + (long long)kvh * G, G);
   // Page ids of this CTA's tiles, held by warp 0: lane i has tile pb + i in pg_lo and
   // tile pb + 32 + i in pg_hi.  The first 64 are read together with seq_lens (any
   // in-bounds table entry may be read; entries past the sequence are never used).
@@ -574,6 +644,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       const long long rec0 = ((long long)b * gridDim.y + kvh) * a.warp_records + (long long)chunk * C::NW;
       for (int i = tid; i < C::NW * 2; i += C::THREADS)
         reinterpret_cast<float4*>(a.part_ml + (rec0 + i / 2) * 8)[i & 1] = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+    } else if (C::HM && a.chunk_merge) {
+      // chunk-merge mode: this CTA's partial is empty (m = -inf), the merge skips it
+      const long long h0 = (long long)b * a.num_q_heads + (long long)kvh * G;
+      for (int v = tid; v < G; v += C::THREADS)
+        reinterpret_cast<float2*>(a.part_ml)[(h0 + v) * a.n_chunks + chunk] = make_float2(-INFINITY, 0.0f);
     } else if (L == 0 && chunk == 0) {  // empty sequence: its heads' outputs are zero
       const long long h0 = (long long)b * a.num_q_heads + (long long)kvh * G;
       for (int idx = tid; idx < G * D; idx += C::THREADS) a.out[h0 * D + idx] = 0.0f;
@@ -599,7 +674,7 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   unsigned* const rcnt = reinterpret_cast<unsigned*>(smem + C::RC_OFF) + pipe * C::NS;
   volatile int* const last_issued = reinterpret_cast<volatile int*>(smem + C::LI_OFF) + pipe * C::NS;
   if (pw == 0 && lane < C::NS) last_issued[lane] = -1;
-  if (C::LEAN && pw == 0) {
+  if ((C::LEAN || C::HM) && pw == 0) {
     pgs[lane] = pg_lo;
     pgs[32 + lane] = pg_hi;
     if (lane < C::NS) rcnt[lane] = 0u;
@@ -689,6 +764,14 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     if (need_enc) encode_new();   // its tile comes later, from the refill path
   }
 
+  if constexpr (C::HM) {
+    // ---------------------------------------------------------- heads-on-M loop
+    if (hm_body<KC, VC, D, GW, HG>(a, smem, b, kvh, chunk, pipe, pw, warp, lane, tid, vchunk, nvc, n_tiles, L, nv,
+                                   sring, bar_full, bar_empty, stage_ok, pgs, rcnt, last_issued, issue_tile,
+                                   load_page, adv, seq_ticket, hmq))
+      split_k_combine<D, C::NW>(a, smem, reinterpret_cast<volatile int*>(smem + C::OK_OFF) + 16, b, kvh, chunk, nv,
+                                (long long)b * a.num_q_heads + (long long)kvh * G, G < 16 * HG ? G : 16 * HG);
+  } else {   // tokens-on-M loop
   // ------------------------------------------------------------ compute warps
   const int hg = pw >> 2;            // head group
   const int ws = pw & 3;             // 16-token slice of every tile
@@ -1567,39 +1650,9 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
     }
   }
   // ------------------------------------------------------------ split-K combine (a8)
-  // Two levels, both done by whichever CTA arrives last (atomic counters in the
-  // workspace, returned to zero by that CTA):
-  //   group: the last of the <= kGroup chunks of a group merges their partials into a
-  //          group partial while the rest of the grid is still streaming;
-  //   unit:  the last group of a (sequence, KV head) merges the group partials into the
-  //          output.  A single group (up to 64 chunks form one) writes the output directly.
-  const long long unit = (long long)b * a.k.num_kv_heads + kvh;
-  const int gsz = nv <= 4 * kGroup ? nv : kGroup;   // up to 64 partials: one level
-  const int ng = (nv + gsz - 1) / gsz;
-  const int g = chunk / gsz;
-  const int g_first = g * gsz;
-  const int g_count = min(gsz, nv - g_first);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::OK_OFF) + 16;
-  if (!arrive_last(a.counters + a.grp_counter_off + unit * a.n_groups + g, g_count, tid, NWT, last_flag,
-                   a.k.status))
-    return;
-  // merge this group's chunk partials
-  merge_partials<D, C::NW>(
-      a.part_ml + (head0 * a.n_chunks + g_first) * 2, a.part_o + (head0 * a.n_chunks + g_first) * D,
-      (long long)a.n_chunks, g_count, gcount, ng == 1,
-      a.gpart_ml + (head0 * a.n_groups + g) * 2, a.gpart_o + (head0 * a.n_groups + g) * D,
-      (long long)a.n_groups, a.out + head0 * D, reinterpret_cast<float*>(smem));
-  if (tid == 0) a.counters[a.grp_counter_off + unit * a.n_groups + g] = 0u;
-  if (ng == 1) {
-    return;
-  }
-  asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");   // group partial written before arriving
-  if (!arrive_last(a.counters + unit, ng, tid, NWT, last_flag, a.k.status)) return;
-  // the group partials were written by other CTAs before their arrivals
-  merge_partials<D, C::NW>(a.gpart_ml + head0 * a.n_groups * 2, a.gpart_o + head0 * a.n_groups * D,
-                           (long long)a.n_groups, ng, gcount, true, nullptr, nullptr, 0, a.out + head0 * D,
-                           reinterpret_cast<float*>(smem));
-  if (tid == 0) a.counters[unit] = 0u;
+  split_k_combine<D, C::NW>(a, smem, reinterpret_cast<volatile int*>(smem + C::OK_OFF) + 16, b, kvh, chunk, nv,
+                            head0, gcount);
+  }   // tokens-on-M loop
 }
 
 template <int KC, int VC, int D, int GW, int HG>
@@ -1650,12 +1703,22 @@ int occupancy(int* pipes) {
   return n;
 }
 
+// The heads-on-M loop serves 9..32 query rows per KV head for q8_0 K and V at head_dim
+// 128 and 256; other shapes take the tokens-on-M loop (up to 16 rows).
+template <int KC, int VC>
+constexpr bool kHeadsOnM = KC == KVQ_CODEC_Q8_0 && VC == KVQ_CODEC_Q8_0;
+
 template <int KC, int VC>
 int occupancy_pair(int head_dim, int g, int* pipes) {
-#define KVQ_MMA_O(D)                                         \
-  if (g <= 4) return occupancy<KC, VC, D, 4, 1>(pipes);      \
-  if (g <= 8) return occupancy<KC, VC, D, 8, 1>(pipes);      \
-  if (g <= 16) return occupancy<KC, VC, D, 8, 2>(pipes);     \
+#define KVQ_MMA_O(D)                                                               \
+  if (g <= 4) return occupancy<KC, VC, D, 4, 1>(pipes);                            \
+  if (g <= 8) return occupancy<KC, VC, D, 8, 1>(pipes);                            \
+  if constexpr (kHeadsOnM<KC, VC> && D >= 128) {                                   \
+    if (g <= 16) return occupancy<KC, VC, D, 16, 1>(pipes);                        \
+    if (g <= 32) return occupancy<KC, VC, D, 16, 2>(pipes);                        \
+  } else {                                                                         \
+    if (g <= 16) return occupancy<KC, VC, D, 8, 2>(pipes);                         \
+  }                                                                                \
   return 0;
   switch (head_dim) {
     case 64: { KVQ_MMA_O(64) }
@@ -1670,10 +1733,15 @@ template <int KC, int VC>
 cudaError_t launch_pair(const DecodeArgs& a, int head_dim, const CUtensorMap& tmk, const CUtensorMap& tmv,
                         cudaStream_t stream) {
   const int g = a.group;
-#define KVQ_MMA_G(D)                                                         \
-  if (g <= 4) return launch<KC, VC, D, 4, 1>(a, tmk, tmv, stream);          \
-  if (g <= 8) return launch<KC, VC, D, 8, 1>(a, tmk, tmv, stream);          \
-  if (g <= 16) return launch<KC, VC, D, 8, 2>(a, tmk, tmv, stream);         \
+#define KVQ_MMA_G(D)                                                               \
+  if (g <= 4) return launch<KC, VC, D, 4, 1>(a, tmk, tmv, stream);                \
+  if (g <= 8) return launch<KC, VC, D, 8, 1>(a, tmk, tmv, stream);                \
+  if constexpr (kHeadsOnM<KC, VC> && D >= 128) {                                   \
+    if (g <= 16) return launch<KC, VC, D, 16, 1>(a, tmk, tmv, stream);             \
+    if (g <= 32) return launch<KC, VC, D, 16, 2>(a, tmk, tmv, stream);             \
+  } else {                                                                         \
+    if (g <= 16) return launch<KC, VC, D, 8, 2>(a, tmk, tmv, stream);              \
+  }                                                                                \
   return cudaErrorNotSupported;
   switch (head_dim) {
     case 64: { KVQ_MMA_G(64) }

@@ -104,6 +104,10 @@ struct DecodeArgs {
   //   part_o  [unit][record][D * 4]: unnormalized O in the accumulator's register order
   // and the record merge kernel (launched right after it) forms the output.
   int warp_records;
+  // Chunk-merge mode (heads-on-M loop): every CTA writes its chunk partial (m = -inf for a
+  // CTA without tokens) to part_ml / part_o and the chunk merge kernel, launched right
+  // after it, combines them into the output (no arrival counters, no in-place merge).
+  int chunk_merge;
   int wait_limit;              // tries of each bounded mbarrier wait before it gives up
   int skip_tile;               // fault injection: tile the first pipeline never issues (-1: none)
 };
@@ -152,6 +156,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 cudaError_t launch_combine_pdl(const DecodeArgs& a, int head_dim, cudaStream_t stream);
+cudaError_t launch_chunk_merge_pdl(const DecodeArgs& a, int head_dim, cudaStream_t stream);
 cudaError_t launch_record_merge_pdl(const DecodeArgs& a, int head_dim, int v_codec, cudaStream_t stream);
 
 void count_launch();

@@ -1,5 +1,6 @@
-// Split-K combine (step a8) for the decode's record mode: merges the per-warp partials
-// (records) of every (sequence, KV head) unit into the output.
+// Split-K combines (step a8) launched after the tensor-core decode kernel: the record merge
+// (record mode: per-warp partials of every (sequence, KV head) unit) and the chunk merge
+// (chunk-merge mode: per-CTA partials of every query row).
 //
 // A record r holds, for each of the unit's (at most 4) query heads h, the warp's running
 // maximum m_rh of the base-2 logits, its sum l_rh = sum 2^(s - m_rh) and the unnormalized
@@ -184,7 +185,128 @@ cudaError_t launch_merge_d(const DecodeArgs& a, int head_dim, cudaStream_t strea
   return cudaErrorNotSupported;
 }
 
+// ---------------------------------------------------------------- chunk merge
+// Split-K combine (step a8) for the chunk-merge mode of the heads-on-M loop: merges the
+// n_chunks chunk partials (m_c, l_c, O_c) of every query row into its output,
+//   M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,
+// skipping partials with m = -inf (chunks without tokens; their O is not written).
+// Grid: (64-element slices of head_dim, query rows).  256 threads = 16 float4 columns x 16
+// chunk groups; each thread loads the O values of its chunks (c = group, group + 16, ...)
+// first, the CTA forms the weights from all chunks' (m, l) meanwhile, and the groups' sums
+// meet in shared memory in a fixed order.
+constexpr int kCmThreads = 256, kCmCols = 16, kCmGroups = kCmThreads / kCmCols, kCmBatch = 8;
+
+__device__ __forceinline__ float block_reduce1(float v, bool is_max, float* red, float* res) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float r = red[0];
+    for (int w = 1; w < kCmThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    *res = r;
+  }
+  __syncthreads();
+  return *res;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kCmThreads) chunk_merge_kernel(DecodeArgs a) {
+  extern __shared__ float cw[];                 // [n_chunks] weights 2^(m_c - M)
+  __shared__ float red[kCmThreads / 32];
+  __shared__ float sres[2];
+  __shared__ float4 racc[kCmGroups][kCmCols];
+  const int tid = threadIdx.x, q = tid % kCmCols, g = tid / kCmCols;
+  const int n = a.n_chunks;
+  const long long row = blockIdx.y;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + row * n;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + row * n * D) + blockIdx.x * kCmCols + q;
+  // this thread's first batch of O values, in flight while the weights are formed
+  float4 ov[kCmBatch];
+#pragma unroll
+  for (int u = 0; u < kCmBatch; ++u) {
+    const int c = g + u * kCmGroups;
+    if (c < n) ov[u] = __ldcg(po + (long long)c * (D / 4));
+  }
+  float m = -INFINITY;
+  for (int c = tid; c < n; c += kCmThreads) m = fmaxf(m, __ldcg(ml + c).x);
+  const float M = block_reduce1(m, true, red, &sres[0]);
+  float den = 0.0f;
+  for (int c = tid; c < n; c += kCmThreads) {
+    const float2 x = __ldcg(ml + c);
+    const float w = x.x == -INFINITY ? 0.0f : fast_exp2(x.x - M);
+    cw[c] = w;
+    den = fmaf(w, x.y, den);
+  }
+  den = block_reduce1(den, false, red, &sres[1]);   // its barriers also publish cw
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  auto fold = [&](int c, const float4& o) {
+    const float w = cw[c];
+    if (w != 0.0f) {
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
+  };
+#pragma unroll
+  for (int u = 0; u < kCmBatch; ++u) {
+    const int c = g + u * kCmGroups;
+    if (c < n) fold(c, ov[u]);
+  }
+  for (int c0 = g + kCmBatch * kCmGroups; c0 < n; c0 += kCmBatch * kCmGroups) {
+#pragma unroll
+    for (int u = 0; u < kCmBatch; ++u) {
+      const int c = c0 + u * kCmGroups;
+      if (c < n) ov[u] = __ldcg(po + (long long)c * (D / 4));
+    }
+#pragma unroll
+    for (int u = 0; u < kCmBatch; ++u) {
+      const int c = c0 + u * kCmGroups;
+      if (c < n) fold(c, ov[u]);
+    }
+  }
+  racc[g][q] = acc;
+  __syncthreads();
+  if (tid < kCmCols) {
+    float4 sum = racc[0][tid];
+    for (int gg = 1; gg < kCmGroups; ++gg) {
+      const float4 x = racc[gg][tid];
+      sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+    }
+    const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+    reinterpret_cast<float4*>(a.out + row * D)[blockIdx.x * kCmCols + tid] =
+        make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
+  }
+}
+
+template <int D>
+cudaError_t launch_cm(const DecodeArgs& a, cudaStream_t stream) {
+  auto kern = chunk_merge_kernel<D>;
+  const size_t smem = (size_t)a.n_chunks * 4;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(D / (4 * kCmCols), (unsigned)((long long)a.batch * a.num_q_heads));
+  const cudaError_t e = launch_pdl(kern, grid, dim3(kCmThreads), smem, stream, a);
+  count_launch();
+  return e;
+}
+
 }  // namespace
+
+cudaError_t launch_chunk_merge_pdl(const DecodeArgs& a, int head_dim, cudaStream_t stream) {
+  if (head_dim == 128) return launch_cm<128>(a, stream);
+  if (head_dim == 256) return launch_cm<256>(a, stream);
+  return cudaErrorNotSupported;
+}
 
 cudaError_t launch_record_merge_pdl(const DecodeArgs& a, int head_dim, int v_codec, cudaStream_t stream) {
   switch (v_codec) {

@@ -212,7 +212,8 @@ kvq_status kvq_decode_workspace_init(void* workspace, size_t workspace_bytes, vo
  *   seq_lens   device int32 [batch], each in [0, max_len_hint]
  *   page_table device int32 [batch][max_pages]
  *   out        device fp32 [batch][num_q_heads][head_dim]
- *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads); up to 16 query heads per
+ *   KV head (32 for q8_0 K and V at head_dim 128 or 256 on the tensor-core kernel).
  *   softmax_scale <= 0 selects 1/sqrt(head_dim).
  *   max_len_hint: host-side upper bound of seq_lens, used to size the split without a
  *   device round trip; a longer sequence is truncated and recorded as a device fault.
@@ -236,8 +237,9 @@ kvq_status kvq_flash_decode(const void* q, const kvq_store* k_store, const kvq_s
  *   out  device fp32 [batch][num_q_heads][num_tokens][head_dim]
  *   seq_lens[b] >= num_tokens (it counts the drafts, already appended with kvq_append_kv).
  * The workspace must hold kvq_decode_workspace_bytes(..., num_q_heads * num_tokens, ...).
- * Needs (num_q_heads / num_kv_heads) * num_tokens <= 16 and the tensor-core kernel
- * (opts->variant 0 or 2), else KVQ_ERR_UNSUPPORTED.  num_tokens == 1 is kvq_flash_decode.
+ * Needs (num_q_heads / num_kv_heads) * num_tokens <= 16 (<= 32 for q8_0 K and V at
+ * head_dim 128 or 256) and the tensor-core kernel (opts->variant 0 or 2), else
+ * KVQ_ERR_UNSUPPORTED.  num_tokens == 1 is kvq_flash_decode.
  * A sequence shorter than num_tokens attends as if its drafts started at position 0
  * (query i sees positions below i + 1 - num_tokens + seq_lens[b], none if that is <= 0,
  * giving zeros). */

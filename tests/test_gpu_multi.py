@@ -76,13 +76,26 @@ def test_one_token_equals_single_decode():
     assert torch.equal(single, multi[:, :, 0])
 
 
+@pytest.mark.parametrize("hq,hkv,T,d", [(32, 2, 2, 256), (32, 2, 2, 128), (32, 8, 8, 128), (32, 8, 5, 128),
+                                        (48, 2, 1, 256), (24, 2, 2, 256)])
+def test_more_than_16_query_rows(hq, hkv, T, d):
+    # 17..32 query rows per KV head (q8_0 K and V): two 16-row groups of the heads-on-M loop,
+    # the second one partly empty for 20 and 24 rows
+    inp = make_inputs([1500, 200, T, T + 3], hq, hkv, d, seed=90 + T, dist="t3", channel_scaled=True)
+    got, want = run(inp, "q8_0", "q8_0", T, seed=91 + T)
+    assert_close(got, want, f"G={hq // hkv} T={T} D={d}")
+
+
 def test_too_many_query_rows_is_unsupported():
     inp = make_inputs([100], 32, 8, 128, seed=88)
     k = kvq()
     ks, vs = build_store(inp, "q8_0", "k"), build_store(inp, "q8_0", "v")
     _, seq, pt = device_inputs(inp)
-    q = torch.zeros((1, 32, 5, 128), dtype=torch.bfloat16, device="cuda")   # G * T = 20 > 16
+    q = torch.zeros((1, 32, 9, 128), dtype=torch.bfloat16, device="cuda")   # G * T = 36 > 32
     with pytest.raises(k.KvqError):
         k.kvq_flash_decode_multi(q, ks, vs, seq, pt)
+    k4, v4 = build_store(inp, "q4s", "k"), build_store(inp, "q4s", "v")
+    with pytest.raises(k.KvqError):   # beyond 16 rows only q8_0 K and V
+        k.kvq_flash_decode_multi(q[:, :, :5].contiguous(), k4, v4, seq, pt)
     with pytest.raises(k.KvqError):   # the CUDA-core kernel has no multi-token form
         k.kvq_flash_decode_multi(q[:, :, :2].contiguous(), ks, vs, seq, pt, variant=1)
