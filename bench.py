@@ -1,13 +1,21 @@
 """Benchmark: decode-attention µs per layer-step and effective KV GB/s (% of HBM peak).
 
-One step = one pass of the whole hot path on one layer: on-device encode of the new K and
-V row into the resident store with seq_lens += 1 (kvq_append_kv, one launch), and the
-split-K fused dequant flash-decode (kvq_flash_decode, one launch for the tensor-core
-kernel, whose last CTAs also merge the split).  The store grows
-by one token per step.  Inputs are resident in HBM when the timed region starts; the L2
-is flushed before every timed step by reading a 2 x L2 buffer (leaving clean lines, so
-the timed kernel pays no write-back), outside its events, with a bounded ~100 µs GPU
-wait queued after it so that the events time the GPU work, not host launch latency.
+One step = one pass of the whole hot path on one layer, through kvq_flash_decode_append:
+the decode kernel encodes the new token's K and V rows into the resident store, runs the
+split-K fused-dequant flash-decode over the whole sequence (new token included), and a
+second kernel, chained to it by programmatic dependent launch, merges the per-warp
+partial results into the output and advances seq_lens by one: two launches per step
+(record mode; plans whose partials do not fit the record layout merge in place inside the
+decode kernel, one launch).  The store grows by one token per step.  Inputs are resident
+in HBM when the timed region starts; the L2 is flushed before every timed step by reading
+a 2 x L2 buffer (leaving clean lines, so the timed kernel pays no write-back), outside its
+events, with a bounded ~100 µs GPU wait queued after it so that the events time the GPU
+work, not host launch latency.  That wait spins a fixed number of SM cycles, so its own
+event-timed length gives the SM clock of every step.
+
+The headline time is the 10%-trimmed mean of the K per-step event times (the event clock
+ticks in ~2 µs steps, which a median would round to); the median, p10/p90 and a
+1000-step distribution with per-step clock bins are reported beside it.
 
 Default workload: 8B-class decode layer, one sequence, 32 query heads on 8 KV heads,
 head_dim 128, kv_len 65536, q8_0 K and V; the sweep adds every codec arm at kv_len 4096,
@@ -37,6 +45,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+DIST_STEPS = 1000                     # steps of the per-step distribution block
 METRIC = "decode-attention µs/layer-step & effective KV GB/s (% of HBM peak) vs kv_len"
 FALLBACK_HBM_GBS = 6800.0
 ROW_BYTES = {"bf16": lambda d: 2 * d, "f16": lambda d: 2 * d, "q8_0": lambda d: d + d // 16,
@@ -304,11 +313,70 @@ def l2_flusher(torch):
     return flush
 
 
+LEAD_CYCLES = 200_000
+
+
 def gpu_lead(torch):
-    """Keeps the GPU busy ~100 µs (a bounded cycle-count wait) so that the host has
-    enqueued the whole step before the GPU reaches the step's first event; otherwise the
-    events would time host launch latency."""
-    torch.cuda._sleep(200_000)
+    """Keeps the GPU busy ~100 µs (a wait of LEAD_CYCLES SM clock cycles) so that the host
+    has enqueued the whole step before the GPU reaches the step's first event; otherwise
+    the events would time host launch latency."""
+    torch.cuda._sleep(LEAD_CYCLES)
+
+
+def trimmed_mean(xs, frac=0.1):
+    """Mean of the values left after dropping the lowest and highest `frac` of them."""
+    xs = sorted(xs)
+    k = int(len(xs) * frac)
+    core = xs[k:len(xs) - k] or xs
+    return sum(core) / len(core)
+
+
+def timed_steps(torch, fn, flush, n):
+    """n calls of fn, each after an L2 flush and the cycle-count lead, each bracketed by
+    CUDA events on the current stream.  Returns (ms per call, SM MHz per call); the clock
+    of a call is LEAD_CYCLES over its lead's event-timed length (an estimate within the
+    event clock's ~2 µs resolution, ~2%)."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        flush()
+        ev[i][0].record()
+        gpu_lead(torch)
+        ev[i][1].record()
+        fn()
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    mhz = [LEAD_CYCLES / max(ev[i][0].elapsed_time(ev[i][1]), 1e-6) / 1e3 for i in range(n)]
+    return ms, mhz
+
+
+def step_stats(ms, mhz=None):
+    """Trimmed mean, median, p10/p90 (µs) of per-step times; with clocks, per-step SM clock
+    bins (steps, trimmed mean and median time per bin)."""
+    out = {"steps": len(ms), "trimmed_mean_us": round(trimmed_mean(ms) * 1e3, 2),
+           "median_us": round(statistics.median(ms) * 1e3, 2),
+           "p10_p90_us": [round(float(np.percentile(ms, 10)) * 1e3, 2),
+                          round(float(np.percentile(ms, 90)) * 1e3, 2)]}
+    if mhz:
+        out["sm_mhz_median"] = round(statistics.median(mhz), 0)
+        bins = {}
+        for lo, hi, name in ((1980, 1e9, ">=1980"), (1880, 1980, "1880-1980"), (0, 1880, "<1880")):
+            sel = [t for t, f in zip(ms, mhz) if lo <= f < hi]
+            if sel:
+                bins[name] = {"steps": len(sel), "trimmed_mean_us": round(trimmed_mean(sel) * 1e3, 2),
+                              "median_us": round(statistics.median(sel) * 1e3, 2)}
+        out["clock_bins_mhz"] = bins
+    return out
+
+
+def bench_config(wl_name, wl, codec, kv_len_desc, world):
+    """The workload this run measures; both arms print the same dict."""
+    return {"workload": f"{wl_name}: B={wl['batch']}, Hq={wl['hq']}, Hkv={wl['hkv']}, D={wl['d']}, "
+                        f"kv_len={kv_len_desc}",
+            "codec": codec, "kv_len": kv_len_desc,
+            "l2": "GPU arm: KV store evicted from L2 before every timed step by reading a 2xL2 buffer "
+                  "(clean lines), outside the step's events; CPU oracle arm: not applicable",
+            "parallelism": f"replicas x{world}"}
 
 
 def max_over_ranks(torch, x: float, world: int, device) -> float:
@@ -373,7 +441,8 @@ def run_mine(args, rank, world):
         seq_lens = [int(x) for x in ragged_lengths(1234 + rank, wl["batch"])]
     else:
         seq_lens = [args.kv_len or wl["kv_len"]] * wl["batch"]
-    extra = args.warmup + 3 * max(args.steps, 20) + 128   # timed, e2e (two passes), unfused
+    # timed, e2e (three passes), unfused, the 1000-step distribution
+    extra = args.warmup + 4 * max(args.steps, 20) + 128 + DIST_STEPS + 16
     layer = Layer(kvq, torch, wl, codec, seq_lens, extra, seed=1000 + rank)
     layer.prepare(args.variant, args.chunk_tokens)
     flush = l2_flusher(torch)
@@ -388,46 +457,44 @@ def run_mine(args, rank, world):
         torch.distributed.barrier()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     kv_bytes = []
     launches0 = kvq.kvq_launch_count()
+
+    def one_step():
+        layer.step()
+        kv_bytes.append(layer.kv_bytes())
     with ClockSampler(torch.cuda.current_device()) as clk:
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i in range(K):
-            flush()
-            gpu_lead(torch)
-            ev[i][0].record()
-            layer.step()
-            ev[i][1].record()
-            kv_bytes.append(layer.kv_bytes())
-        torch.cuda.synchronize()
+        step_ms, step_mhz = timed_steps(torch, one_step, flush, K)   # synchronizes at the end
         wall = time.perf_counter() - t0
     if world > 1:
         torch.distributed.barrier()
     launches = kvq.kvq_launch_count() - launches0
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    # the step is the one fused kernel (the CUDA-core variant: append + decode + combine)
+    # the step is the decode kernel plus its PDL-chained merge kernel (the CUDA-core
+    # variant: append + decode + combine)
     dec_ms = step_ms
-    # median over the K per-step event pairs (mean and worst step reported beside it): an
-    # nvidia-smi sample landing inside one step can stall that step by ~100 us
-    ms_per_step = max_over_ranks(torch, statistics.median(step_ms), world, "cuda")
+    # 10%-trimmed mean over the K per-step event pairs: robust to the event clock's ~2 us
+    # ticks (which a median rounds to) and to the odd step an nvidia-smi sample stalls
+    ms_per_step = max_over_ranks(torch, trimmed_mean(step_ms), world, "cuda")
     kvb = statistics.mean(kv_bytes)
     value = job_gbs(kvb, world, ms_per_step)
     peak, peak_kind = hbm_peak()
-    dec_mean = statistics.median(dec_ms)
+    dec_mean = trimmed_mean(dec_ms)
     achieved = kvb / (dec_mean * 1e-3) / 1e9
     sha = kernel_sources_sha()
     key = f"{args.workload}:{codec}:{seq_lens[0] if len(set(seq_lens)) == 1 else 'ragged'}"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": recorded_traffic(sha, key),
-                "kernel": "decode_mma_kernel with the fused append (kvq_flash_decode_append), one launch per step" if args.variant != 1 else "kvq_append_kv + decode_simt + combine",
+                "kernel": "decode_mma_kernel with the fused append + record_merge_kernel (kvq_flash_decode_append), timed together per step" if args.variant != 1 else "kvq_append_kv + decode_simt + combine",
                 "peak_source": f"{peak_kind} copy bandwidth",
                 "decode_us": round(dec_mean * 1e3, 2),
+                "decode_us_median": round(statistics.median(dec_ms) * 1e3, 2),
                 "decode_us_p10_p90": [round(float(np.percentile(dec_ms, 10)) * 1e3, 2),
                                       round(float(np.percentile(dec_ms, 90)) * 1e3, 2)],
                 "cv": round(statistics.pstdev(dec_ms) / statistics.mean(dec_ms), 4),
-                "stat": "median of per-step CUDA-event times",
+                "stat": "10%-trimmed mean of per-step CUDA-event times",
+                "clock_bins_mhz": step_stats(step_ms, step_mhz)["clock_bins_mhz"],
                 "read_probe_gbs": round(probe, 1), "frac_of_read_probe": round(achieved / probe, 4)}
 
     e2e = measure_e2e(torch, kvq, layer, flush, max(20, K))
@@ -448,6 +515,12 @@ def run_mine(args, rank, world):
         unfused = {"step_us": round(statistics.mean(a.elapsed_time(c) for a, _, c in ev2) * 1e3, 2),
                    "decode_us": round(statistics.mean(b.elapsed_time(c) for _, b, c in ev2) * 1e3, 2)}
 
+    # a longer run of the same step for its distribution: per-step times and SM clocks
+    dist_ms, dist_mhz = timed_steps(torch, layer.step, flush, DIST_STEPS)
+    distribution = step_stats(dist_ms, dist_mhz)
+    distribution["timing"] = ("the timed step repeated after the timed region, each after an L2 "
+                              "flush; clock per step from the cycle-count lead's event-timed length")
+
     sweep = extras = None
     if rank == 0 and args.workload == "layer8b":
         if not args.no_sweep:
@@ -463,12 +536,11 @@ def run_mine(args, rank, world):
         "us_per_step_max": [round(max(step_ms) * 1e3, 2), int(np.argmax(step_ms))],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, device-generated bf16 rows encoded on device)",
-        "config": {"workload": f"{args.workload}: B={wl['batch']}, Hq={wl['hq']}, Hkv={wl['hkv']}, "
-                               f"D={wl['d']}, kv_len={seq_lens[0] if len(set(seq_lens)) == 1 else 'U[1024,32768]'}",
-                   "codec": codec, "kv_bytes_per_step": int(kvb), "variant": args.variant,
-                   "chunk_tokens": args.chunk_tokens, "l2": "evicted before every timed step by reading a 2xL2 buffer (clean lines), outside its events; ~100 us GPU lead so events exclude host launch latency",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(args.workload, wl, codec, kv_len_desc(wl, seq_lens[0]), world),
+        "run": {"kv_bytes_per_step": int(kvb), "variant": args.variant, "chunk_tokens": args.chunk_tokens,
+                "lead": "~100 us cycle-count GPU wait before each step so that events exclude host launch latency"},
         "roofline": roofline,
+        "distribution": distribution,
         "unfused_step": unfused,
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -598,12 +670,25 @@ def measure_e2e(torch, kvq, layer, flush, iters):
 
     ms, kvb = timed(zc_one)
     sync_ms = timed(zc_one, sync_each=True, n=min(iters, 20))
+    # the same zero-copy call timed on the device, L2 evicted before each (cold, like the
+    # headline), next to the warm back-to-back loop above
+    ctr = [0]
+
+    def zc_next():
+        zc_one(ctr[0] % iters)
+        ctr[0] += 1
+    ev_ms, _ = timed_steps(torch, zc_next, flush, min(iters, 50))
+    ev_t = trimmed_mean(ev_ms)
     return {"ms": round(ms, 5), "unit": "GB/s", "h2d_bytes_per_step": int(n_in * 2),
             "d2h_bytes_per_step": int(layer.out.numel() * 4), "kvb": kvb,
             "timing": f"host wall clock over {iters} back-to-back steps, each one library call whose "
                       "kernel reads the step's inputs from its pinned host slot and writes the output "
                       "to its pinned host slot (zero-copy over the host link), one synchronize at the end",
             "copy_engine": ce,
+            "l2_evicted": {"ms": round(ev_t, 5), "value": round(layer.kv_bytes() / (ev_t * 1e-3) / 1e9, 1),
+                           "timing": "CUDA events around each zero-copy step (inputs read from and output "
+                                     "written to pinned host memory inside it), L2 evicted before each, "
+                                     f"10%-trimmed mean of {len(ev_ms)}"},
             "sync_step": {"ms": round(sync_ms, 5),
                           "value": round(layer.kv_bytes() / (sync_ms * 1e-3) / 1e9, 1),
                           "timing": "one step at a time: the zero-copy step + synchronize, L2 evicted before, median"}}
@@ -844,7 +929,11 @@ def cpu_baseline(args, wl, codec, L):
             "ms_per_layer_step_scaled": round(statistics.mean(times) * wl["hkv"] * 1e3, 1)}
 
 
-def run_reference(args):
+def kv_len_desc(wl, kv_len):
+    return str(kv_len) if wl["kv_len"] is not None else "U[1024,32768]"
+
+
+def run_reference(args, world):
     wl = dict(WORKLOADS[args.workload])
     codec = args.codec or wl["codec"]
     L = args.kv_len or wl["kv_len"] or 16384
@@ -864,9 +953,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded NumPy)", "impl": "reference",
-            "config": {"workload": f"{args.workload}: B={wl['batch']}, Hq={wl['hq']}, Hkv={wl['hkv']}, "
-                                   f"D={wl['d']}, kv_len={L}",
-                       "codec": codec, "kv_len": L},
+            "config": bench_config(args.workload, wl, codec, kv_len_desc(wl, L), world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -894,7 +981,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)))
+            print(json.dumps(run_reference(args, world)))
         return
     if world > 1:
         import torch

@@ -80,8 +80,9 @@ struct HmQ<KC, D, HG, THREADS, true> {
   static __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
     return pack2<false>(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
   }
-  // fragments [HG][QS][32] x 16 bytes; seeds [HG][NB][8] x (row r, row r + 8): -1152 times
-  // the sum of the block's q as the f16 values the MMA multiplies
+  // fragments [HG][QS][32] x 16 bytes; seeds [HG][NB][8] x float4 (row r, row r, row r + 8,
+  // row r + 8), the QK accumulator's initial value: -1152 times the sum of the block's q as
+  // the f16 values the MMA multiplies
   __device__ __forceinline__ void store(uint8_t* smem_qf, uint8_t* smem_sd) const {
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
@@ -105,7 +106,8 @@ struct HmQ<KC, D, HG, THREADS, true> {
           sum += f.x + f.y;
         }
       }
-      reinterpret_cast<float*>(smem_sd)[((g * NB + bb) * 8 + (row & 7)) * 2 + (row >> 3)] = -kBias8 * sum;
+      const float sv = -kBias8 * sum;
+      reinterpret_cast<float2*>(smem_sd)[((g * NB + bb) * 8 + (row & 7)) * 2 + (row >> 3)] = make_float2(sv, sv);
     }
   }
 };
@@ -113,11 +115,6 @@ struct HmQ<KC, D, HG, THREADS, true> {
 // The tile loop of one warp and the CTA's merge of its warps.  Returns true when the CTA
 // wrote a split-K partial for the in-place combine (the caller then runs it), false when
 // it wrote the output itself or leaves its partial to the chunk merge kernel.
-//
-// With DS = 2 (head_dim 256) the two warps of a slice pair split head_dim: each forms the
-// scores of one 8-token N-tile over all of head_dim and accumulates O for half of head_dim
-// (64 accumulator registers, so 16 warps fit an SM); the pair trades its score halves
-// through shared memory under an mbarrier (bounded wait) and then runs the same softmax.
 template <int KC, int VC, int D, int GW, int HG, class QRegs, class IssueFn, class PageFn, class TicketFn>
 __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int b, int kvh, int chunk, int pipe,
                                         int pw, int warp, int lane, int tid, int vchunk, int nvc, int n_tiles,
@@ -128,22 +125,12 @@ __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int 
   using C = Cfg<KC, VC, D, GW, HG>;
   static_assert(KC == KVQ_CODEC_Q8_0 && VC == KVQ_CODEC_Q8_0, "heads-on-M loop: q8_0 K and V");
   constexpr int QS = D / 16, NB = D / 32, NT8 = D / 8;
-  constexpr int DS = C::DS;          // warps per slice (parts of head_dim)
-  constexpr int NTQ = 2 / DS;        // QK N-tiles (8 tokens) per warp
-  constexpr int NBW = NB / DS;       // PV blocks per warp
-  constexpr int NTO = NT8 / DS;      // O N-tiles per warp
   const int G = a.group, T = a.tokens;
   const long long head0 = (long long)b * a.num_q_heads + (long long)kvh * G;
   const int NWT = C::NW * 32;
-  // warp roles: head group, 16-token slice, part of head_dim (pairs are adjacent warps)
-  const int hg = pw / (4 * DS), ws = (pw % (4 * DS)) / DS, dh = pw % DS;
-  const int pair = (pipe * HG + hg) * 4 + ws;
-  const uint32_t xbar = smem_u32(smem) + C::XB_OFF + pair * 16;   // [pair][2] score exchange
-  float4* const xs = reinterpret_cast<float4*>(smem + C::XS_OFF) + pair * 2 * 2 * 32;   // [2 buf][2 half][32]
+  const int hg = pw >> 2, ws = pw & 3;               // head group, 16-token slice
 
   hmq.store(smem + C::QF_OFF, smem + C::SD_OFF);
-  if (DS > 1 && tid < C::NP * HG * 4 * 2) mbar_init(smem_u32(smem) + C::XB_OFF + tid * 8, 2);
-  if (DS > 1) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   asm volatile("bar.sync 1, %0;" ::"r"(C::THREADS) : "memory");
   // fused advance: the CTA's ticket, taken after the last CTA-wide barrier before the loop
   if (take_ticket && warp == C::NW - 1 && lane == 0) ticket();
@@ -152,25 +139,34 @@ __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int 
   const int r = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, mr = lane & 7;            // ldmatrix address roles
   const uint4* qf = reinterpret_cast<const uint4*>(smem + C::QF_OFF) + hg * QS * 32 + lane;
-  const float2* sdp = reinterpret_cast<const float2*>(smem + C::SD_OFF) + hg * NB * 8 + r;
+  const float4* sdp = reinterpret_cast<const float4*>(smem + C::SD_OFF) + hg * NB * 8 + r;
   uint8_t* const ring = smem + pipe * C::PRING;
   const int va = 16 * hg + r, vb = va + 8;           // this lane's rows (virtual heads)
   const int lim_a = L - T + 1 + va % T, lim_b = L - T + 1 + vb % T;   // causal limits (T > 1)
-  // the slice's block scales as f32: K [NB][16 tokens], then V [NBW][16 tokens]
-  float* const scw = reinterpret_cast<float*>(smem + C::SC_OFF) + warp * (NB + NBW) * 16;
-
-  float o[NTO][4];   // O N-tile jl = 4 * (block - dh * NBW) + 2 * chunk + parity
+  // the slice's block scales as f32: K [NB][16 tokens], then V [NB][16 tokens]
+  float* const scw = reinterpret_cast<float*>(smem + C::SC_OFF) + warp * 2 * NB * 16;
+  // Per-lane byte offsets of the ldmatrix rows inside a stage's K or V rows (128-byte
+  // swizzle: 16-byte chunk x of row t sits at (x >> 3) * 64 * 128 + t * 128 + ((x ^ t) & 7) * 16,
+  // and t & 7 = mr for every row a lane addresses): row t0 + 8 (mi >> 1) + mr, chunk
+  // 2 bb + (mi & 1), one offset per bb & 3
+  uint32_t roff[4];
 #pragma unroll
-  for (int j = 0; j < NTO; ++j)
+  for (int e = 0; e < 4; ++e)
+    roff[e] = (t0 + 8 * (mi >> 1) + mr) * 128 + ((((2 * e + (mi & 1)) ^ mr) & 7) << 4);
+  static_assert(C::KRB == D && C::VRB == D && D >= 128, "q8_0 rows of at least 128 bytes");
+
+  float o[NT8][4];   // O N-tile j = 4 * block + 2 * chunk + parity
+#pragma unroll
+  for (int j = 0; j < NT8; ++j)
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[j][k] = 0.0f;
+  // running max of rows r, r + 8 (log2 units), and their sums and O in units of
+  // 2^(E - kPScale) (E: running power-of-two bound of this warp's V scales)
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
-  int E = -100;                                       // running V-scale exponent bound
+  int E = -100;
   const float qk_mul = a.qk_scale_log2;
   bool timed_out = false;
   const int wlim = a.wait_limit;
-  int xb = 0;                                         // exchange buffer and its phases
-  uint32_t xph = 0u;
 
   int s = 0;
   uint32_t ph = 0u;
@@ -182,134 +178,92 @@ __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int 
     const int pos_w = (vchunk + tile * nvc) * kT + t0;
     const int n_valid = stage_ok[s] != 0 ? max(0, min(16, L - pos_w)) : 0;
     if (n_valid > 0) {
-      const bool partial = n_valid < 16;
-      const bool causal = T > 1 && pos_w + 16 > L - T + 1;
       const uint32_t kst = sring + s * C::STAGE, vst = kst + C::V_OFF;
       const uint8_t* ksc = ring + s * C::STAGE + C::KSC_OFF;
       const uint8_t* vsc = ring + s * C::STAGE + C::VSC_OFF;
 
-      // ---------------- block scales to f32 (K of this warp's QK tokens, V of its blocks);
-      // V scales of tokens past the end are zeroed (their stage bytes are not data), which
+      // ---------------- block scales to f32: lane (t, h) converts blocks h NB/2 .. of token
+      // t; V scales of tokens past the end are zeroed (their stage bytes are not data), which
       // also keeps them out of E
       uint32_t vmax = 0u;   // largest V scale bit pattern seen by this lane (scales are >= 0)
       {
-        constexpr int KTOK = 8 * NTQ, KLPT = 32 / KTOK, KPL = NB / KLPT;   // K: lanes per token, values per lane
-        const int kt = (DS > 1 ? 8 * dh : 0) + lane / KLPT, kb0 = (lane % KLPT) * KPL;
-        constexpr int VPL = NBW / 2;                                     // V: 2 lanes per token
-        const int vt = lane >> 1, vb0 = (lane & 1) * VPL;
-        uint32_t kw[KPL / 2], vw[VPL / 2];
+        constexpr int PL = NB / 2;                     // values per lane (2 lanes per token)
+        const int tt = lane >> 1, b0 = (lane & 1) * PL;
+        uint32_t kw[PL / 2], vw[PL / 2];
 #pragma unroll
-        for (int u = 0; u < KPL / 2; ++u)
-          kw[u] = *reinterpret_cast<const uint32_t*>(ksc + (t0 + kt) * NB * 2 + (kb0 + 2 * u) * 2);
-#pragma unroll
-        for (int u = 0; u < VPL / 2; ++u)
-          vw[u] = *reinterpret_cast<const uint32_t*>(vsc + (t0 + vt) * NB * 2 + (dh * NBW + vb0 + 2 * u) * 2);
-#pragma unroll
-        for (int u = 0; u < KPL / 2; ++u) {
-          const float2 f = unpack2<false>(kw[u]);
-          scw[(kb0 + 2 * u) * 16 + kt] = f.x;
-          scw[(kb0 + 2 * u + 1) * 16 + kt] = f.y;
+        for (int u = 0; u < PL / 2; ++u) {
+          kw[u] = *reinterpret_cast<const uint32_t*>(ksc + (t0 + tt) * NB * 2 + (b0 + 2 * u) * 2);
+          vw[u] = *reinterpret_cast<const uint32_t*>(vsc + (t0 + tt) * NB * 2 + (b0 + 2 * u) * 2);
         }
-        const bool tv = vt < n_valid;
 #pragma unroll
-        for (int u = 0; u < VPL / 2; ++u) {
+        for (int u = 0; u < PL / 2; ++u) {
+          const float2 f = unpack2<false>(kw[u]);
+          scw[(b0 + 2 * u) * 16 + tt] = f.x;
+          scw[(b0 + 2 * u + 1) * 16 + tt] = f.y;
+        }
+        const bool tv = tt < n_valid;
+#pragma unroll
+        for (int u = 0; u < PL / 2; ++u) {
           const uint32_t x = tv ? vw[u] : 0u;
           vmax = max(vmax, max(x & 0xffffu, x >> 16));
           const float2 f = unpack2<false>(x);
-          scw[(NB + vb0 + 2 * u) * 16 + vt] = f.x;
-          scw[(NB + vb0 + 2 * u + 1) * 16 + vt] = f.y;
+          scw[(NB + b0 + 2 * u) * 16 + tt] = f.x;
+          scw[(NB + b0 + 2 * u + 1) * 16 + tt] = f.y;
         }
       }
       __syncwarp();
       const uint32_t vmax_w = __reduce_max_sync(0xffffffffu, vmax);
       const int ex_w = vmax_w ? max((int)(vmax_w >> 10), 1) - 14 : -127;   // this warp's V scales < 2^ex_w
 
-      // ---------------- QK^T: S rows r, r + 8; columns tokens 8 nt + 2c (+1)
-      float sc[2][4];
+      // ---------------- QK^T: S (unscaled) as pairs: sc[nt][0] rows r, sc[nt][1] rows r + 8,
+      // columns tokens 8 nt + 2c, 8 nt + 2c + 1
+      float2 sc[2][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sc[nt][k] = 0.0f;
-      if constexpr (DS == 1) {
+      for (int bb = 0; bb < NB; ++bb) {
+        uint32_t w0, w1, w2, w3;
+        // matrices: (tok 0-7, chunk 2bb), (tok 0-7, chunk 2bb+1), (tok 8-15, 2bb), (tok 8-15, 2bb+1)
+        ldsm_x4(kst + roff[bb & 3] + (bb >> 2) * (kT * 128), w0, w1, w2, w3);
+        w0 ^= 0x80808080u; w1 ^= 0x80808080u; w2 ^= 0x80808080u; w3 ^= 0x80808080u;
+        const uint4 qa = qf[(2 * bb) * 32], qb = qf[(2 * bb + 1) * 32];
+        const uint32_t fa[4] = {qa.x, qa.y, qa.z, qa.w}, fb[4] = {qb.x, qb.y, qb.z, qb.w};
+        float cb[2][4];
 #pragma unroll
-        for (int bb = 0; bb < NB; ++bb) {
-          uint32_t w0, w1, w2, w3;
-          // matrices: (tok 0-7, chunk 2bb), (tok 0-7, chunk 2bb+1), (tok 8-15, 2bb), (tok 8-15, 2bb+1)
-          ldsm_x4(row_chunk<C::KRB>(kst, t0 + (mi >> 1) * 8 + mr, 2 * bb + (mi & 1)), w0, w1, w2, w3);
-          w0 ^= 0x80808080u; w1 ^= 0x80808080u; w2 ^= 0x80808080u; w3 ^= 0x80808080u;
-          const uint4 qa = qf[(2 * bb) * 32], qb = qf[(2 * bb + 1) * 32];
-          const uint32_t fa[4] = {qa.x, qa.y, qa.z, qa.w}, fb[4] = {qb.x, qb.y, qb.z, qb.w};
-          const float2 sd = sdp[bb * 8];
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t x0 = nt ? w2 : w0, x1 = nt ? w3 : w1;
-            float cb[4] = {sd.x, sd.x, sd.y, sd.y};
-            mma16816<false>(cb, fa, i8pair_raw(x0, 0x4140), i8pair_raw(x0, 0x4342));
-            mma16816<false>(cb, fb, i8pair_raw(x1, 0x4140), i8pair_raw(x1, 0x4342));
-            // tokens 8 nt + 2c, 8 nt + 2c + 1: S += d_k * block dot, as f32 pairs
-            const float2 dk = *reinterpret_cast<const float2*>(scw + bb * 16 + 8 * nt + 2 * c);
-            const float2 s01 = __ffma2_rn(dk, make_float2(cb[0], cb[1]), make_float2(sc[nt][0], sc[nt][1]));
-            const float2 s23 = __ffma2_rn(dk, make_float2(cb[2], cb[3]), make_float2(sc[nt][2], sc[nt][3]));
-            sc[nt][0] = s01.x; sc[nt][1] = s01.y; sc[nt][2] = s23.x; sc[nt][3] = s23.y;
-          }
+        for (int nt = 0; nt < 2; ++nt) {
+          const float4 sd = sdp[bb * 8];
+          cb[nt][0] = sd.x; cb[nt][1] = sd.y; cb[nt][2] = sd.z; cb[nt][3] = sd.w;
         }
-      } else {
-        // this warp's N-tile dh, two blocks per ldmatrix: (tok, chunk 4bp), ..., (tok, chunk 4bp + 3)
-        float sw[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // first k-steps of both N-tiles, then second k-steps
+        mma16816<false>(cb[0], fa, i8pair_raw(w0, 0x4140), i8pair_raw(w0, 0x4342));
+        mma16816<false>(cb[1], fa, i8pair_raw(w2, 0x4140), i8pair_raw(w2, 0x4342));
+        mma16816<false>(cb[0], fb, i8pair_raw(w1, 0x4140), i8pair_raw(w1, 0x4342));
+        mma16816<false>(cb[1], fb, i8pair_raw(w3, 0x4140), i8pair_raw(w3, 0x4342));
 #pragma unroll
-        for (int bp = 0; bp < NB / 2; ++bp) {
-          uint32_t wk[4];
-          ldsm_x4(row_chunk<C::KRB>(kst, t0 + 8 * dh + mr, 4 * bp + mi), wk[0], wk[1], wk[2], wk[3]);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int bb = 2 * bp + h;
-            const uint32_t x0 = wk[2 * h] ^ 0x80808080u, x1 = wk[2 * h + 1] ^ 0x80808080u;
-            const uint4 qa = qf[(2 * bb) * 32], qb = qf[(2 * bb + 1) * 32];
-            const uint32_t fa[4] = {qa.x, qa.y, qa.z, qa.w}, fb[4] = {qb.x, qb.y, qb.z, qb.w};
-            const float2 sd = sdp[bb * 8];
-            float cb[4] = {sd.x, sd.x, sd.y, sd.y};
-            mma16816<false>(cb, fa, i8pair_raw(x0, 0x4140), i8pair_raw(x0, 0x4342));
-            mma16816<false>(cb, fb, i8pair_raw(x1, 0x4140), i8pair_raw(x1, 0x4342));
-            const float2 dk = *reinterpret_cast<const float2*>(scw + bb * 16 + 8 * dh + 2 * c);
-            const float2 s01 = __ffma2_rn(dk, make_float2(cb[0], cb[1]), make_float2(sw[0], sw[1]));
-            const float2 s23 = __ffma2_rn(dk, make_float2(cb[2], cb[3]), make_float2(sw[2], sw[3]));
-            sw[0] = s01.x; sw[1] = s01.y; sw[2] = s23.x; sw[3] = s23.y;
-          }
-        }
-        // trade score halves with the pair's other warp
-        xs[(xb * 2 + dh) * 32 + lane] = make_float4(sw[0], sw[1], sw[2], sw[3]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(xbar + 8 * xb);
-        if (!mbar_wait_warp(xbar + 8 * xb, (xph >> xb) & 1u, wlim)) {
-          timed_out = true;
-          break;
-        }
-        const float4 ot = xs[(xb * 2 + (dh ^ 1)) * 32 + lane];
-        xph ^= 1u << xb;
-        xb ^= 1;
-        const float own[4] = {sw[0], sw[1], sw[2], sw[3]}, oth[4] = {ot.x, ot.y, ot.z, ot.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          sc[0][k] = dh == 0 ? own[k] : oth[k];
-          sc[1][k] = dh == 0 ? oth[k] : own[k];
+        for (int nt = 0; nt < 2; ++nt) {
+          // tokens 8 nt + 2c, 8 nt + 2c + 1: S += d_k * block dot, as f32 pairs
+          const float2 dk = *reinterpret_cast<const float2*>(scw + bb * 16 + 8 * nt + 2 * c);
+          sc[nt][0] = __ffma2_rn(dk, make_float2(cb[nt][0], cb[nt][1]), sc[nt][0]);
+          sc[nt][1] = __ffma2_rn(dk, make_float2(cb[nt][2], cb[nt][3]), sc[nt][1]);
         }
       }
+      if (n_valid < 16 || (T > 1 && pos_w + 16 > L - T + 1)) {
+        // tokens past the end, and the causal limit of each query token
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          sc[nt][k] *= qk_mul;
-          if (partial || causal) {
-            const int tok = 8 * nt + 2 * c + (k & 1);
-            const int lim = (k >> 1) ? lim_b : lim_a;
-            if (tok >= n_valid || (causal && pos_w + tok >= lim)) sc[nt][k] = -INFINITY;
+          for (int hr = 0; hr < 2; ++hr) {
+            const int tok = 8 * nt + 2 * c, lim = hr ? lim_b : lim_a;
+            float2& x = sc[nt][hr];
+            if (tok >= n_valid || pos_w + tok >= lim) x.x = -INFINITY;
+            if (tok + 1 >= n_valid || pos_w + tok + 1 >= lim) x.y = -INFINITY;
           }
-        }
+      }
 
-      // ---------------- lazy online softmax, per row (the same in both warps of a pair;
-      // E is each warp's own)
-      const float lma = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-      const float lmb = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      // ---------------- lazy online softmax, per row.  Scores in log2 units are s * qk_mul
+      // (qk_mul > 0).
+      const float lma = fmaxf(fmaxf(sc[0][0].x, sc[0][0].y), fmaxf(sc[1][0].x, sc[1][0].y)) * qk_mul;
+      const float lmb = fmaxf(fmaxf(sc[0][1].x, sc[0][1].y), fmaxf(sc[1][1].x, sc[1][1].y)) * qk_mul;
       const bool over = (lma > m_a + kLazy) || (lmb > m_b + kLazy) || (ex_w > E);
       if (__any_sync(0xffffffffu, over)) {
         float xa = lma, xb2 = lmb;
@@ -319,86 +273,72 @@ __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int 
           xb2 = fmaxf(xb2, __shfl_xor_sync(0xffffffffu, xb2, off));
         }
         const int E_new = max(E, ex_w);
-        // the reference max moves only past the lazy margin (the same decision in both
-        // warps of a pair: it depends on the scores alone)
+        // the reference max of a row moves only past the lazy margin
         const float na = xa > m_a + kLazy ? fmaxf(m_a, xa) : m_a;
         const float nb = xb2 > m_b + kLazy ? fmaxf(m_b, xb2) : m_b;
         const float e2 = __uint_as_float((uint32_t)(127 + E - E_new) << 23);  // 2^(E - E_new)
-        float fa = (na == -INFINITY) ? 1.0f : fast_exp2(m_a - na);
-        float fb = (nb == -INFINITY) ? 1.0f : fast_exp2(m_b - nb);
+        const float fa = ((na == -INFINITY) ? 1.0f : fast_exp2(m_a - na)) * e2;
+        const float fb = ((nb == -INFINITY) ? 1.0f : fast_exp2(m_b - nb)) * e2;
         l_a *= fa;
         l_b *= fb;
-        fa *= e2;
-        fb *= e2;
 #pragma unroll
-        for (int j = 0; j < NTO; ++j) {
+        for (int j = 0; j < NT8; ++j) {
           o[j][0] *= fa; o[j][1] *= fa; o[j][2] *= fb; o[j][3] *= fb;
         }
         m_a = na;
         m_b = nb;
         E = E_new;
       }
-      // a row whose every score so far was masked keeps m = -inf: its p are 0
-      const float ra = m_a == -INFINITY ? 0.0f : m_a, rb = m_b == -INFINITY ? 0.0f : m_b;
-      float p[2][4];
+      // p * 2^(kPScale - E) = 2^(s qk_mul - m + kPScale - E); a row whose every score so far
+      // was masked keeps m = -inf and its p are 0
+      const float ba = (float)(kPScale - E) - (m_a == -INFINITY ? 0.0f : m_a);
+      const float bb2 = (float)(kPScale - E) - (m_b == -INFINITY ? 0.0f : m_b);
+      float2 p[2][2];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        p[nt][0] = fast_exp2(sc[nt][0] - ra);
-        p[nt][1] = fast_exp2(sc[nt][1] - ra);
-        p[nt][2] = fast_exp2(sc[nt][2] - rb);
-        p[nt][3] = fast_exp2(sc[nt][3] - rb);
+        p[nt][0] = make_float2(fast_exp2(fmaf(sc[nt][0].x, qk_mul, ba)), fast_exp2(fmaf(sc[nt][0].y, qk_mul, ba)));
+        p[nt][1] = make_float2(fast_exp2(fmaf(sc[nt][1].x, qk_mul, bb2)), fast_exp2(fmaf(sc[nt][1].y, qk_mul, bb2)));
       }
-      l_a += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
-      l_b += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
-      const float pscale = __uint_as_float((uint32_t)(127 + kPScale - E) << 23);   // 2^(kPScale - E)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) p[nt][k] *= pscale;
+      l_a += (p[0][0].x + p[0][0].y) + (p[1][0].x + p[1][0].y);
+      l_b += (p[0][1].x + p[0][1].y) + (p[1][1].x + p[1][1].y);
 
-      // ---------------- PV over this warp's blocks
+      // ---------------- PV, block by block
 #pragma unroll
-      for (int bi = 0; bi < NBW; ++bi) {
-        const int bb = dh * NBW + bi;
+      for (int bb = 0; bb < NB; ++bb) {
         // A fragment: a0 (row r, tok 2c | 2c+1), a1 (row r+8, ...), a2 (row r, tok 2c+8 | 2c+9), a3
         uint32_t ahi[4], alo[4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const float2 dv = *reinterpret_cast<const float2*>(scw + (NB + bi) * 16 + 8 * nt + 2 * c);
-          const float2 pa = __fmul2_rn(make_float2(p[nt][0], p[nt][1]), dv);
-          const float2 pb = __fmul2_rn(make_float2(p[nt][2], p[nt][3]), dv);
+          const float2 dv = *reinterpret_cast<const float2*>(scw + (NB + bb) * 16 + 8 * nt + 2 * c);
+          const float2 pa = __fmul2_rn(p[nt][0], dv);
+          const float2 pb = __fmul2_rn(p[nt][1], dv);
           split2<false>(pa.x, pa.y, ahi[2 * nt], alo[2 * nt]);
           split2<false>(pb.x, pb.y, ahi[2 * nt + 1], alo[2 * nt + 1]);
         }
         uint32_t y0, y1, y2, y3;
         // matrices: (tok 0-7, chunk 2bb), (tok 0-7, chunk 2bb+1), (tok 8-15, 2bb), (tok 8-15, 2bb+1)
-        ldsm_x4_t(row_chunk<C::VRB>(vst, t0 + (mi >> 1) * 8 + mr, 2 * bb + (mi & 1)), y0, y1, y2, y3);
+        ldsm_x4_t(vst + roff[bb & 3] + (bb >> 2) * (kT * 128), y0, y1, y2, y3);
+        // B fragments of the block's four N-tiles (chunk h, even / odd elements): the
+        // even elements 2n of a chunk are bytes 0, 2 of each word, the odd ones bytes 1, 3
+        uint32_t bv[4][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t ya = (h ? y1 : y0) ^ 0x80808080u, yb = (h ? y3 : y2) ^ 0x80808080u;
-          // even elements 2n of the chunk (bytes 0, 2), odd elements 2n + 1 (bytes 1, 3)
-          const uint32_t be0 = hsub2_u32(i8pair_raw(ya, 0x4240), 0x64806480u);
-          const uint32_t be1 = hsub2_u32(i8pair_raw(yb, 0x4240), 0x64806480u);
-          const uint32_t bo0 = hsub2_u32(i8pair_raw(ya, 0x4341), 0x64806480u);
-          const uint32_t bo1 = hsub2_u32(i8pair_raw(yb, 0x4341), 0x64806480u);
-          float* oe = o[4 * bi + 2 * h];
-          float* oo = o[4 * bi + 2 * h + 1];
-          mma16816<false>(oe, ahi, be0, be1);
-          mma16816<false>(oe, alo, be0, be1);
-          mma16816<false>(oo, ahi, bo0, bo1);
-          mma16816<false>(oo, alo, bo0, bo1);
+          bv[2 * h][0] = hsub2_u32(i8pair_raw(ya, 0x4240), 0x64806480u);
+          bv[2 * h][1] = hsub2_u32(i8pair_raw(yb, 0x4240), 0x64806480u);
+          bv[2 * h + 1][0] = hsub2_u32(i8pair_raw(ya, 0x4341), 0x64806480u);
+          bv[2 * h + 1][1] = hsub2_u32(i8pair_raw(yb, 0x4341), 0x64806480u);
         }
+        // hi parts into the four accumulators, then lo parts (no accumulator twice in a row)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma16816<false>(o[4 * bb + n], ahi, bv[n][0], bv[n][1]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma16816<false>(o[4 * bb + n], alo, bv[n][0], bv[n][1]);
       }
     }
     // release the stage; the pipeline's last warp to release it refills it
     __syncwarp();
-    uint32_t last = 0u;
-    if (lane == 0) {
-      mbar_arrive(bar_empty + 8 * s);
-      last = atomicAdd(rcnt + s, 1u) == (unsigned)(C::PW - 1) ? 1u : 0u;
-      if (last) atomicExch(rcnt + s, 0u);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
+    const bool last = release_last(bar_empty + 8 * s, rcnt + s, lane, C::PW);
     if (last && tile + C::NS < n_tiles) {
       if (!mbar_wait_warp(bar_empty + 8 * s, ph, wlim)) {   // every release is in: no wait
         timed_out = true;
@@ -429,33 +369,32 @@ __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int 
     l_a += __shfl_xor_sync(0xffffffffu, l_a, off);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, off);
   }
-  const float oscale = __uint_as_float((uint32_t)(127 + E - kPScale) << 23);   // O true scale
+  const float oscale = __uint_as_float((uint32_t)(127 + E - kPScale) << 23);   // true scale of l and O
   float2* mlw = reinterpret_cast<float2*>(smem + C::ML_OFF);      // [NW][16] (m, l) per row
   float2* hml = mlw + C::NW * 16;                                 // [HG * 16] (M, l) of the CTA
   if (c == 0) {
-    mlw[warp * 16 + r] = make_float2(m_a, l_a);
-    mlw[warp * 16 + r + 8] = make_float2(m_b, l_b);
+    mlw[warp * 16 + r] = make_float2(m_a, l_a * oscale);
+    mlw[warp * 16 + r + 8] = make_float2(m_b, l_b * oscale);
   }
   // every warp reaches this barrier (a timed-out warp skips only its tiles); after it all
   // loops are done, so the rings are idle
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
-  // warps of head group g holding part d of head_dim: pipeline pp, slice w -> warp
-  // pp * PW + g * 4 DS + w DS + d (i = 4 pp + w)
+  // warps of head group g: pipeline pp, slice w -> warp pp * PW + 4 g + w (i = 4 pp + w)
   constexpr int GWARPS = 4 * C::NP;
-  auto gwarp = [&](int g, int i, int d) { return (i >> 2) * C::PW + g * 4 * DS + (i & 3) * DS + d; };
+  auto gwarp = [&](int g, int i) { return (i >> 2) * C::PW + 4 * g + (i & 3); };
   float Ma = -INFINITY, Mb = -INFINITY;
 #pragma unroll
   for (int i = 0; i < GWARPS; ++i) {
-    Ma = fmaxf(Ma, mlw[gwarp(hg, i, dh) * 16 + r].x);
-    Mb = fmaxf(Mb, mlw[gwarp(hg, i, dh) * 16 + r + 8].x);
+    Ma = fmaxf(Ma, mlw[gwarp(hg, i) * 16 + r].x);
+    Mb = fmaxf(Mb, mlw[gwarp(hg, i) * 16 + r + 8].x);
   }
-  if (ws == 0 && dh == 0 && (warp / C::PW) == 0 && c < 2) {
+  if (ws == 0 && (warp / C::PW) == 0 && c < 2) {
     // the CTA's sum for row r (c = 0) or r + 8 (c = 1) of this head group
     const int row = r + 8 * c;
     const float M = c ? Mb : Ma;
     float lsum = 0.0f;
     for (int i = 0; i < GWARPS; ++i) {
-      const float2 x = mlw[gwarp(hg, i, 0) * 16 + row];
+      const float2 x = mlw[gwarp(hg, i) * 16 + row];
       if (x.x != -INFINITY) lsum += fast_exp2(x.x - M) * x.y;
     }
     hml[16 * hg + row] = make_float2(M, lsum);
@@ -465,15 +404,14 @@ __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int 
     // N-tile: rows r (k = 0, 1) and r + 8 (k = 2, 3))
     const float fa = (m_a == -INFINITY) ? 0.0f : fast_exp2(m_a - Ma) * oscale;
     const float fb = (m_b == -INFINITY) ? 0.0f : fast_exp2(m_b - Mb) * oscale;
-    float4* ob = reinterpret_cast<float4*>(smem) + warp * NTO * 32 + lane;
+    float4* ob = reinterpret_cast<float4*>(smem) + warp * NT8 * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < NTO; ++j) ob[j * 32] = make_float4(o[j][0] * fa, o[j][1] * fa, o[j][2] * fb, o[j][3] * fb);
+    for (int j = 0; j < NT8; ++j) ob[j * 32] = make_float4(o[j][0] * fa, o[j][1] * fa, o[j][2] * fb, o[j][3] * fb);
   }
   asm volatile("bar.sync 1, %0;" ::"r"(NWT) : "memory");
   // Output float4 (group g, row half rh, block bb, chunk h, lane (r, c)): row r + 8 rh, elements
   // 32 bb + 16 h + 4c .. + 3 of head_dim, which are (k = 2 rh, 2 rh + 1) of the even N-tile
-  // j = 4 bb + 2 h and of the odd one j + 1 (elements 4c, 4c + 2 and 4c + 1, 4c + 3), held by
-  // the warps of part d = bb / NBW as their tiles j - 4 d NBW
+  // j = 4 bb + 2 h and of the odd one j + 1 (elements 4c, 4c + 2 and 4c + 1, 4c + 3)
   const float2* obuf = reinterpret_cast<const float2*>(smem);
   const bool direct = nv == 1 && !a.chunk_merge;   // the whole sequence is this chunk
   for (int t = tid; t < HG * 2 * (NT8 / 2) * 32; t += NWT) {
@@ -481,13 +419,13 @@ __device__ __forceinline__ bool hm_body(const DecodeArgs& a, uint8_t* smem, int 
     const int jp = rest % (NT8 / 2), rh = (rest / (NT8 / 2)) & 1, g = rest / NT8;
     const int row = (ln >> 2) + 8 * rh, v = 16 * g + row;
     if (v >= G) continue;
-    const int j = 2 * jp, d = (j >> 2) / NBW, jl = j - 4 * d * NBW;
+    const int j = 2 * jp;
     float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < GWARPS; ++i) {
-      const int w = gwarp(g, i, d);
-      const float2 e = obuf[((w * NTO + jl) * 32 + ln) * 2 + rh];
-      const float2 od = obuf[((w * NTO + jl + 1) * 32 + ln) * 2 + rh];
+      const int w = gwarp(g, i);
+      const float2 e = obuf[((w * NT8 + j) * 32 + ln) * 2 + rh];
+      const float2 od = obuf[((w * NT8 + j + 1) * 32 + ln) * 2 + rh];
       sum.x += e.x; sum.y += od.x; sum.z += e.y; sum.w += od.y;
     }
     const int dim = 16 * jp + 4 * (ln & 3);

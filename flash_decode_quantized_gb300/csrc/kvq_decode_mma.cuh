@@ -66,6 +66,24 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrival by lane 0 of the warp (predicated, no branch).
+__device__ __forceinline__ void mbar_arrive_lane0(uint32_t bar, int lane) {
+  asm volatile("{\n .reg .pred p;\n setp.eq.s32 p, %1, 0;\n @p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n"
+               ::"r"(bar), "r"(lane) : "memory");
+}
+// Release of a stage by one of `warps` warps: lane 0 arrives on the stage's empty barrier
+// and counts the release; true (in every lane) for the warp whose release is the last
+// one, which also returns the count to zero.
+__device__ __forceinline__ bool release_last(uint32_t bar_empty, unsigned* cnt, int lane, int warps) {
+  uint32_t old = 0u;
+  asm volatile("{\n .reg .pred p;\n setp.eq.s32 p, %2, 0;\n"
+               " @p mbarrier.arrive.shared::cta.b64 _, [%1];\n"
+               " @p atom.shared::cta.add.u32 %0, [%3], 1;\n}\n"
+               : "+r"(old) : "r"(bar_empty), "r"(lane), "r"((uint32_t)__cvta_generic_to_shared(cnt)) : "memory");
+  const bool last = __shfl_sync(0xffffffffu, old, 0) == (uint32_t)(warps - 1);
+  if (last && lane == 0) atomicExch(cnt, 0u);
+  return last;
+}
 __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -73,6 +91,22 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(done) : "r"(bar), "r"(parity) : "memory");
   return done;
+}
+// try_wait that may suspend the warp for up to 1 us (it resumes as soon as the phase
+// completes): fewer retries of a long wait.
+__device__ __forceinline__ uint32_t mbar_try_suspend(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done;
+}
+// mbar_wait_warp with suspending tries (each try waits up to 1 us).
+__device__ __forceinline__ bool mbar_wait_warp_s(uint32_t bar, uint32_t parity, int limit) {
+  for (int it = 0; it < limit; ++it)
+    if (__all_sync(0xffffffffu, mbar_try_suspend(bar, parity))) return true;
+  return false;
 }
 // Bounded wait, by every lane of a warp, for the phase of parity `parity` to complete.
 // Each lane observes the completion itself (acquire); the result is warp-uniform, so
@@ -251,11 +285,9 @@ __device__ __forceinline__ void load_scale_words(const uint8_t* base, int t, uin
 template <int KC, int VC, int D, int GW, int HG>
 struct Cfg {
   // Heads on M (GW == 16, kvq_decode_hm.cuh): warps of 16 query rows x 16 tokens, HG row
-  // groups per pipeline; at head_dim 256 the two warps of a slice pair split head_dim
-  // (DS = 2) so that a warp's O accumulators take 64 registers and 16 warps fit an SM.
+  // groups per pipeline.
   static constexpr bool HM = GW == 16;
-  static constexpr int DS = HM && D == 256 ? 2 : 1;
-  static constexpr int PW = 4 * HG * DS;                  // warps per pipeline (4 per head group)
+  static constexpr int PW = 4 * HG;                       // warps per pipeline (4 per head group)
   static constexpr int NPV = GW <= 4 ? 1 : 2;             // PV n-tiles per warp
   static constexpr bool KBF = KC == KVQ_CODEC_BF16;       // MMA type of QK^T
   static constexpr bool VBF = VC == KVQ_CODEC_BF16;       // MMA type of PV
@@ -279,7 +311,8 @@ struct Cfg {
   // pipelines in shared memory, so a split has a quarter as many partials as with one
   // pipeline per CTA.  Otherwise one pipeline per CTA and register use sets occupancy.
   static constexpr bool PACK = HG == 1 && GW <= 4 && D <= 128 && 2 * STAGE + 6 * 1024 <= 56 * 1024;
-  // HM: two pipelines per CTA for one row group, one for two
+  // HM: two pipelines per CTA for one row group (8 warps per SM at up to 255 registers:
+  // the O accumulators alone take D / 2), one for two
   static constexpr int NP = PACK ? 4 : (HM && HG == 1) ? 2 : 1;   // pipelines per CTA
   // the lean tile loop (see decode_cta) serves warps of at most 4 heads at D <= 128
   static constexpr bool LEAN = HG == 1 && GW <= 4 && D <= 128;
@@ -287,12 +320,12 @@ struct Cfg {
   static constexpr int THREADS = NW * 32;
   static constexpr int MINB = 1;
   // ring depth per pipeline: as many stages (2..4) as fit the per-pipeline budget
-  static constexpr int SMEM_BUDGET = HM ? (DS > 1 ? (HG > 1 ? 140 * 1024 : 70 * 1024) : HG > 1 ? 204 * 1024 : 104 * 1024 + 2048)
+  static constexpr int SMEM_BUDGET = HM ? (HG > 1 ? 204 * 1024 : 104 * 1024 + 2048)
                                      : HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : PACK ? 54 * 1024 : 70 * 1024;
   static constexpr int NS0 = (SMEM_BUDGET - 2048) / STAGE;
   static constexpr int NS = NS0 > 4 ? 4 : (NS0 < 2 ? 2 : NS0);
   static constexpr int PRING = NS * STAGE;                // one pipeline's ring
-  static constexpr int OBUF = NW * (HM ? 16 * D / DS : 8 * D) * 4;   // merge buffer (reuses the rings)
+  static constexpr int OBUF = NW * (HM ? 16 : 8) * D * 4;   // merge buffer (reuses the rings)
   static constexpr int RING = NP * PRING > OBUF ? NP * PRING : OBUF;
   static constexpr int BAR_OFF = RING;                    // [NP][full NS | empty NS] mbarriers
   static constexpr int OK_OFF = BAR_OFF + NP * 2 * NS * 8;  // [NP][NS] "tile is valid" flags, then a flag
@@ -303,17 +336,12 @@ struct Cfg {
   static constexpr int RC_OFF = PG_OFF + NP * 64 * 4;     // [NP][NS] releases counted per stage
   static constexpr int LI_OFF = RC_OFF + 16 * 4;          // [NP][NS] last tile issued into each stage
   // HM: q in MMA fragment order [HG][D/16][32 lanes] x 16 bytes, then the QK seeds
-  // [HG][NB][8] f32x2 (rows r, r + 8)
+  // [HG][NB][8] f32x4 (rows r, r, r + 8, r + 8)
   static constexpr int QF_OFF = LI_OFF + 16 * 4;
   static constexpr int SD_OFF = QF_OFF + (HM ? HG * (D / 16) * 512 : 0);
-  // HM: per warp, the f32 block scales of its 16-token slice, K [NB][16] then V [NB/DS][16];
-  // with DS = 2 the score exchange of each slice pair, [pair][2 buffers][2 halves][32 lanes]
-  // float4, and its mbarriers [pair][2]
-  static constexpr int SC_OFF = SD_OFF + (HM ? HG * NB * 64 : 0);
-  static constexpr int XS_OFF = SC_OFF + (HM ? NW * (NB + NB / DS) * 16 * 4 : 0);
-  static constexpr int NPAIRS = HM && DS > 1 ? NP * HG * 4 : 0;
-  static constexpr int XB_OFF = XS_OFF + NPAIRS * 2 * 2 * 32 * 16;
-  static constexpr int SMEM = XB_OFF + NPAIRS * 16 + 1024;   // +1024: alignment
+  // HM: per warp, the f32 block scales of its 16-token slice, K [NB][16] then V [NB][16]
+  static constexpr int SC_OFF = SD_OFF + (HM ? HG * NB * 128 : 0);
+  static constexpr int SMEM = SC_OFF + (HM ? NW * 2 * NB * 16 * 4 : 0) + 1024;   // +1024: alignment
   static constexpr uint32_t K_TX = kT * KRB + (KQ ? kT * NB * 2 : 0);
   static constexpr uint32_t V_TX = kT * VRB + (VQ ? kT * NB * 2 : 0);
   static constexpr int QSTEPS = D / 16;                   // k16 steps of QK^T
@@ -685,14 +713,16 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   // Lane 0 of the pipeline's first warp issues its copies: the first NS tiles up front,
   // then tile k + NS into stage k % NS as soon as every warp of the pipeline has released
   // tile k.
-  auto issue_tile = [&](int tile, int page) {
+  // Copies of the pipeline's local tile `tile` (into stage tile % NS), which is the sequence's
+  // 64-token tile g.
+  auto issue_at = [&](int tile, int g, int page) {
     const int s = tile % C::NS;
     // fault injection (tests of the timeout path): the first pipeline never issues this
     // tile, neither its copies nor an arrival, so its consumers' bounded waits run out on a
     // stage with nothing in flight
     if (vchunk == 0 && tile == a.skip_tile) return;
     last_issued[s] = tile;
-    const int pos0 = (vchunk + tile * nvc) * kT;
+    const int pos0 = g * kT;
     const int row0 = pos0 % P;
     const uint32_t full = bar_full + 8 * s;
     // the flag is published to the warps by the mbarrier phase that completes below
@@ -725,6 +755,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       bulk_load_ef(st + C::VSC_OFF, src, kT * C::NB * 2, full, pol);
     }
   };
+  // local tile t is the sequence's tile vchunk + t * nvc
+  auto issue_tile = [&](int tile, int page) { issue_at(tile, vchunk + tile * nvc, page); };
   // Page of tile t (t >= pb, nondecreasing over calls), by all of the producer warp.  Crossing a
   // 32-tile boundary shifts the window and starts the loads for the batch after next,
   // 32 tiles before they are needed.
