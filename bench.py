@@ -784,6 +784,26 @@ def run_extras(torch, kvq, args, flush, peak):
         out.append(row)
         del layer
         torch.cuda.empty_cache()
+    # the same chunk at the long-context shape (GQA 16:1, head_dim 256)
+    ptimes = {}
+    for arm in ("f16/f16", "q8_0/q8_0"):
+        layer = Layer(kvq, torch, WORKLOADS["longctx"], arm, [depth + T], 0, seed=94)
+        qp = torch.randn((1, T, layer.hq, layer.d), device="cuda").to(torch.bfloat16)
+        outp = torch.empty((1, T, layer.hq, layer.d), dtype=torch.float32, device="cuda")
+
+        def pf2(layer=layer, qp=qp, outp=outp):
+            kvq.kvq_prefill_attention(qp, layer.k_store, layer.v_store, layer.seq_lens, layer.page_table, out=outp)
+        time_decode_only(torch, layer, flush, 2, pf2)
+        ms = statistics.median(time_decode_only(torch, layer, flush, 6, pf2))
+        ptimes[arm] = ms
+        flops = 4.0 * layer.d * layer.hq * sum(depth + i + 1 for i in range(T))
+        row = {"workload": "prefill_attention_longctx", "depth": depth, "chunk_tokens": T, "codec": arm,
+               "us": round(ms * 1e3, 1), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+        if arm == "q8_0/q8_0":
+            row["vs_f16_time"] = round(ms / ptimes["f16/f16"], 3)
+        out.append(row)
+        del layer
+        torch.cuda.empty_cache()
     # speculative-draft verification: T query tokens per sequence in one decode, against
     # T single-token decodes of the same cache (8B-class layer, 65536 tokens, q8_0 K+V)
     layer = Layer(kvq, torch, WORKLOADS["layer8b"], "q8_0/q8_0", [65536], 0, seed=91)
@@ -798,6 +818,21 @@ def run_extras(torch, kvq, args, flush, peak):
                     "us": round(ms * 1e3, 2), "single_token_us": round(one * 1e3, 2),
                     "vs_T_single_decodes": round(ms / (T * one), 3),
                     "gbs": round(layer.kv_bytes() / (ms * 1e-3) / 1e9, 1)})
+    del layer
+    torch.cuda.empty_cache()
+    # the same at long context (GQA 16:1, D = 256, 131072 tokens, q8_0 K+V): two draft tokens
+    # are 32 query rows per KV head
+    layer = Layer(kvq, torch, WORKLOADS["longctx"], "q8_0/q8_0", [131072], 0, seed=93)
+    layer.prepare(args.variant, 0)
+    time_decode_only(torch, layer, flush, 3)
+    one = statistics.median(time_decode_only(torch, layer, flush, 10))
+    fn = (lambda: layer.multi(2))
+    time_decode_only(torch, layer, flush, 3, fn)
+    ms = statistics.median(time_decode_only(torch, layer, flush, 10, fn))
+    out.append({"workload": "spec_verify_longctx", "kv_len": 131072, "codec": "q8_0/q8_0", "query_tokens": 2,
+                "us": round(ms * 1e3, 2), "single_token_us": round(one * 1e3, 2),
+                "vs_T_single_decodes": round(ms / (2 * one), 3),
+                "gbs": round(layer.kv_bytes() / (ms * 1e-3) / 1e9, 1)})
     del layer
     torch.cuda.empty_cache()
     from workloads import ragged_lengths

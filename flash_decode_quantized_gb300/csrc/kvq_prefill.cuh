@@ -49,7 +49,13 @@ struct PCfg {
   static constexpr int NS = NS0 > 3 ? 3 : (NS0 < 2 ? 2 : NS0);
   static constexpr int BAR_OFF = NS * STAGE;
   static constexpr int OK_OFF = BAR_OFF + 2 * NS * 8;
-  static constexpr int SMEM = OK_OFF + 32 + 1024;
+  // head_dim 256: the warps' Q fragments live in shared memory ([warp][k-step][32 lanes] x 16
+  // bytes) instead of registers, which the 16 x 256 O accumulators (128 per thread) need
+  static constexpr bool QSM = D == 256;
+  static constexpr int QF_OFF = OK_OFF + 32;
+  // ... and the QK seeds ([warp][block][32 lanes] x float2)
+  static constexpr int SD_OFF = QF_OFF + (QSM ? kWarps * KSTEPS * 512 : 0);
+  static constexpr int SMEM = SD_OFF + (QSM ? kWarps * NB * 256 : 0) + 1024;
   static constexpr uint32_t K_TX = kT * KRB + KSC, V_TX = kT * VRB + VSC;
 };
 
@@ -177,6 +183,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
   }
 
   // ---------------------------------------------------------------- Q fragments (A of QK)
+  // (with QSM only the seeds keep them: the fragments go to shared memory below)
   uint32_t qa[C::KSTEPS][4];
   {
     const __nv_bfloat16* qrow[2];
@@ -223,6 +230,29 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     seed[bb][1] = -bias * sB;
   }
   const float qk_mul = a.qk_scale_log2 * (KC == KVQ_CODEC_Q4S ? 2.0f : 1.0f);
+  uint4* const qfs = reinterpret_cast<uint4*>(smem + C::QF_OFF) + warp * C::KSTEPS * 32 + lane;
+  float2* const sds = reinterpret_cast<float2*>(smem + C::SD_OFF) + warp * C::NB * 32 + lane;
+  if constexpr (C::QSM) {
+#pragma unroll
+    for (int s = 0; s < C::KSTEPS; ++s) qfs[s * 32] = make_uint4(qa[s][0], qa[s][1], qa[s][2], qa[s][3]);
+#pragma unroll
+    for (int bb = 0; bb < C::NB; ++bb) sds[bb * 32] = make_float2(seed[bb][0], seed[bb][1]);
+    __syncwarp();
+  }
+  // QK seeds of block bb (rows g, g + 8)
+  auto seed_of = [&](int bb) -> float2 {
+    if constexpr (C::QSM) return sds[bb * 32];
+    else return make_float2(seed[bb][0], seed[bb][1]);
+  };
+  // A fragment of k-step ks
+  auto qfrag = [&](int ks, uint32_t* f) {
+    if constexpr (C::QSM) {
+      const uint4 v = qfs[ks * 32];
+      f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    } else {
+      f[0] = qa[ks][0]; f[1] = qa[ks][1]; f[2] = qa[ks][2]; f[3] = qa[ks][3];
+    }
+  };
 
   float o[C::ONT][4];
 #pragma unroll
@@ -259,14 +289,17 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
 #pragma unroll
           for (int bb = 0; bb < C::NB; ++bb) {
             float cb[4][4];
+            const float2 sdb = seed_of(bb);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-              cb[m][0] = seed[bb][0]; cb[m][1] = seed[bb][0];
-              cb[m][2] = seed[bb][1]; cb[m][3] = seed[bb][1];
+              cb[m][0] = sdb.x; cb[m][1] = sdb.x;
+              cb[m][2] = sdb.y; cb[m][3] = sdb.y;
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int ks = 2 * bb + half;
+              uint32_t qk[4];
+              qfrag(ks, qk);
               uint32_t y[4];
               // matrix m: tokens 8(4nq+m) .. +7; q8: chunk ks (16 dims); q4: chunk bb (32 dims)
               const int chunk = KC == KVQ_CODEC_Q8_0 ? ks : bb;
@@ -282,7 +315,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                   b0 = u4pair_half(half ? (y[m] >> 2) : (y[m] << 6));
                   b1 = u4pair_half(half ? (y[m] >> 6) : (y[m] << 2));
                 }
-                mma16816<false>(cb[m], qa[ks], b0, b1);
+                mma16816<false>(cb[m], qk, b0, b1);
               }
             }
             // scale by the tokens' block scales: columns 2*i4, 2*i4+1 of n-tile 4nq + m
@@ -302,12 +335,14 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
       } else {
 #pragma unroll
         for (int ks = 0; ks < C::KSTEPS; ++ks) {
+          uint32_t qk[4];
+          qfrag(ks, qk);
 #pragma unroll
           for (int np = 0; np < 4; ++np) {   // n-tiles 2np, 2np+1: matrices (n, k lo), (n, k hi), ...
             uint32_t y[4];
             ldsm_x4(row_chunk<C::KRB>(kst, 8 * (2 * np + (mi >> 1)) + mr, 2 * ks + (mi & 1)), y[0], y[1], y[2], y[3]);
-            mma16816<C::KBF>(sc[2 * np], qa[ks], y[0], y[1]);
-            mma16816<C::KBF>(sc[2 * np + 1], qa[ks], y[2], y[3]);
+            mma16816<C::KBF>(sc[2 * np], qk, y[0], y[1]);
+            mma16816<C::KBF>(sc[2 * np + 1], qk, y[2], y[3]);
           }
         }
       }
@@ -521,11 +556,10 @@ cudaError_t launch(const PrefillArgs& a, int batch, const CUtensorMap& tmk, cons
 template <int KC, int VC>
 cudaError_t launch_pair(const PrefillArgs& a, int batch, int head_dim, const CUtensorMap& tmk,
                         const CUtensorMap& tmv, cudaStream_t stream) {
-  // head_dim 256 would need O split across warps (its 16 x 256 accumulators alone take
-  // 128 registers per thread): not built
   switch (head_dim) {
     case 64: return launch<KC, VC, 64>(a, batch, tmk, tmv, stream);
     case 128: return launch<KC, VC, 128>(a, batch, tmk, tmv, stream);
+    case 256: return launch<KC, VC, 256>(a, batch, tmk, tmv, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -258,8 +258,9 @@ kvq_status kvq_flash_decode_multi(const void* q, const kvq_store* k_store, const
  *   q    device bf16 [batch][num_tokens][num_q_heads][head_dim] (16-byte aligned)
  *   out  device fp32 [batch][num_tokens][num_q_heads][head_dim]
  * One launch, no workspace: a CTA owns 64 (token, head) query rows of one KV head and
- * streams the KV prefix once.  Built for head_dim 64 and 128 and the pairs q8_0/q8_0,
- * q4s/q4s, q8_0/q4s, f16/f16, bf16/bf16; others give KVQ_ERR_UNSUPPORTED.  softmax_scale <= 0
+ * streams the KV prefix once.  Built for head_dim 64, 128 and 256 and the pairs of
+ * kvq_flash_decode's tensor-core kernel (bf16/bf16, f16/f16, q8_0/bf16, q8_0/q8_0, q4s/q4s,
+ * q8_0/q4s, q4s/q8_0, q4s/bf16); others give KVQ_ERR_UNSUPPORTED.  softmax_scale <= 0
  * selects 1/sqrt(head_dim).  Device faults as for kvq_flash_decode. */
 kvq_status kvq_prefill_attention(const void* q, const kvq_store* k_store, const kvq_store* v_store,
                                  const int32_t* seq_lens, const int32_t* page_table, int max_pages,

@@ -15,7 +15,8 @@ from workloads import f32_to_bf16_bits, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-PAIRS = [("q8_0", "q8_0"), ("q4s", "q4s"), ("q8_0", "q4s"), ("f16", "f16"), ("bf16", "bf16")]
+PAIRS = [("q8_0", "q8_0"), ("q4s", "q4s"), ("q8_0", "q4s"), ("f16", "f16"), ("bf16", "bf16"),
+         ("q8_0", "bf16"), ("q4s", "q8_0"), ("q4s", "bf16")]
 
 
 def run(inp, kc, vc, T, seed):
@@ -71,11 +72,20 @@ def test_prefill_chunk_longer_than_sequence_gives_zeros_for_blind_queries():
     assert_close(got, want, "short")
 
 
-def test_prefill_unsupported_shapes():
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q4s", "q8_0"), ("f16", "f16"), ("bf16", "bf16")])
+def test_prefill_head_dim_256(kc, vc):
+    # GQA 16:1 at head_dim 256 (the long-context shape), heavy-tailed channel-scaled values
+    inp = make_inputs([900, 70], 32, 2, 256, seed=209, dist="t3", channel_scaled=True)
+    got, want = run(inp, kc, vc, 70, seed=210)
+    assert_close(got, want, f"D=256 {kc}/{vc}")
+
+
+def test_prefill_unsupported_pair():
     k = kvq()
-    inp = make_inputs([100], 8, 2, 256, seed=209)
-    ks, vs = build_store(inp, "q8_0", "k"), build_store(inp, "q8_0", "v")
+    inp = make_inputs([100], 8, 2, 128, seed=211)
+    ks, vs = build_store(inp, "bf16", "k"), build_store(inp, "q8_0", "v")   # 16-bit K, quantized V
     _, seq, pt = device_inputs(inp)
-    q = torch.zeros((1, 4, 8, 256), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(k.KvqError):      # head_dim 256 is not built for prefill
+    q = torch.zeros((1, 4, 8, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(k.KvqError) as e:
         k.kvq_prefill_attention(q, ks, vs, seq, pt)
+    assert e.value.status == k.KVQ_ERR_UNSUPPORTED
