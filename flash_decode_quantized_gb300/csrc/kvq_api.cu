@@ -43,14 +43,14 @@ cudaError_t mma_launch_q4s_q8_0(const DecodeArgs&, int, const CUtensorMap&, cons
 cudaError_t mma_launch_q4s_bf16(const DecodeArgs&, int, const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 cudaError_t prefill_launch(int kc, int vc, const PrefillArgs& a, int batch, int head_dim,
                            const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream);
-int mma_occupancy_bf16_bf16(int, int, int*);
-int mma_occupancy_f16_f16(int, int, int*);
-int mma_occupancy_q8_0_bf16(int, int, int*);
-int mma_occupancy_q8_0_q8_0(int, int, int*);
-int mma_occupancy_q4s_q4s(int, int, int*);
-int mma_occupancy_q8_0_q4s(int, int, int*);
-int mma_occupancy_q4s_q8_0(int, int, int*);
-int mma_occupancy_q4s_bf16(int, int, int*);
+int mma_occupancy_bf16_bf16(int, int, int*, int);
+int mma_occupancy_f16_f16(int, int, int*, int);
+int mma_occupancy_q8_0_bf16(int, int, int*, int);
+int mma_occupancy_q8_0_q8_0(int, int, int*, int);
+int mma_occupancy_q4s_q4s(int, int, int*, int);
+int mma_occupancy_q8_0_q4s(int, int, int*, int);
+int mma_occupancy_q4s_q8_0(int, int, int*, int);
+int mma_occupancy_q4s_bf16(int, int, int*, int);
 
 namespace {
 
@@ -82,25 +82,25 @@ MmaFn mma_fn(int kc, int vc) {
 
 // Resident CTAs per SM of the tensor-core kernel for this shape, and its pipelines per
 // CTA (cached per process).
-int mma_occupancy(int kc, int vc, int head_dim, int group, int* pipes) {
+int mma_occupancy(int kc, int vc, int head_dim, int group, int* pipes, bool solo = false) {
   static std::mutex mu;
-  static int cache[4][4][3][4] = {};
-  static int cache_pipes[4][4][3][4] = {};
+  static int cache[4][4][3][5] = {};
+  static int cache_pipes[4][4][3][5] = {};
   const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
-  const int gi = group <= 4 ? 0 : group <= 8 ? 1 : group <= 16 ? 2 : 3;
+  const int gi = group <= 4 ? (solo ? 4 : 0) : group <= 8 ? 1 : group <= 16 ? 2 : 3;
   std::lock_guard<std::mutex> lock(mu);
   int& slot = cache[kc & 3][vc & 3][di][gi];
   int& pslot = cache_pipes[kc & 3][vc & 3][di][gi];
   if (slot == 0) {
     int n = 0, np = 1;
-    if (kc == KVQ_CODEC_BF16 && vc == KVQ_CODEC_BF16) n = mma_occupancy_bf16_bf16(head_dim, group, &np);
-    else if (kc == KVQ_CODEC_F16 && vc == KVQ_CODEC_F16) n = mma_occupancy_f16_f16(head_dim, group, &np);
-    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_BF16) n = mma_occupancy_q8_0_bf16(head_dim, group, &np);
-    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q8_0_q8_0(head_dim, group, &np);
-    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q4s_q4s(head_dim, group, &np);
-    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q8_0_q4s(head_dim, group, &np);
-    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q4s_q8_0(head_dim, group, &np);
-    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_BF16) n = mma_occupancy_q4s_bf16(head_dim, group, &np);
+    if (kc == KVQ_CODEC_BF16 && vc == KVQ_CODEC_BF16) n = mma_occupancy_bf16_bf16(head_dim, group, &np, solo ? 1 : 0);
+    else if (kc == KVQ_CODEC_F16 && vc == KVQ_CODEC_F16) n = mma_occupancy_f16_f16(head_dim, group, &np, solo ? 1 : 0);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_BF16) n = mma_occupancy_q8_0_bf16(head_dim, group, &np, solo ? 1 : 0);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q8_0_q8_0(head_dim, group, &np, solo ? 1 : 0);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q4s_q4s(head_dim, group, &np, solo ? 1 : 0);
+    else if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) n = mma_occupancy_q8_0_q4s(head_dim, group, &np, solo ? 1 : 0);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q8_0) n = mma_occupancy_q4s_q8_0(head_dim, group, &np, solo ? 1 : 0);
+    else if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_BF16) n = mma_occupancy_q4s_bf16(head_dim, group, &np, solo ? 1 : 0);
     slot = n > 0 ? n : 1;
     pslot = np > 0 ? np : 1;
   }
@@ -183,6 +183,7 @@ struct Plan {
   int n_groups;
   int variant;
   int records;       // record mode: records per (sequence, KV head), else 0
+  bool solo;         // tensor-core kernel, at most 4 rows per KV head: one pipeline per CTA
   size_t ml_off;     // chunk partials: o at 0, (m, l) at ml_off
   size_t go_off;     // group partials: o at go_off, (m, l) at gml_off
   size_t gml_off;
@@ -207,15 +208,21 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   if (chunk < 0 || chunk % 64 != 0) return KVQ_ERR_INVALID_ARG;
   p->variant = (opts && opts->variant) ? opts->variant : 2;
   const int group_all = num_q_heads / k->desc.num_kv_heads;
+  const int sms = sm_count();
+  if (sms <= 0) return KVQ_ERR_CUDA;
+  // More (sequence, KV head) units than SMs: many CTAs, each short (batched decode); the
+  // single-pipeline configuration keeps four of them per SM so that their prologues and
+  // merges overlap.  Otherwise one CTA of four pipelines per SM.
+  p->solo = p->variant == 2 && group_all <= 4 && k->desc.head_dim <= 128 &&
+            (long long)batch * k->desc.num_kv_heads > sms;
   int pipes = 1;
   if (p->variant == 2)
-    (void)mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec, k->desc.head_dim, group_all, &pipes);
+    (void)mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec, k->desc.head_dim, group_all, &pipes,
+                        p->solo);
   if (chunk == 0) {
-    const int sms = sm_count();
-    if (sms <= 0) return KVQ_ERR_CUDA;
     const int group = num_q_heads / k->desc.num_kv_heads;
     const int per_sm = p->variant == 2 ? mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec,
-                                                       k->desc.head_dim, group, &pipes)
+                                                       k->desc.head_dim, group, &pipes, p->solo)
                                        : 2;
     const long long units = (long long)batch * k->desc.num_kv_heads;
     const long long slots = (long long)sms * per_sm;
@@ -478,6 +485,7 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
   a.seq_lens_adv = seq_lens_adv;
   a.seq_counters = reinterpret_cast<unsigned*>(ws + p.seq_cnt_off);
   a.warp_records = p.records;
+  a.solo = p.solo ? 1 : 0;
   // the heads-on-M loop (q8_0 K and V, head_dim 128 or 256, 9..32 query rows per KV head)
   // leaves its chunk partials to the chunk merge kernel
   a.chunk_merge = (p.variant == 2 && kd.codec == KVQ_CODEC_Q8_0 && vd.codec == KVQ_CODEC_Q8_0 &&

@@ -282,7 +282,9 @@ __device__ __forceinline__ void load_scale_words(const uint8_t* base, int t, uin
 
 // ---------------------------------------------------------------- layout
 
-template <int KC, int VC, int D, int GW, int HG>
+// SOLO: one 4-warp pipeline per CTA and up to four CTAs per SM, for grids of many short
+// CTAs (more (sequence, KV head) units than SMs), whose prologues and merges then overlap.
+template <int KC, int VC, int D, int GW, int HG, bool SOLO = false>
 struct Cfg {
   // Heads on M (GW == 16, kvq_decode_hm.cuh): warps of 16 query rows x 16 tokens, HG row
   // groups per pipeline.
@@ -310,7 +312,7 @@ struct Cfg {
   // D <= 128).  Each pipeline is 4 warps with its own ring of stages; the CTA merges its
   // pipelines in shared memory, so a split has a quarter as many partials as with one
   // pipeline per CTA.  Otherwise one pipeline per CTA and register use sets occupancy.
-  static constexpr bool PACK = HG == 1 && GW <= 4 && D <= 128 && 2 * STAGE + 6 * 1024 <= 56 * 1024;
+  static constexpr bool PACK = !SOLO && HG == 1 && GW <= 4 && D <= 128 && 2 * STAGE + 6 * 1024 <= 56 * 1024;
   // HM: two pipelines per CTA for one row group (8 warps per SM at up to 255 registers:
   // the O accumulators alone take D / 2), one for two
   static constexpr int NP = PACK ? 4 : (HM && HG == 1) ? 2 : 1;   // pipelines per CTA
@@ -318,10 +320,10 @@ struct Cfg {
   static constexpr bool LEAN = HG == 1 && GW <= 4 && D <= 128;
   static constexpr int NW = PW * NP;                      // warps per CTA
   static constexpr int THREADS = NW * 32;
-  static constexpr int MINB = 1;
+  static constexpr int MINB = SOLO ? 4 : 1;
   // ring depth per pipeline: as many stages (2..4) as fit the per-pipeline budget
   static constexpr int SMEM_BUDGET = HM ? (HG > 1 ? 204 * 1024 : 104 * 1024 + 2048)
-                                     : HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : PACK ? 54 * 1024 : 70 * 1024;
+                                     : HG > 1 ? 200 * 1024 : D == 256 ? 100 * 1024 : (PACK || SOLO) ? 54 * 1024 : 70 * 1024;
   static constexpr int NS0 = (SMEM_BUDGET - 2048) / STAGE;
   static constexpr int NS = NS0 > 4 ? 4 : (NS0 < 2 ? 2 : NS0);
   static constexpr int PRING = NS * STAGE;                // one pipeline's ring
@@ -572,9 +574,9 @@ __device__ __forceinline__ unsigned seq_arrive(unsigned* cnt) {
   return old;
 }
 
-template <int KC, int VC, int D, int GW, int HG>
+template <int KC, int VC, int D, int GW, int HG, bool SOLO>
 __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeArgs& a) {
-  using C = Cfg<KC, VC, D, GW, HG>;
+  using C = Cfg<KC, VC, D, GW, HG, SOLO>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle pattern
   // (offset from the array itself, so accesses through `smem` stay in the shared space)
@@ -1687,23 +1689,23 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
   }   // tokens-on-M loop
 }
 
-template <int KC, int VC, int D, int GW, int HG>
-__global__ void __launch_bounds__(Cfg<KC, VC, D, GW, HG>::THREADS, Cfg<KC, VC, D, GW, HG>::MINB)
+template <int KC, int VC, int D, int GW, int HG, bool SOLO>
+__global__ void __launch_bounds__(Cfg<KC, VC, D, GW, HG, SOLO>::THREADS, Cfg<KC, VC, D, GW, HG, SOLO>::MINB)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   DecodeArgs a) {
-  decode_cta<KC, VC, D, GW, HG>(tmk, tmv, a);
+  decode_cta<KC, VC, D, GW, HG, SOLO>(tmk, tmv, a);
 }
 
 // Sets the kernel's shared-memory attributes once per device.
-template <int KC, int VC, int D, int GW, int HG>
+template <int KC, int VC, int D, int GW, int HG, bool SOLO>
 cudaError_t prepare() {
-  using C = Cfg<KC, VC, D, GW, HG>;
+  using C = Cfg<KC, VC, D, GW, HG, SOLO>;
   static unsigned long long done = 0;   // bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && (done >> dev) & 1ull) return cudaSuccess;
-  auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
+  auto kern = decode_mma_kernel<KC, VC, D, GW, HG, SOLO>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -1711,11 +1713,11 @@ cudaError_t prepare() {
   return e;
 }
 
-template <int KC, int VC, int D, int GW, int HG>
+template <int KC, int VC, int D, int GW, int HG, bool SOLO = false>
 cudaError_t launch(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
-  using C = Cfg<KC, VC, D, GW, HG>;
-  auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
-  cudaError_t e = prepare<KC, VC, D, GW, HG>();
+  using C = Cfg<KC, VC, D, GW, HG, SOLO>;
+  auto kern = decode_mma_kernel<KC, VC, D, GW, HG, SOLO>;
+  cudaError_t e = prepare<KC, VC, D, GW, HG, SOLO>();
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_chunks, a.k.num_kv_heads, a.batch);
   e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, stream, tmk, tmv, a);
@@ -1724,12 +1726,12 @@ cudaError_t launch(const DecodeArgs& a, const CUtensorMap& tmk, const CUtensorMa
 }
 
 // Resident CTAs per SM of one instantiation (0 on error); *pipes = its pipelines per CTA.
-template <int KC, int VC, int D, int GW, int HG>
+template <int KC, int VC, int D, int GW, int HG, bool SOLO = false>
 int occupancy(int* pipes) {
-  using C = Cfg<KC, VC, D, GW, HG>;
-  auto kern = decode_mma_kernel<KC, VC, D, GW, HG>;
+  using C = Cfg<KC, VC, D, GW, HG, SOLO>;
+  auto kern = decode_mma_kernel<KC, VC, D, GW, HG, SOLO>;
   *pipes = C::NP;
-  if (prepare<KC, VC, D, GW, HG>() != cudaSuccess) return 0;
+  if (prepare<KC, VC, D, GW, HG, SOLO>() != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM) != cudaSuccess) return 0;
   return n;
@@ -1741,8 +1743,11 @@ template <int KC, int VC>
 constexpr bool kHeadsOnM = KC == KVQ_CODEC_Q8_0 && VC == KVQ_CODEC_Q8_0;
 
 template <int KC, int VC>
-int occupancy_pair(int head_dim, int g, int* pipes) {
+int occupancy_pair(int head_dim, int g, int* pipes, bool solo) {
 #define KVQ_MMA_O(D)                                                               \
+  if constexpr (D <= 128) {                                                        \
+    if (g <= 4 && solo) return occupancy<KC, VC, D, 4, 1, true>(pipes);            \
+  }                                                                                \
   if (g <= 4) return occupancy<KC, VC, D, 4, 1>(pipes);                            \
   if (g <= 8) return occupancy<KC, VC, D, 8, 1>(pipes);                            \
   if constexpr (kHeadsOnM<KC, VC> && D >= 128) {                                   \
@@ -1766,6 +1771,9 @@ cudaError_t launch_pair(const DecodeArgs& a, int head_dim, const CUtensorMap& tm
                         cudaStream_t stream) {
   const int g = a.group;
 #define KVQ_MMA_G(D)                                                               \
+  if constexpr (D <= 128) {                                                        \
+    if (g <= 4 && a.solo) return launch<KC, VC, D, 4, 1, true>(a, tmk, tmv, stream); \
+  }                                                                                \
   if (g <= 4) return launch<KC, VC, D, 4, 1>(a, tmk, tmv, stream);                \
   if (g <= 8) return launch<KC, VC, D, 8, 1>(a, tmk, tmv, stream);                \
   if constexpr (kHeadsOnM<KC, VC> && D >= 128) {                                   \

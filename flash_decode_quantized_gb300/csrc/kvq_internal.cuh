@@ -108,6 +108,7 @@ struct DecodeArgs {
   // CTA without tokens) to part_ml / part_o and the chunk merge kernel, launched right
   // after it, combines them into the output (no arrival counters, no in-place merge).
   int chunk_merge;
+  int solo;                    // at most 4 query rows per KV head: one pipeline per CTA (Cfg SOLO)
   int wait_limit;              // tries of each bounded mbarrier wait before it gives up
   int skip_tile;               // fault injection: tile the first pipeline never issues (-1: none)
 };

@@ -6,7 +6,7 @@ cudaError_t mma_launch_f16_f16(const DecodeArgs& a, int head_dim, const CUtensor
                             const CUtensorMap& tmv, cudaStream_t stream) {
   return mma::launch_pair<KVQ_CODEC_F16, KVQ_CODEC_F16>(a, head_dim, tmk, tmv, stream);
 }
-int mma_occupancy_f16_f16(int head_dim, int group, int* pipes) {
-  return mma::occupancy_pair<KVQ_CODEC_F16, KVQ_CODEC_F16>(head_dim, group, pipes);
+int mma_occupancy_f16_f16(int head_dim, int group, int* pipes, int solo) {
+  return mma::occupancy_pair<KVQ_CODEC_F16, KVQ_CODEC_F16>(head_dim, group, pipes, solo != 0);
 }
 }  // namespace kvq

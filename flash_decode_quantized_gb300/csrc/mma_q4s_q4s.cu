@@ -6,7 +6,7 @@ cudaError_t mma_launch_q4s_q4s(const DecodeArgs& a, int head_dim, const CUtensor
                             const CUtensorMap& tmv, cudaStream_t stream) {
   return mma::launch_pair<KVQ_CODEC_Q4S, KVQ_CODEC_Q4S>(a, head_dim, tmk, tmv, stream);
 }
-int mma_occupancy_q4s_q4s(int head_dim, int group, int* pipes) {
-  return mma::occupancy_pair<KVQ_CODEC_Q4S, KVQ_CODEC_Q4S>(head_dim, group, pipes);
+int mma_occupancy_q4s_q4s(int head_dim, int group, int* pipes, int solo) {
+  return mma::occupancy_pair<KVQ_CODEC_Q4S, KVQ_CODEC_Q4S>(head_dim, group, pipes, solo != 0);
 }
 }  // namespace kvq

@@ -6,7 +6,7 @@ cudaError_t mma_launch_q4s_q8_0(const DecodeArgs& a, int head_dim, const CUtenso
                             const CUtensorMap& tmv, cudaStream_t stream) {
   return mma::launch_pair<KVQ_CODEC_Q4S, KVQ_CODEC_Q8_0>(a, head_dim, tmk, tmv, stream);
 }
-int mma_occupancy_q4s_q8_0(int head_dim, int group, int* pipes) {
-  return mma::occupancy_pair<KVQ_CODEC_Q4S, KVQ_CODEC_Q8_0>(head_dim, group, pipes);
+int mma_occupancy_q4s_q8_0(int head_dim, int group, int* pipes, int solo) {
+  return mma::occupancy_pair<KVQ_CODEC_Q4S, KVQ_CODEC_Q8_0>(head_dim, group, pipes, solo != 0);
 }
 }  // namespace kvq
