@@ -66,11 +66,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// Arrival by lane 0 of the warp (predicated, no branch).
-__device__ __forceinline__ void mbar_arrive_lane0(uint32_t bar, int lane) {
-  asm volatile("{\n .reg .pred p;\n setp.eq.s32 p, %1, 0;\n @p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n"
-               ::"r"(bar), "r"(lane) : "memory");
-}
 // Release of a stage by one of `warps` warps: lane 0 arrives on the stage's empty barrier
 // and counts the release; true (in every lane) for the warp whose release is the last
 // one, which also returns the count to zero.
@@ -91,22 +86,6 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(done) : "r"(bar), "r"(parity) : "memory");
   return done;
-}
-// try_wait that may suspend the warp for up to 1 us (it resumes as soon as the phase
-// completes): fewer retries of a long wait.
-__device__ __forceinline__ uint32_t mbar_try_suspend(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-  return done;
-}
-// mbar_wait_warp with suspending tries (each try waits up to 1 us).
-__device__ __forceinline__ bool mbar_wait_warp_s(uint32_t bar, uint32_t parity, int limit) {
-  for (int it = 0; it < limit; ++it)
-    if (__all_sync(0xffffffffu, mbar_try_suspend(bar, parity))) return true;
-  return false;
 }
 // Bounded wait, by every lane of a warp, for the phase of parity `parity` to complete.
 // Each lane observes the completion itself (acquire); the result is warp-uniform, so
