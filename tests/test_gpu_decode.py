@@ -68,6 +68,38 @@ def test_ragged_paged_batch(kc, vc, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("head_dim", [128, 256])
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q4s", "q4s")])
+def test_ragged_batch_gqa16(kc, vc, head_dim, variant):
+    # GQA 16:1 (q8_0: the heads-on-M loop and its chunk merge, where CTAs past a short
+    # sequence write empty partials; q4s: the tokens-on-M loop over two 8-head groups)
+    lens = [1, 63, 64, 65, 700, 2049, 0, 3000]
+    inp = make_inputs(lens, 32, 2, head_dim, seed=131, channel_scaled=True)
+    got, _ = run_decode(inp, kc, vc, variant=variant)
+    assert_close(got, oracle_out(inp, kc, vc), f"ragged GQA 16:1 D={head_dim} {kc}/{vc}")
+    assert np.all(got[6] == 0.0)  # the empty sequence yields zeros
+
+
+@pytest.mark.parametrize("head_dim", [128, 256])
+def test_heavy_tailed_values_gqa16(head_dim):
+    # Student-t values and keys with per-channel scales at GQA 16:1: the heads-on-M loop's
+    # V-scale bound and lazy max under large magnitudes
+    inp = make_inputs([3000, 1200], 32, 2, head_dim, seed=132, dist="t3", channel_scaled=True)
+    got, _ = run_decode(inp, "q8_0", "q8_0")
+    assert_close(got, oracle_out(inp, "q8_0", "q8_0"), f"t3 GQA 16:1 D={head_dim}")
+
+
+def test_page_permutation_invariance_gqa16():
+    # the heads-on-M loop's result depends on the positions only, not on where the pages are
+    a = make_inputs([2600, 700], 32, 2, 256, seed=133, permute_pages=True)
+    b = make_inputs([2600, 700], 32, 2, 256, seed=133, permute_pages=False)
+    assert not np.array_equal(a.page_table, b.page_table)
+    ga, _ = run_decode(a, "q8_0", "q8_0", chunk_tokens=256)
+    gb, _ = run_decode(b, "q8_0", "q8_0", chunk_tokens=256)
+    assert np.array_equal(ga, gb)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q8_0", "q4s")])
 def test_heavy_tailed_values(kc, vc, variant):
     inp = make_inputs([1500], 32, 8, 128, seed=14, dist="t3", channel_scaled=True)
