@@ -198,7 +198,8 @@ struct Plan {
 // units = batch x kv_heads, so the longest sequence fills one wave; chunk_tokens =
 // ceil(max_len / n_chunks) rounded up to 64 is the number of tokens a CTA covers (the
 // tensor-core kernel deals the 64-token tiles to its CTAs round-robin).  When units
-// outnumber slots, chunks are capped at 1024 tokens so long sequences still spread.
+// outnumber slots, chunks are capped (1024 tokens per pipeline, 2048 for single-pipeline CTAs)
+// so long sequences still spread.
 // It sizes the workspace: chunk partials, group partials (groups of kMergeGroup chunks)
 // and the arrival counters of the merge.
 kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_q_heads,
@@ -234,8 +235,10 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
     if (c < 128) c = 128;
     // With one or two CTAs per unit a long sequence among short ones would run alone
     // (lengths are on the device): keep chunks short enough for the block scheduler to
-    // balance the batch (1024 tokens per pipeline of the CTA).
-    const long long cap_tokens = 1024LL * pipes;
+    // balance the batch (1024 tokens per pipeline of the CTA; 2048 for the single-pipeline
+    // CTAs of a batch, whose fixed costs 1024-token chunks did not amortize: the
+    // 64-sequence ragged batch 496 -> 449 us, uniform batches unchanged or faster).
+    const long long cap_tokens = (p->solo ? 2048LL : 1024LL) * pipes;
     const bool capped = units * 4 > slots && c > cap_tokens;
     if (capped) c = cap_tokens;
     chunk = (int)c;
@@ -251,15 +254,18 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   const size_t D = (size_t)k->desc.head_dim;
   const size_t heads = (size_t)batch * num_q_heads;
   const size_t units = (size_t)batch * k->desc.num_kv_heads;
-  // Record mode (tensor-core kernel, at most 4 query rows per KV head, head_dim <= 128):
-  // every warp leaves its partial as a record ((chunk * pipes + pipe) * 4 + slice) and a
-  // separate merge kernel combines them.  Used while all records fit in 16 MiB (they stay
-  // in L2 between the two kernels and add little traffic); otherwise, and beyond 4096
-  // records per unit, the decode kernel merges in place (last-arriving CTA).
+  // Record mode (tensor-core kernel, at most 4 query rows per KV head, head_dim <= 128,
+  // four-pipeline CTAs): every warp leaves its partial as a record ((chunk * pipes + pipe)
+  // * 4 + slice) and a separate merge kernel combines them.  Used while all records fit in
+  // 16 MiB (they stay in L2 between the two kernels and add little traffic); otherwise,
+  // beyond 4096 records per unit, and for the single-pipeline CTAs of a batch (many units
+  // of few chunks, where a second kernel over every unit cost more than it saved: 160 ->
+  // 150 us for 160 sequences of 2048 tokens), the decode kernel merges in place
+  // (last-arriving CTA; a unit of one chunk writes its output directly).
   const long long recs = (long long)p->n_chunks * pipes * 4;
   const long long rec_bytes = (long long)units * recs * (long long)(D * 4 + 8) * 4;
-  p->records = (p->variant == 2 && group_all <= 4 && D <= 128 && recs <= 4096 && rec_bytes <= (16LL << 20))
-                   ? (int)recs : 0;
+  p->records = (p->variant == 2 && !p->solo && group_all <= 4 && D <= 128 && recs <= 4096 &&
+                rec_bytes <= (16LL << 20)) ? (int)recs : 0;
   if (p->records) {
     p->ml_off = round_up(units * p->records * (D * 4) * sizeof(float), 256);
     p->go_off = p->ml_off + round_up(units * p->records * 8 * sizeof(float), 256);

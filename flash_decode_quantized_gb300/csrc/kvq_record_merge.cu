@@ -11,10 +11,14 @@
 // runs in a fixed order, so the result does not depend on the order in which the decode
 // kernel's warps finished.
 //
-// Grid: (32-position slices of a record, units).  A CTA's 512 threads are 8 float4
-// positions x 64 record groups; each thread loads the O values of its records first (one
-// round trip for up to 512 records), the CTA meanwhile forms the per-head maxima, weights
-// and denominators from all records' (m, l), and the weighted sums meet in shared memory.
+// Grid: (slices of a record, units).  A CTA's 512 threads are NQ float4 positions x
+// 512 / NQ record groups, NQ chosen from the records per unit: 8 positions x 64 groups for
+// many records (a record in 16 or 8 slices), up to a whole record per CTA x 4 groups for a
+// few, so that the grid does not grow past what the records need (with thousands of units,
+// 16 CTAs per unit of mostly idle groups ran for ~100 us).  Each thread loads the O values
+// of its records first (one round trip for up to 8 per group), the CTA meanwhile forms the
+// per-head maxima, weights and denominators from all records' (m, l), and the weighted
+// sums meet in shared memory.
 // Launched with programmatic stream serialization right after the decode kernel: its CTAs
 // start as the decode's CTAs leave and wait (griddepcontrol.wait) for that grid's writes.
 #include "kvq_decode_mma.cuh"
@@ -24,8 +28,6 @@ namespace kvq {
 namespace {
 
 constexpr int kMergeThreads = 512;
-constexpr int kNQ = 8;                        // float4 positions per CTA
-constexpr int kNG = kMergeThreads / kNQ;      // record groups
 constexpr int kBatch = 8;                     // records per thread per round of loads
 
 __device__ __forceinline__ float4 ld_cg4(const float4* p) { return __ldcg(p); }
@@ -52,13 +54,18 @@ __device__ __forceinline__ void block_reduce4(float* v, bool is_max, float (*red
   __syncthreads();
 }
 
-template <int VC, int D>
-__global__ void __launch_bounds__(kMergeThreads) record_merge_kernel(DecodeArgs a) {
+template <int VC, int D, int kNQ>
+__global__ void __launch_bounds__(kMergeThreads, 2) record_merge_kernel(DecodeArgs a) {
   constexpr int P = D / 16 * 64;              // floats per record (4 heads x D)
+  constexpr int kNG = kMergeThreads / kNQ;    // record groups
+  static_assert(kNQ * 4 <= P && kNG >= 4, "slice shape");
+  // partial sums meet per warp (groups of a warp summed by shuffles first) for NQ < 32,
+  // per group otherwise
+  constexpr int kRG = kNQ < 32 ? kMergeThreads / 32 : kNG;
   extern __shared__ float w_sm[];             // [R][4] weights 2^(m - M)
   __shared__ float red[kMergeThreads / 32][4];
   __shared__ float sM[4], sden[4];
-  __shared__ float4 racc[kMergeThreads / 32][kNQ];
+  __shared__ float4 racc[kRG][kNQ];
   const int tid = threadIdx.x, q = tid & (kNQ - 1), g = tid / kNQ;
   const int R = a.warp_records;
   const long long unit = blockIdx.y;
@@ -135,20 +142,25 @@ __global__ void __launch_bounds__(kMergeThreads) record_merge_kernel(DecodeArgs 
       if (r < R) fold(r, ov[u]);
     }
   }
-  // over the record groups: lanes of a warp with the same q (g % 4 differs), then warps
+  // over the record groups: lanes of a warp with the same q (NQ < 32: the groups of a
+  // warp), then warps or groups, in a fixed order
+  if constexpr (kNQ < 32) {
 #pragma unroll
-  for (int off = kNQ; off < 32; off <<= 1) {
-    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    for (int off = kNQ; off < 32; off <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    if ((tid & 31) < kNQ) racc[tid >> 5][q] = acc;
+  } else {
+    racc[g][q] = acc;
   }
-  if ((tid & 31) < kNQ) racc[tid >> 5][q] = acc;
   __syncthreads();
-  if (tid < kNQ * 4) {
-    const int qq = tid >> 2, c = tid & 3;
+  for (int t4 = tid; t4 < kNQ * 4; t4 += kMergeThreads) {
+    const int qq = t4 >> 2, c = t4 & 3;
     float sum = 0.0f;
-    for (int w = 0; w < kMergeThreads / 32; ++w) sum += (&racc[w][qq].x)[c];
+    for (int w = 0; w < kRG; ++w) sum += (&racc[w][qq].x)[c];
     const int t = slice * kNQ * 4 + qq * 4 + c;      // position in the record
     const int mt = t >> 6, ln = (t >> 1) & 31, rr = ln >> 2, ii = ln & 3;
     const int dim = mma::pv_dim<VC>(mt, ii < 2 ? rr : rr + 8);
@@ -163,9 +175,9 @@ __global__ void __launch_bounds__(kMergeThreads) record_merge_kernel(DecodeArgs 
   }
 }
 
-template <int VC, int D>
-cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
-  auto kern = record_merge_kernel<VC, D>;
+template <int VC, int D, int kNQ>
+cudaError_t launch_merge_nq(const DecodeArgs& a, cudaStream_t stream) {
+  auto kern = record_merge_kernel<VC, D, kNQ>;
   const size_t smem = (size_t)a.warp_records * 16;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -176,6 +188,17 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
   const cudaError_t e = launch_pdl(kern, grid, dim3(kMergeThreads), smem, stream, a);
   count_launch();
   return e;
+}
+
+// Slice shape from the records per unit: about one round of loads per group (8 records)
+// while that keeps 4 or more groups per CTA.
+template <int VC, int D>
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int P4 = D / 16 * 16;   // float4 positions per record
+  const int R = a.warp_records;
+  if (R <= 4 * kBatch) return launch_merge_nq<VC, D, P4>(a, stream);                    // 512 / P4 groups
+  if (R <= 16 * kBatch) return launch_merge_nq<VC, D, 32>(a, stream);                   // 16 groups
+  return launch_merge_nq<VC, D, 8>(a, stream);                                          // 64 groups
 }
 
 template <int VC>
