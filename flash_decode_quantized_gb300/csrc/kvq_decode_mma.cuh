@@ -297,9 +297,12 @@ struct Cfg {
   // warps at 168 registers, no spills: 54 -> 47 us for GQA 16:1 at 65536 tokens, 8 KV
   // heads); one pipeline for two row groups.  8-head warps at head_dim <= 128: three
   // pipelines (12 warps at 168 registers instead of two CTAs of 4 warps at 223: GQA 8:1 at
-  // 65536 tokens 48 -> 43.6 us for q8_0, 50 -> 45 us for q4s; four pipelines gain nothing)
+  // 65536 tokens 48 -> 43.6 us for q8_0, 50 -> 45 us for q4s; four pipelines gain nothing).
+  // 4-head warps at head_dim 256 where two stages of each of three pipelines fit: three
+  // (8192 tokens 24.9 -> 20.6 us, one KV head at 131072 tokens 34.8 -> 31.6 us)
   static constexpr int NP = PACK ? 4 : (HM && HG == 1) ? (D == 128 ? 3 : 2)
-                                   : (GW == 8 && HG == 1 && D <= 128) ? 3 : 1;   // pipelines per CTA
+                          : ((GW == 8 && D <= 128) || (GW == 4 && D == 256 && !SOLO && 6 * STAGE <= 210 * 1024)) && HG == 1
+                              ? 3 : 1;   // pipelines per CTA
   // the lean tile loop (see decode_cta) serves warps of at most 4 heads at D <= 128
   static constexpr bool LEAN = HG == 1 && GW <= 4 && D <= 128;
   static constexpr int NW = PW * NP;                      // warps per CTA
