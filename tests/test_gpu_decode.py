@@ -80,6 +80,16 @@ def test_ragged_batch_gqa16(kc, vc, head_dim, variant):
     assert np.all(got[6] == 0.0)  # the empty sequence yields zeros
 
 
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q4s", "q4s"), ("bf16", "bf16")])
+def test_ragged_batch_gqa8(kc, vc):
+    # 8 query heads per KV head: three pipelines of 8-head warps per CTA, a ragged batch
+    # (pipelines of one CTA finish at different times; empty and one-token sequences)
+    inp = make_inputs([5, 1, 0, 64, 1500, 4100], 64, 8, 128, seed=134)
+    got, _ = run_decode(inp, kc, vc)
+    assert_close(got, oracle_out(inp, kc, vc), f"ragged GQA 8:1 {kc}/{vc}")
+    assert np.all(got[2] == 0.0)
+
+
 @pytest.mark.parametrize("head_dim", [128, 256])
 def test_heavy_tailed_values_gqa16(head_dim):
     # Student-t values and keys with per-channel scales at GQA 16:1: the heads-on-M loop's
@@ -108,7 +118,8 @@ def test_heavy_tailed_values(kc, vc, variant):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("group,head_dim", [(1, 128), (2, 64), (8, 128), (16, 128), (4, 256)])
+@pytest.mark.parametrize("group,head_dim", [(1, 128), (2, 64), (8, 128), (16, 128), (4, 256),
+                                            (8, 64), (6, 128), (2, 256), (12, 128)])
 def test_group_and_head_dim_sweep(group, head_dim, variant):
     inp = make_inputs([777, 129], 2 * group, 2, head_dim, seed=15)
     got, _ = run_decode(inp, "q8_0", "q8_0", variant=variant)
