@@ -77,6 +77,23 @@ def test_fused_ragged_batch(kc, vc):
     assert_close(got, oracle_out(inp, kc, vc), "ragged fused step")
 
 
+@pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q4s", "q4s")])
+def test_fused_step_many_units(kc, vc):
+    # 24 sequences x 8 KV heads = 192 units, more than the SMs: single-pipeline CTAs that
+    # merge in place and advance the lengths by tickets (no merge kernel)
+    prefix = [int(x) for x in np.random.default_rng(39).integers(0, 2500, size=24)]
+    prefix[3], prefix[10] = 0, 255
+    inp = make_inputs([n + 1 for n in prefix], 32, 8, 128, seed=39)
+    ks, vs, seq, pt = prefix_stores(inp, kc, vc, prefix)
+    kn, vn = new_rows(inp, prefix)
+    k = kvq()
+    got = k.kvq_flash_decode_append(bf16_tensor(inp.q), kn, vn, ks, vs, seq, pt).cpu().numpy()
+    assert seq.cpu().tolist() == [n + 1 for n in prefix]
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+    check_rows(inp, ks, vs, kc, vc, prefix)
+    assert_close(got, oracle_out(inp, kc, vc), f"{kc}/{vc} 24-sequence fused step")
+
+
 def test_fused_equals_append_then_decode():
     prefix = [700, 1500]
     inp = make_inputs([n + 1 for n in prefix], 32, 8, 128, seed=32, dist="t3", channel_scaled=True)
