@@ -213,9 +213,14 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   if (sms <= 0) return KVQ_ERR_CUDA;
   // More (sequence, KV head) units than SMs: many CTAs, each short (batched decode); the
   // single-pipeline configuration keeps four of them per SM so that their prologues and
-  // merges overlap.  Otherwise one CTA of four pipelines per SM.
-  p->solo = p->variant == 2 && group_all <= 4 && k->desc.head_dim <= 128 &&
-            (long long)batch * k->desc.num_kv_heads > sms;
+  // merges overlap.  Also from 9 units up where whole single-pipeline CTAs per unit fill at
+  // least 90 % of the 4 x SMs slots in one wave: a unit's CTAs then come in steps of one
+  // pipeline instead of four (4 sequences x 65536 tokens 130 -> 117 us, 8 x 32768 141 ->
+  // 123 us).  Otherwise one CTA of four pipelines per SM.
+  const long long units_all = (long long)batch * k->desc.num_kv_heads;
+  const long long solo_slots = 4LL * sms;
+  const bool solo_fills = units_all > 8 && (solo_slots / units_all) * units_all * 10 >= 9 * solo_slots;
+  p->solo = p->variant == 2 && group_all <= 4 && k->desc.head_dim <= 128 && (units_all > sms || solo_fills);
   int pipes = 1;
   if (p->variant == 2)
     (void)mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec, k->desc.head_dim, group_all, &pipes,
