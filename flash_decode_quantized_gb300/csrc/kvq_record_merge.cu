@@ -213,11 +213,12 @@ cudaError_t launch_merge_d(const DecodeArgs& a, int head_dim, cudaStream_t strea
 // n_chunks chunk partials (m_c, l_c, O_c) of every query row into its output,
 //   M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,
 // skipping partials with m = -inf (chunks without tokens; their O is not written).
-// Grid: (64-element slices of head_dim, query rows).  256 threads = 16 float4 columns x 16
-// chunk groups; each thread loads the O values of its chunks (c = group, group + 16, ...)
-// first, the CTA forms the weights from all chunks' (m, l) meanwhile, and the groups' sums
-// meet in shared memory in a fixed order.
-constexpr int kCmThreads = 256, kCmCols = 16, kCmGroups = kCmThreads / kCmCols, kCmBatch = 8;
+// Grid: (slices of head_dim, query rows).  256 threads = COLS float4 columns x 256 / COLS
+// chunk groups (a whole row for few chunks, 64-element slices x 16 groups for many); each
+// thread loads the O values of its chunks (c = group, group + groups, ...) first, the CTA
+// forms the weights from all chunks' (m, l) meanwhile, and the groups' sums meet in shared
+// memory in a fixed order.
+constexpr int kCmThreads = 256, kCmBatch = 8;
 
 __device__ __forceinline__ float block_reduce1(float v, bool is_max, float* red, float* res) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -237,8 +238,9 @@ __device__ __forceinline__ float block_reduce1(float v, bool is_max, float* red,
   return *res;
 }
 
-template <int D>
+template <int D, int kCmCols>
 __global__ void __launch_bounds__(kCmThreads) chunk_merge_kernel(DecodeArgs a) {
+  constexpr int kCmGroups = kCmThreads / kCmCols;   // chunk groups
   extern __shared__ float cw[];                 // [n_chunks] weights 2^(m_c - M)
   __shared__ float red[kCmThreads / 32];
   __shared__ float sres[2];
@@ -309,9 +311,9 @@ __global__ void __launch_bounds__(kCmThreads) chunk_merge_kernel(DecodeArgs a) {
   }
 }
 
-template <int D>
-cudaError_t launch_cm(const DecodeArgs& a, cudaStream_t stream) {
-  auto kern = chunk_merge_kernel<D>;
+template <int D, int kCmCols>
+cudaError_t launch_cm_cols(const DecodeArgs& a, cudaStream_t stream) {
+  auto kern = chunk_merge_kernel<D, kCmCols>;
   const size_t smem = (size_t)a.n_chunks * 4;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -321,6 +323,16 @@ cudaError_t launch_cm(const DecodeArgs& a, cudaStream_t stream) {
   const cudaError_t e = launch_pdl(kern, grid, dim3(kCmThreads), smem, stream, a);
   count_launch();
   return e;
+}
+
+// Slice shape from the chunks per row: a whole row per CTA while its groups take every
+// chunk in one round of loads (a batch of many rows and few chunks then runs as many CTAs
+// as rows instead of D / 64 times as many), else 64-element slices with 16 chunk groups.
+template <int D>
+cudaError_t launch_cm(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int kRowCols = D / 4;                      // float4 columns of a row
+  if (a.n_chunks <= (kCmThreads / kRowCols) * kCmBatch) return launch_cm_cols<D, kRowCols>(a, stream);
+  return launch_cm_cols<D, 16>(a, stream);
 }
 
 }  // namespace
