@@ -218,9 +218,16 @@ kvq_status make_plan(const kvq_store* k, const kvq_store* v, int batch, int num_
   // pipeline instead of four (4 sequences x 65536 tokens 130 -> 117 us, 8 x 32768 141 ->
   // 123 us).  Otherwise one CTA of four pipelines per SM.
   const long long units_all = (long long)batch * k->desc.num_kv_heads;
-  const long long solo_slots = 4LL * sms;
-  const bool solo_fills = units_all > 8 && (solo_slots / units_all) * units_all * 10 >= 9 * solo_slots;
-  p->solo = p->variant == 2 && group_all <= 4 && k->desc.head_dim <= 128 && (units_all > sms || solo_fills);
+  const int vcodec = v ? v->desc.codec : k->desc.codec;
+  bool solo_ok = p->variant == 2 && group_all <= 4 && k->desc.head_dim <= 128;
+  long long solo_slots = 0;
+  if (solo_ok) {
+    int solo_pipes = 1;
+    solo_slots = (long long)sms * mma_occupancy(k->desc.codec, vcodec, k->desc.head_dim, group_all, &solo_pipes, true);
+    solo_ok = solo_slots > 0;
+  }
+  const bool solo_fills = solo_ok && units_all > 8 && (solo_slots / units_all) * units_all * 10 >= 9 * solo_slots;
+  p->solo = solo_ok && (units_all > sms || solo_fills);
   int pipes = 1;
   if (p->variant == 2)
     (void)mma_occupancy(k->desc.codec, v ? v->desc.codec : k->desc.codec, k->desc.head_dim, group_all, &pipes,
