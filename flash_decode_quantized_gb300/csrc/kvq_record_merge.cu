@@ -14,8 +14,8 @@
 // Grid: (slices of a record, units).  A CTA's 512 threads are NQ float4 positions x
 // 512 / NQ record groups, NQ chosen from the records per unit: 8 positions x 64 groups for
 // many records (a record in 16 or 8 slices), up to a whole record per CTA x 4 groups for a
-// few, so that the grid does not grow past what the records need (with thousands of units,
-// 16 CTAs per unit of mostly idle groups ran for ~100 us).  Each thread loads the O values
+// few, so that the grid does not grow past what the records need (with 512 units of 4
+// records, 16 CTAs per unit of mostly idle groups ran for ~100 us).  Each thread loads the O values
 // of its records first (one round trip for up to 8 per group), the CTA meanwhile forms the
 // per-head maxima, weights and denominators from all records' (m, l), and the weighted
 // sums meet in shared memory.
