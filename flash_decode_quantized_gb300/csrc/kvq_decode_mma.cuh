@@ -195,16 +195,19 @@ __device__ __forceinline__ uint32_t u4pair_hi_raw(uint32_t w) {
 }
 constexpr uint32_t kSixteenth2 = 0x2C002C00u;   // f16 pair (1/16, 1/16)
 constexpr uint32_t kMinus72x2 = 0xD480D480u;    // f16 pair (-72, -72)
-// Nibble pair (bits 6-9 and 22-25 of w) holding u = q + 8 -> the f16 pair 8 + u/2 =
-// 12 + q/2 (0x48 << 8 is 8.0; the nibble lands in the top mantissa bits).  The K codes of
-// the 4-bit codec use this form: with the 1024-based one the seeded accumulator carried
-// ~1000x the block's dot product and the tensor-core accumulate lost its low bits
+// Nibble pair (bits 4-7 and 20-23 of w) holding u = q + 8 -> the f16 pair 8 + u/8 =
+// 9 + q/8 (0x48 << 8 is 8.0; the nibble lands in mantissa bits 4-7, so a word's nibbles
+// need shifts by 4, 0, -4 and -8 bits: three shifts and four lop3s per word).  The K
+// codes of the 4-bit codec use this form: its offset is ~10x a code's step, as for the
+// 8-bit codes; with the 1024-based one (offset ~150x the step) the seeded accumulator
+// carried ~1000x the block's dot product and the tensor-core accumulate lost its low bits
 // (score errors ~1e-3 in log2 units for keys of magnitude ~50).
 __device__ __forceinline__ uint32_t u4pair_half(uint32_t w) {
-  return and_or(w, 0x03C003C0u, 0x48004800u);
+  return and_or(w, 0x00F000F0u, 0x48004800u);
 }
 constexpr float kBias8 = 1152.0f;            // offset of i8pair_raw values
-constexpr float kBias4K = 12.0f;             // offset of u4pair_half values (which carry q/2)
+constexpr float kBias4K = 9.0f;              // offset of u4pair_half values (which carry q/8)
+constexpr float kScale4K = 8.0f;             // u4pair_half values carry q/8
 
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -869,8 +872,8 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
       for (int k = 0; k < 4; ++k) o[mt][n][k] = 0.0f;
   // reference max (warp-uniform) and this lane's partial sum for QK columns 2*i4, 2*i4+1
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-  // softmax scale in log2 units; 4-bit K fragments carry q/2
-  const float qk_mul = a.qk_scale_log2 * (KC == KVQ_CODEC_Q4S ? 2.0f : 1.0f);
+  // softmax scale in log2 units; 4-bit K fragments carry q/8
+  const float qk_mul = a.qk_scale_log2 * (KC == KVQ_CODEC_Q4S ? kScale4K : 1.0f);
   int E = -100;                                                 // running V-scale exponent bound
   bool timed_out = false;
   const int wlim = a.wait_limit;   // tries of mbarrier.try_wait before a wait gives up
@@ -949,11 +952,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
                 const uint32_t ra = x[2 * h2], rb = x[2 * h2 + 1];  // rows r and r+8 of block bb+h2
                 float cb[4] = {kbr[bb + h2].x, kbr[bb + h2].y, kbr[bb + h2].x, kbr[bb + h2].y};
                 uint32_t af[4];
-                af[0] = u4pair_half(ra << 6); af[1] = u4pair_half(rb << 6);
-                af[2] = u4pair_half(ra << 2); af[3] = u4pair_half(rb << 2);
+                af[0] = u4pair_half(ra << 4); af[1] = u4pair_half(rb << 4);
+                af[2] = u4pair_half(ra); af[3] = u4pair_half(rb);
                 mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
-                af[0] = u4pair_half(ra >> 2); af[1] = u4pair_half(rb >> 2);
-                af[2] = u4pair_half(ra >> 6); af[3] = u4pair_half(rb >> 6);
+                af[0] = u4pair_half(ra >> 4); af[1] = u4pair_half(rb >> 4);
+                af[2] = u4pair_half(ra >> 8); af[3] = u4pair_half(rb >> 8);
                 mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
                 sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
                 sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);
@@ -1237,11 +1240,11 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tmk, const CUtenso
                 const float2 kb = kbs[(hg * C::NB + bb + h2) * 4 + i4];
                 float cb[4] = {kb.x, kb.y, kb.x, kb.y};
                 uint32_t af[4];
-                af[0] = u4pair_half(ra << 6); af[1] = u4pair_half(rb << 6);
-                af[2] = u4pair_half(ra << 2); af[3] = u4pair_half(rb << 2);
+                af[0] = u4pair_half(ra << 4); af[1] = u4pair_half(rb << 4);
+                af[2] = u4pair_half(ra); af[3] = u4pair_half(rb);
                 mma16816<false>(cb, af, qf[2 * (bb + h2)][0], qf[2 * (bb + h2)][1]);
-                af[0] = u4pair_half(ra >> 2); af[1] = u4pair_half(rb >> 2);
-                af[2] = u4pair_half(ra >> 6); af[3] = u4pair_half(rb >> 6);
+                af[0] = u4pair_half(ra >> 4); af[1] = u4pair_half(rb >> 4);
+                af[2] = u4pair_half(ra >> 8); af[3] = u4pair_half(rb >> 8);
                 mma16816<false>(cb, af, qf[2 * (bb + h2) + 1][0], qf[2 * (bb + h2) + 1][1]);
                 sc[0] = fmaf(dk[0][bb + h2], cb[0], sc[0]);
                 sc[1] = fmaf(dk[0][bb + h2], cb[1], sc[1]);

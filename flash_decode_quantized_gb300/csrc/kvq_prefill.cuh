@@ -229,7 +229,7 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
     seed[bb][0] = -bias * sA;
     seed[bb][1] = -bias * sB;
   }
-  const float qk_mul = a.qk_scale_log2 * (KC == KVQ_CODEC_Q4S ? 2.0f : 1.0f);
+  const float qk_mul = a.qk_scale_log2 * (KC == KVQ_CODEC_Q4S ? kScale4K : 1.0f);
   uint4* const qfs = reinterpret_cast<uint4*>(smem + C::QF_OFF) + warp * C::KSTEPS * 32 + lane;
   float2* const sds = reinterpret_cast<float2*>(smem + C::SD_OFF) + warp * C::NB * 32 + lane;
   if constexpr (C::QSM) {
@@ -312,8 +312,8 @@ prefill_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constan
                   b0 = i8pair_raw(u, 0x4140);
                   b1 = i8pair_raw(u, 0x4342);
                 } else {
-                  b0 = u4pair_half(half ? (y[m] >> 2) : (y[m] << 6));
-                  b1 = u4pair_half(half ? (y[m] >> 6) : (y[m] << 2));
+                  b0 = u4pair_half(half ? (y[m] >> 4) : (y[m] << 4));
+                  b1 = u4pair_half(half ? (y[m] >> 8) : y[m]);
                 }
                 mma16816<false>(cb[m], qk, b0, b1);
               }
