@@ -31,6 +31,17 @@ def test_page_sizes(page_size, kc, vc):
     assert_close(decode(inp, kc, vc), oracle_out(inp, kc, vc), f"page {page_size} {kc}/{vc}")
 
 
+@pytest.mark.parametrize("page_size", [64, 128])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 2, 256), (32, 2, 128), (64, 8, 128)])
+def test_small_pages_for_the_wide_groups(page_size, hq, hkv, d):
+    # heads-on-M (GQA 16:1) and three-pipeline 8-head warps (GQA 8:1) where every tile is
+    # a whole page or half of one, with a ragged tail
+    inp = make_inputs([2000, 3 * page_size + 5], hq, hkv, d, seed=74 + page_size + d, page_size=page_size,
+                      channel_scaled=True)
+    assert_close(decode(inp, "q8_0", "q8_0"), oracle_out(inp, "q8_0", "q8_0"),
+                 f"page {page_size} GQA {hq // hkv}:1 D={d}")
+
+
 @pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q4s", "q8_0"), ("f16", "f16")])
 def test_largest_head_dim_and_group_at_the_largest_page(kc, vc):
     # head_dim 256, 16 query heads per KV head, 1024-token pages, channel-scaled values
