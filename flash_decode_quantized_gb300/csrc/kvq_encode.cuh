@@ -39,6 +39,19 @@ __device__ __forceinline__ float round_quotient_mag(float ax, float d, float rcp
   return aq;
 }
 
+// fp32(amax / c) correctly rounded, for c = 127 or 7 and amax a finite bf16 value: the
+// product by the rounded reciprocal and one FMA correction (Markstein's division step),
+// which an exhaustive check over every positive finite bf16 amax finds equal to the IEEE
+// quotient for both constants; infinities and NaNs pass through the product.
+template <int C>
+__device__ __forceinline__ float scale_quotient(float amax) {
+  constexpr float r = 1.0f / C;                       // rounded reciprocal
+  const float q0 = __fmul_rn(amax, r);
+  const float e = fmaf(-q0, (float)C, amax);          // exact residual
+  const float q1 = fmaf(e, r, q0);
+  return amax <= 3.402823466e38f ? q1 : q0;
+}
+
 // Lane `lane`'s EPL elements of one bf16 row, as floats (exact).
 // One vector load per lane (rows are 16-byte aligned: the bindings check it).
 template <int EPL>
@@ -92,7 +105,7 @@ __device__ __forceinline__ void store_row(const StoreView& st, int page, int r, 
 #pragma unroll
     for (int off = 1; off < LANES_PER_BLOCK; off <<= 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const __half dh = __float2half_rn(__fdiv_rn(amax, C));
+    const __half dh = __float2half_rn(scale_quotient<CODEC == KVQ_CODEC_Q8_0 ? 127 : 7>(amax));
     const float d = __half2float(dh);
     int qv[EPL];
     // warp-uniform choice, so the division path costs nothing when no block needs it
@@ -114,16 +127,28 @@ __device__ __forceinline__ void store_row(const StoreView& st, int page, int r, 
     uint8_t* dst = slab + (long long)r * st.row_bytes;
     // the lane's codes as one store: EPL bytes (q8_0) or EPL nibbles (q4s)
     if constexpr (CODEC == KVQ_CODEC_Q8_0) {
-      uint32_t w[(EPL + 3) / 4] = {};
+      // low bytes of the codes (two's complement) gathered by byte permutes
+      uint32_t w[(EPL + 3) / 4];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) w[e / 4] |= (uint32_t)(uint8_t)(int8_t)qv[e] << (8 * (e % 4));
+      for (int k = 0; k < (EPL + 3) / 4; ++k) {
+        const int e = 4 * k;
+        if constexpr (EPL == 2) {
+          w[k] = __byte_perm((uint32_t)qv[0], (uint32_t)qv[1], 0x0040);
+        } else {
+          w[k] = __byte_perm(__byte_perm((uint32_t)qv[e], (uint32_t)qv[e + 1], 0x0040),
+                             __byte_perm((uint32_t)qv[e + 2], (uint32_t)qv[e + 3], 0x0040), 0x5410);
+        }
+      }
       if constexpr (EPL == 2) *reinterpret_cast<uint16_t*>(dst + lane * 2) = (uint16_t)w[0];
       else if constexpr (EPL == 4) *reinterpret_cast<uint32_t*>(dst + lane * 4) = w[0];
       else *reinterpret_cast<uint2*>(dst + lane * 8) = make_uint2(w[0], w[1]);
     } else {
-      uint32_t w = 0;
+      // sum_e (q_e + 8) 16^e: each term lies in [1, 15], so no nibble carries
+      int acc = 0;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) w |= (uint32_t)(qv[e] + 8) << (4 * e);
+      for (int e = EPL - 1; e >= 0; --e) acc = acc * 16 + qv[e];
+      constexpr uint32_t kEights = EPL == 2 ? 0x88u : EPL == 4 ? 0x8888u : 0x88888888u;
+      const uint32_t w = (uint32_t)acc + kEights;
       if constexpr (EPL == 2) dst[lane] = (uint8_t)w;
       else if constexpr (EPL == 4) *reinterpret_cast<uint16_t*>(dst + lane * 2) = (uint16_t)w;
       else *reinterpret_cast<uint32_t*>(dst + lane * 4) = w;
