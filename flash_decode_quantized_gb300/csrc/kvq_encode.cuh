@@ -42,7 +42,8 @@ __device__ __forceinline__ float round_quotient_mag(float ax, float d, float rcp
 // fp32(amax / c) correctly rounded, for c = 127 or 7 and amax a finite bf16 value: the
 // product by the rounded reciprocal and one FMA correction (Markstein's division step),
 // which an exhaustive check over every positive finite bf16 amax finds equal to the IEEE
-// quotient for both constants; infinities and NaNs pass through the product.
+// quotient for both constants (tests/test_encode_quotient.py); infinities and NaNs pass
+// through the product.
 template <int C>
 __device__ __forceinline__ float scale_quotient(float amax) {
   constexpr float r = 1.0f / C;                       // rounded reciprocal
