@@ -109,6 +109,17 @@ def test_page_permutation_invariance_gqa16():
     assert np.array_equal(ga, gb)
 
 
+@pytest.mark.parametrize("batch", [3, 16])
+def test_mid_size_batches(batch):
+    # 24 units (single-pipeline CTAs filling the slots in one wave) and 128 units (four-
+    # pipeline CTAs with capped chunks), ragged lengths, both merge paths
+    lens = [int(x) for x in np.random.default_rng(135 + batch).integers(1, 6000, size=batch)]
+    inp = make_inputs(lens, 32, 8, 128, seed=135 + batch)
+    for kc, vc in (("q8_0", "q8_0"), ("q4s", "q4s")):
+        got, _ = run_decode(inp, kc, vc)
+        assert_close(got, oracle_out(inp, kc, vc), f"B={batch} {kc}/{vc}")
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("kc,vc", [("q8_0", "q8_0"), ("q8_0", "q4s")])
 def test_heavy_tailed_values(kc, vc, variant):
