@@ -115,7 +115,7 @@ def test_mid_size_batches(batch):
     # pipeline CTAs with capped chunks), ragged lengths, both merge paths
     lens = [int(x) for x in np.random.default_rng(135 + batch).integers(1, 6000, size=batch)]
     inp = make_inputs(lens, 32, 8, 128, seed=135 + batch)
-    for kc, vc in (("q8_0", "q8_0"), ("q4s", "q4s")):
+    for kc, vc in (("q8_0", "q8_0"), ("q4s", "q4s"), ("bf16", "bf16"), ("q8_0", "bf16")):
         got, _ = run_decode(inp, kc, vc)
         assert_close(got, oracle_out(inp, kc, vc), f"B={batch} {kc}/{vc}")
 
