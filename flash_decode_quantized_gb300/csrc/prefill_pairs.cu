@@ -1,11 +1,20 @@
-// Prefill attention kernels for the K/V codec pairs that have them (instantiations of
-// kvq_prefill.cuh).
+// Prefill attention kernels for the K/V codec pairs that have them: the tensor-core
+// (tcgen05) kernel of kvq_prefill_tc.cuh for head_dim 128 with K and V each q8_0 or f16,
+// the warp-MMA kernel of kvq_prefill.cuh for the other pairs and head sizes.
 #include "kvq_prefill.cuh"
+#include "kvq_prefill_tc.cuh"
 
 namespace kvq {
 cudaError_t prefill_launch(int kc, int vc, const PrefillArgs& a, int batch, int head_dim,
                            const CUtensorMap& tmk, const CUtensorMap& tmv, cudaStream_t stream) {
   using namespace prefill;
+  if (head_dim == 128) {
+    constexpr int Q8 = KVQ_CODEC_Q8_0, F16 = KVQ_CODEC_F16;
+    if (kc == Q8 && vc == Q8) return prefill_tc::launch<Q8, Q8>(a, batch, tmk, tmv, stream);
+    if (kc == F16 && vc == F16) return prefill_tc::launch<F16, F16>(a, batch, tmk, tmv, stream);
+    if (kc == Q8 && vc == F16) return prefill_tc::launch<Q8, F16>(a, batch, tmk, tmv, stream);
+    if (kc == F16 && vc == Q8) return prefill_tc::launch<F16, Q8>(a, batch, tmk, tmv, stream);
+  }
   if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q8_0) return launch_pair<KVQ_CODEC_Q8_0, KVQ_CODEC_Q8_0>(a, batch, head_dim, tmk, tmv, stream);
   if (kc == KVQ_CODEC_Q4S && vc == KVQ_CODEC_Q4S) return launch_pair<KVQ_CODEC_Q4S, KVQ_CODEC_Q4S>(a, batch, head_dim, tmk, tmv, stream);
   if (kc == KVQ_CODEC_Q8_0 && vc == KVQ_CODEC_Q4S) return launch_pair<KVQ_CODEC_Q8_0, KVQ_CODEC_Q4S>(a, batch, head_dim, tmk, tmv, stream);

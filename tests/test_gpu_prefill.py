@@ -16,7 +16,7 @@ from workloads import f32_to_bf16_bits, make_inputs
 pytestmark = pytest.mark.gpu
 
 PAIRS = [("q8_0", "q8_0"), ("q4s", "q4s"), ("q8_0", "q4s"), ("f16", "f16"), ("bf16", "bf16"),
-         ("q8_0", "bf16"), ("q4s", "q8_0"), ("q4s", "bf16")]
+         ("q8_0", "bf16"), ("q4s", "q8_0"), ("q4s", "bf16"), ("q8_0", "f16"), ("f16", "q8_0")]
 
 
 def run(inp, kc, vc, T, seed):
@@ -78,6 +78,32 @@ def test_prefill_head_dim_256(kc, vc):
     inp = make_inputs([900, 70], 32, 2, 256, seed=209, dist="t3", channel_scaled=True)
     got, want = run(inp, kc, vc, 70, seed=210)
     assert_close(got, want, f"D=256 {kc}/{vc}")
+
+
+def _rescaled(rows, factor):
+    return f32_to_bf16_bits((ocodec.bf16_bits_to_f64(rows) * factor).astype(np.float32))
+
+
+def test_prefill_magnitudes_past_the_f16_range():
+    # V up to ~2e5 (q8_0 scales near 1500: d q alone would overflow f16) and K down at
+    # ~1/64: the tensor-core kernel's per-tile powers of two must keep both exact; compared
+    # in units of the V factor
+    inp = make_inputs([1500, 90], 16, 4, 128, seed=213, dist="t3")
+    fv = 4.0e4
+    inp.k_rows = [_rescaled(x, 1.0 / 64.0) for x in inp.k_rows]
+    inp.v_rows = [_rescaled(x, fv) for x in inp.v_rows]
+    got, want = run(inp, "q8_0", "q8_0", 90, seed=214)
+    assert np.isfinite(got).all()
+    assert_close(got / fv, want / fv, "q8_0 magnitudes")
+
+
+@pytest.mark.parametrize("page_size", [64, 1024])
+def test_prefill_page_sizes(page_size):
+    # tiles from pages of one tile and of sixteen; chunks spanning several 128-row CTAs
+    inp = make_inputs([2100, 333], 32, 8, 128, seed=215, page_size=page_size)
+    for kc, vc in (("q8_0", "q8_0"), ("f16", "f16")):
+        got, want = run(inp, kc, vc, 200, seed=216)
+        assert_close(got, want, f"page {page_size} {kc}/{vc}")
 
 
 def test_prefill_unsupported_pair():
