@@ -1,25 +1,29 @@
-// Chunked prefill attention on the 5th-generation tensor cores (tcgen05, accumulators in
-// tensor memory), head_dim 128, K and V each q8_0 or f16: the prompt-processing arm of
-// halobench record clm-0022's depth tables (pp512 at depth), with the dequantization fused
-// into the load of each KV tile.
+// Chunked prefill attention on the 5th-generation tensor cores (tcgen05, operands and
+// accumulators in tensor memory), head_dim 128, K and V each q8_0 or f16: the
+// prompt-processing arm of halobench record clm-0022's depth tables (pp512 at depth), with
+// the dequantization fused into the load of each KV tile.
 //
-// A CTA owns 128 query rows of one (sequence, KV head), row = token * G + head-in-group;
-// thread t owns row t and tensor-memory lane t.  Per 64-token KV tile:
+// A CTA owns 128 query rows of one (sequence, KV head), row = token * G + head-in-group,
+// one per tensor-memory lane.  Per 64-token KV tile:
 //  * the tile arrives by TMA in the 128-byte swizzled layout that the MMA reads; a q8_0 tile
-//    is first turned, once for all 128 rows, into two f16 tiles of the same layout whose sum
-//    is d * q exactly (hi = d q rounded, lo = the rounding error, exact in f16: d has 11
+//    is turned, once for all 128 rows, into two f16 tiles of the same layout whose sum is
+//    d q exactly (hi = d q rounded, lo = the rounding error, exact in f16: d has 11
 //    significant bits and q 7), with a power of two 2^-sigma folded in per tile (from the
 //    tile's largest scale) that keeps every hi below 2^15;
-//  * S = Q K^T: M 128 x N 64 x K 128 (two MMAs per K step for a q8_0 K: hi and lo) into 64
-//    tensor-memory columns; S is exact up to the f32 sums, as in the 16-bit path;
-//  * softmax by row (each thread its own row; base 2, lazy running maximum as in the decode
-//    kernels); P is written to shared memory as f16 hi + lo (P = P_h + P_l to ~22 bits);
+//  * S = Q K^T: M 128 x N 64 x K 128, Q in tensor memory, two MMAs per K step for a q8_0 K
+//    (hi and lo), into one of two 64-column score buffers;
+//  * softmax by row (one thread per row; base 2, lazy running maximum as in the decode
+//    kernels); P goes to tensor memory as f16 hi + lo (P = P_h + P_l to ~22 bits);
 //  * O += P V: M 128 x N 128 x K 64, V as an MN-major operand straight from the tile layout;
 //    P_h V_h + P_l V_h (+ P_h V_l for a q8_0 V), O in 128 tensor-memory columns.  A q8_0 V
 //    tile carries its own 2^-sigma; O is kept in units of the largest sigma so far and
 //    rescaled (with the lazy maximum's rescale) when it grows.
-// Each step waits for the previous one (one tile in flight on the tensor cores); every wait
-// is bounded and a timeout is reported in the K store's status word.
+// Warp roles, linked by mbarriers only (no CTA-wide barrier inside the tile loop):
+//  warps 0-3 softmax (rows 32 w .. 32 w + 31, their tensor-memory lanes), warp 4 issues the
+//  MMAs (S of tile t, then PV of tile t - 1, so the tensor cores compute S(t) during the
+//  softmax of tile t - 1), warp 5 loads tiles, warps 6-9 convert q8_0 tiles (double
+//  buffered).  Every wait is bounded; a wait that runs out raises a CTA-wide abort flag that
+//  the other waits watch, and the timeout is reported in the K store's status word.
 #pragma once
 
 #include "kvq_decode_mma.cuh"
@@ -31,15 +35,17 @@ namespace prefill_tc {
 using namespace kvq::mma;
 
 constexpr int kD = 128;
-constexpr int kRows = 128;        // query rows per CTA = threads = tensor-memory lanes
-constexpr int kThreads = 128;
-constexpr int kStages = 3;
-constexpr int kTmemCols = 256;    // S: columns 0..63, O: columns 128..255
-constexpr int kTile16 = kT * kD * 2;   // one 64 x 128 f16 operand tile (16 KB)
+constexpr int kRows = 128;              // query rows per CTA = tensor-memory lanes
+constexpr int kTile16 = kT * kD * 2;    // one 64 x 128 f16 operand tile (16 KB)
+constexpr int kTmemCols = 512;
+// tensor-memory columns: S buffers 0 and 64, O 128, P buffers (hi 32, lo 32) 256 and 320, Q 384
+constexpr uint32_t kColO = 128, kColP = 256, kColQ = 384;
+constexpr int kSoftmaxWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kConvWarp0 = 6, kConvWarps = 4;
 
 template <int KC, int VC>
 struct TCfg {
-  static constexpr bool KQ = KC == KVQ_CODEC_Q8_0, VQ = VC == KVQ_CODEC_Q8_0;
+  static constexpr bool KQ = KC == KVQ_CODEC_Q8_0, VQ = VC == KVQ_CODEC_Q8_0, CONV = KQ || VQ;
+  static constexpr int THREADS = 32 * (CONV ? kConvWarp0 + kConvWarps : kConvWarp0);
   static constexpr int NB = kD / kBlock;
   static constexpr int KRB = KQ ? kD : 2 * kD, VRB = VQ ? kD : 2 * kD;
   static constexpr int KROWS = kT * KRB, VROWS = kT * VRB;
@@ -47,15 +53,22 @@ struct TCfg {
   static constexpr int V_OFF = KROWS, KSC_OFF = KROWS + VROWS, VSC_OFF = KSC_OFF + KSC;
   static constexpr int al1k(int x) { return (x + 1023) / 1024 * 1024; }
   static constexpr int STAGE = al1k(KROWS + VROWS + KSC + VSC);
-  static constexpr int KH_OFF = kStages * STAGE;                 // converted K: hi, lo
-  static constexpr int VH_OFF = KH_OFF + (KQ ? 2 * kTile16 : 0);  // converted V: hi, lo
-  static constexpr int Q_OFF = VH_OFF + (VQ ? 2 * kTile16 : 0);   // Q: 128 rows x 128 f16
-  static constexpr int P_OFF = Q_OFF + kRows * kD * 2;            // P hi, P lo: 128 x 64 f16 each
-  static constexpr int BAR_OFF = P_OFF + 2 * kRows * kT * 2;      // full[kStages], s_done, o_done
-  static constexpr int MISC_OFF = BAR_OFF + 8 * (kStages + 2);    // tensor-memory base, stage flags
+  static constexpr int FIXED = (KQ ? 4 * kTile16 : 0) + (VQ ? 4 * kTile16 : 0) + 2048;
+  static constexpr int NST0 = (227 * 1024 - 1024 - FIXED) / STAGE;
+  static constexpr int NST = NST0 > 6 ? 6 : NST0;                 // TMA stages
+  static constexpr int KC_OFF = NST * STAGE;                       // converted K: 2 x (hi, lo)
+  static constexpr int VC_OFF = KC_OFF + (KQ ? 4 * kTile16 : 0);   // converted V: 2 x (hi, lo)
+  static constexpr int BAR_OFF = VC_OFF + (VQ ? 4 * kTile16 : 0);
+  // barriers: full[NST], empty[NST], then pairs kc_full, kc_empty, vc_full, vc_empty, s_full,
+  // s_empty, p_full, p_empty, then q_full, drain
+  static constexpr int NBAR = 2 * NST + 16 + 2;
+  static constexpr int MISC_OFF = BAR_OFF + 8 * NBAR;              // tensor-memory base, abort, stage flags
   static constexpr int SMEM = MISC_OFF + 64 + 1024;
   static constexpr uint32_t TX = KROWS + VROWS + KSC + VSC;
-  static_assert(SMEM <= 227 * 1024, "shared memory");
+  // arrivals that release a stage: softmax warps (flags, scales), converter warps, and the
+  // MMA warp's commit when an MMA reads the stage itself
+  static constexpr int EMPTY_COUNT = kSoftmaxWarps + (CONV ? kConvWarps : 0) + (KQ && VQ ? 0 : 1);
+  static_assert(NST >= 3 && SMEM <= 227 * 1024, "shared memory");
 };
 
 // Byte offset of 16-byte chunk `c` (8 elements of 16 bits) of row `t` in a tile of 64-row
@@ -79,12 +92,13 @@ __device__ __forceinline__ int tile_sigma(const uint8_t* sc, int lane, int n_val
 
 // q8_0 tile (TMA layout, one 128-byte line per row) + its scales -> f16 hi and lo tiles of
 // the two-region layout, d q 2^-sigma = hi + lo exactly; rows >= n_valid become zeros.
-__device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* sc, uint8_t* dst, int tid,
+// Thread ct of nct converts 16-code chunks ct, ct + nct, ...
+__device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* sc, uint8_t* dst, int ct, int nct,
                                            int n_valid, int sigma) {
   const float f = __uint_as_float((uint32_t)(127 - sigma) << 23);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int i = tid + kThreads * u, t = i >> 3, c = i & 7;   // row, 16-code chunk
+#pragma unroll 2
+  for (int i = ct; i < kT * 8; i += nct) {
+    const int t = i >> 3, c = i & 7;   // row, 16-code chunk
     uint32_t hi[8], lo[8];
     if (t < n_valid) {
       const uint4 w = *reinterpret_cast<const uint4*>(rows + t * 128 + (((c ^ (t & 7)) << 4)));
@@ -96,8 +110,7 @@ __device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* s
         const uint32_t q2 = hsub2_u32(i8pair_raw(ws[k >> 1], (k & 1) ? 0x4342 : 0x4140), 0x64806480u);
         __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&q2), *reinterpret_cast<const __half2*>(&d2));
         hi[k] = *reinterpret_cast<uint32_t*>(&h);
-        const uint32_t nh = hi[k] ^ 0x80008000u;
-        lo[k] = hfma2_u32(q2, d2, nh);
+        lo[k] = hfma2_u32(q2, d2, hi[k] ^ 0x80008000u);   // the product's rounding error, exact
       }
     } else {
 #pragma unroll
@@ -111,16 +124,38 @@ __device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* s
   }
 }
 
+// Bounded wait of a whole warp for the phase of parity `parity`; gives up (false) at the
+// limit, raising the abort flag, or as soon as another role has raised it.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  for (int it = 0; it < kTimeoutIters; ++it) {
+    if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+// One arrival per warp (lane 0, after the warp's own work).
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 template <int KC, int VC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TCfg<KC, VC>::THREADS, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   PrefillArgs a) {
   using C = TCfg<KC, VC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + C::BAR_OFF, bar_s = bar_full + 8 * kStages, bar_o = bar_s + 8;
+  const uint32_t bars = sbase + C::BAR_OFF;
+  const uint32_t bar_full = bars, bar_empty = bars + 8 * C::NST;
+  const uint32_t pairs = bar_empty + 8 * C::NST;   // each pair: buffer 0, buffer 1
+  const uint32_t kc_full = pairs, kc_empty = pairs + 16, vc_full = pairs + 32, vc_empty = pairs + 48;
+  const uint32_t s_full = pairs + 64, s_empty = pairs + 80, p_full = pairs + 96, p_empty = pairs + 112;
+  const uint32_t q_full = pairs + 128, bar_drain = pairs + 136;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile int* stage_ok = reinterpret_cast<volatile int*>(misc + 4);
 
   const int rt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -150,13 +185,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   const long long kv_end_ll = min(L, L - T + i_last + 1);
   const int kv_end = kv_end_ll > 0 ? (int)kv_end_ll : 0;
   const int n_tiles = (kv_end + kT - 1) / kT;
-  const int r = row0 + tid;
-  const int lim = r < rows_total ? (int)(L - T + r / G) : -1;   // last position row r sees
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(bar_full + 8 * s, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, C::EMPTY_COUNT);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kc_full + 8 * i, kConvWarps);
+      mbar_init(kc_empty + 8 * i, 1);
+      mbar_init(vc_full + 8 * i, kConvWarps);
+      mbar_init(vc_empty + 8 * i, 1);
+      mbar_init(s_full + 8 * i, 1);
+      mbar_init(s_empty + 8 * i, kSoftmaxWarps);
+      mbar_init(p_full + 8 * i, kSoftmaxWarps);
+      mbar_init(p_empty + 8 * i, 1);
+    }
+    mbar_init(q_full, kSoftmaxWarps);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(sbase + C::MISC_OFF, kTmemCols);
@@ -164,272 +211,289 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = misc[0];
-  const uint32_t t_s = tmem, t_o = tmem + 128;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-  // ---------------------------------------------------------------- producer (warp 0)
-  auto load_page = [&](int tile) -> int {
-    const long long pos0 = (long long)tile * kT;
-    return pos0 < cap ? __ldg(pt + pos0 / P) : -1;
+  auto nv_of = [&](int t) -> int {   // valid rows of tile t (none when its page was bad)
+    return stage_ok[t % C::NST] ? min(kT, kv_end - t * kT) : 0;
   };
-  int pg_lo = -1, pg_hi = -1, pb = 0;
-  if (warp == 0) {
-    pg_lo = load_page(lane);
-    pg_hi = load_page(32 + lane);
-  }
-  auto page_of = [&](int t) -> int {
-    while (t >= pb + 32) {
-      pg_lo = pg_hi;
-      pb += 32;
-      pg_hi = load_page(pb + 32 + lane);
-    }
-    return __shfl_sync(0xffffffffu, pg_lo, t - pb);
-  };
-  auto issue_tile = [&](int tile, int page) {   // lane 0 of warp 0
-    const int s = tile % kStages;
-    const int rr0 = (tile * kT) % P;
-    const uint32_t full = bar_full + 8 * s;
-    const bool ok = page >= 0 && page < a.k.num_pages && page < a.v.num_pages;
-    stage_ok[s] = ok ? 1 : 0;
-    if (!ok) {
-      record_fault(a.k.status, KVQ_DEVICE_BAD_PAGE);
-      record_fault(a.v.status, KVQ_DEVICE_BAD_PAGE);
-      mbar_arrive(full);
-      return;
-    }
-    mbar_expect_tx(full, C::TX);
-    const uint32_t st = sbase + s * C::STAGE;
-#pragma unroll
-    for (int seg = 0; seg < C::KRB / 128; ++seg) tma_load_4d(st + seg * kT * 128, &tmk, seg * 128, rr0, kvh, page, full);
-#pragma unroll
-    for (int seg = 0; seg < C::VRB / 128; ++seg)
-      tma_load_4d(st + C::V_OFF + seg * kT * 128, &tmv, seg * 128, rr0, kvh, page, full);
-    if constexpr (C::KQ)
-      bulk_load(st + C::KSC_OFF, a.k.buf + ((long long)page * a.k.num_kv_heads + kvh) * a.k.slab_bytes +
-                                     (long long)P * C::KRB + (long long)rr0 * C::NB * 2,
-                kT * C::NB * 2, full);
-    if constexpr (C::VQ)
-      bulk_load(st + C::VSC_OFF, a.v.buf + ((long long)page * a.v.num_kv_heads + kvh) * a.v.slab_bytes +
-                                     (long long)P * C::VRB + (long long)rr0 * C::NB * 2,
-                kT * C::NB * 2, full);
-  };
-  if (warp == 0) {
-    for (int tile = 0; tile < n_tiles && tile < kStages; ++tile) {
-      const int page = page_of(tile);
-      if (lane == 0) issue_tile(tile, page);
-    }
-    __syncwarp();
-  }
-  int issued = min(n_tiles, kStages);
 
-  // ---------------------------------------------------------------- Q row -> f16 operand
-  {
-    const bool qv = r < rows_total;
-    const __nv_bfloat16* qrow =
-        a.q + (((long long)b * T + (qv ? r / G : 0)) * a.num_q_heads + (long long)kvh * G + (qv ? r % G : 0)) * kD;
-    uint8_t* qs = smem + C::Q_OFF;
-#pragma unroll 4
-    for (int c = 0; c < kD / 8; ++c) {
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (qv) {
-        const uint4 x = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-        const float2 f0 = unpack2<true>(x.x), f1 = unpack2<true>(x.y), f2 = unpack2<true>(x.z), f3 = unpack2<true>(x.w);
-        w = make_uint4(pack2<false>(f0.x, f0.y), pack2<false>(f1.x, f1.y), pack2<false>(f2.x, f2.y),
-                       pack2<false>(f3.x, f3.y));
+  if (warp == kLoadWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    auto load_page = [&](int tile) -> int {
+      const long long pos0 = (long long)tile * kT;
+      return pos0 < cap ? __ldg(pt + pos0 / P) : -1;
+    };
+    int pg_lo = load_page(lane), pg_hi = load_page(32 + lane), pb = 0;
+    int issued = 0;
+    for (; issued < n_tiles; ++issued) {
+      const int t = issued, s = t % C::NST;
+      if (t >= C::NST && !wait_phase(bar_empty + 8 * s, ((t / C::NST) - 1) & 1, abort_flag)) break;
+      while (t >= pb + 32) {
+        pg_lo = pg_hi;
+        pb += 32;
+        pg_hi = load_page(pb + 32 + lane);
       }
-      *reinterpret_cast<uint4*>(qs + (c >> 3) * (kRows * 128) + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) = w;
+      const int page = __shfl_sync(0xffffffffu, pg_lo, t - pb);
+      if (lane == 0) {
+        const int rr0 = (t * kT) % P;
+        const uint32_t full = bar_full + 8 * s;
+        const bool ok = page >= 0 && page < a.k.num_pages && page < a.v.num_pages;
+        stage_ok[s] = ok ? 1 : 0;
+        if (!ok) {
+          record_fault(a.k.status, KVQ_DEVICE_BAD_PAGE);
+          record_fault(a.v.status, KVQ_DEVICE_BAD_PAGE);
+          mbar_arrive(full);
+        } else {
+          mbar_expect_tx(full, C::TX);
+          const uint32_t st = sbase + s * C::STAGE;
+#pragma unroll
+          for (int seg = 0; seg < C::KRB / 128; ++seg)
+            tma_load_4d(st + seg * kT * 128, &tmk, seg * 128, rr0, kvh, page, full);
+#pragma unroll
+          for (int seg = 0; seg < C::VRB / 128; ++seg)
+            tma_load_4d(st + C::V_OFF + seg * kT * 128, &tmv, seg * 128, rr0, kvh, page, full);
+          if constexpr (C::KQ)
+            bulk_load(st + C::KSC_OFF, a.k.buf + ((long long)page * a.k.num_kv_heads + kvh) * a.k.slab_bytes +
+                                           (long long)P * C::KRB + (long long)rr0 * C::NB * 2,
+                      kT * C::NB * 2, full);
+          if constexpr (C::VQ)
+            bulk_load(st + C::VSC_OFF, a.v.buf + ((long long)page * a.v.num_kv_heads + kvh) * a.v.slab_bytes +
+                                           (long long)P * C::VRB + (long long)rr0 * C::NB * 2,
+                      kT * C::NB * 2, full);
+        }
+      }
+      __syncwarp();
     }
-  }
-
-  const uint32_t idS = tc::idesc_f16(kRows, kT, false), idO = tc::idesc_f16(kRows, kD, true);
-  const uint32_t sQ = sbase + C::Q_OFF, sPh = sbase + C::P_OFF, sPl = sPh + kRows * kT * 2;
-  uint8_t* const ph_row = smem + C::P_OFF + tid * 128;
-  uint8_t* const pl_row = ph_row + kRows * kT * 2;
-  float m = -INFINITY, l = 0.0f;
-  int sv_run = -1000;          // exponent of O's unit 2^-sv_run (q8_0 V)
-  int n_s = 0, n_o = 0;        // S and PV rounds committed
-  bool o_pending = false, timed_out = false;
-
-  int tile = 0;
-  for (; tile < n_tiles; ++tile) {
-    const int s = tile % kStages;
-    const uint32_t st = sbase + s * C::STAGE;
-    bool ok = true;
-    if (o_pending) {   // the previous PV round is done: P, the operand tiles and O are free
-      ok = mbar_wait_warp(bar_o, (n_o - 1) & 1);
-      o_pending = !ok;
+    if (*abort_flag) {
+      // copies still in flight land before the CTA leaves (bounded)
+      for (int t = max(0, issued - C::NST); t < issued; ++t)
+        mbar_wait_warp(bar_full + 8 * (t % C::NST), (t / C::NST) & 1, 1 << 16);
     }
-    ok = mbar_wait_warp(bar_full + 8 * s, (tile / kStages) & 1) && ok;
-    if (__syncthreads_or(!ok)) {
-      timed_out = true;
-      break;
-    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issue
+    const uint32_t idS = tc::idesc_f16(kRows, kT, false), idO = tc::idesc_f16(kRows, kD, true);
+    bool ok = wait_phase(q_full, 0, abort_flag);
     tc::fence_after_sync();
-    // refill the stage of the previous tile (its data are converted or read by finished MMAs)
-    if (tile > 0 && issued < n_tiles) {
-      if (warp == 0) {
-        const int page = page_of(issued);
-        if (lane == 0) issue_tile(issued, page);
+    for (int t = 0; ok && t <= n_tiles; ++t) {
+      if (t < n_tiles) {   // S(t) into score buffer t & 1
+        const int bb = t & 1;
+        ok = C::KQ ? wait_phase(kc_full + 8 * bb, (t >> 1) & 1, abort_flag)
+                   : wait_phase(bar_full + 8 * (t % C::NST), (t / C::NST) & 1, abort_flag);
+        if (ok && t >= 2) ok = wait_phase(s_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        if (lane == 0) {
+          const uint32_t kb = C::KQ ? sbase + C::KC_OFF + bb * 2 * kTile16 : sbase + (t % C::NST) * C::STAGE;
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint64_t bd = tc::sdesc_sw128(kb + (ks >> 2) * (kT * 128) + (ks & 3) * 32, 16, 1024);
+            tc::mma_f16_ta(tmem + 64 * bb, tmem + kColQ + 8 * ks, bd, idS, ks > 0);
+            if constexpr (C::KQ) {
+              const uint64_t bl = tc::sdesc_sw128(kb + kTile16 + (ks >> 2) * (kT * 128) + (ks & 3) * 32, 16, 1024);
+              tc::mma_f16_ta(tmem + 64 * bb, tmem + kColQ + 8 * ks, bl, idS, true);
+            }
+          }
+          tc::mma_commit(s_full + 8 * bb);
+          if constexpr (C::KQ) tc::mma_commit(kc_empty + 8 * bb);
+        }
         __syncwarp();
       }
-      ++issued;
-    }
-    if (stage_ok[s] == 0) continue;
-    const int pos0 = tile * kT;
-    const int n_valid = min(kT, kv_end - pos0);
-
-    // ---------------------------------------------------------------- operand tiles
-    int sk = 0, svt = 0;
-    uint32_t kb = st, vb = st + C::V_OFF;
-    if constexpr (C::KQ) {
-      sk = tile_sigma(smem + s * C::STAGE + C::KSC_OFF, lane, n_valid);
-      convert_q8(smem + s * C::STAGE, smem + s * C::STAGE + C::KSC_OFF, smem + C::KH_OFF, tid, n_valid, sk);
-      kb = sbase + C::KH_OFF;
-    }
-    if constexpr (C::VQ) {
-      svt = tile_sigma(smem + s * C::STAGE + C::VSC_OFF, lane, n_valid);
-      convert_q8(smem + s * C::STAGE + C::V_OFF, smem + s * C::STAGE + C::VSC_OFF, smem + C::VH_OFF, tid, n_valid,
-                 svt);
-      vb = sbase + C::VH_OFF;
-    } else if (n_valid < kT) {
-      // rows past the length hold whatever the page holds: zero them (0 x NaN would reach O)
-      uint8_t* vt = smem + s * C::STAGE + C::V_OFF;
-      for (int i = tid; i < (kT - n_valid) * 16; i += kThreads) {
-        const int t = n_valid + (i >> 4), c = i & 15;
-        *reinterpret_cast<uint4*>(vt + tile_chunk(t, c)) = make_uint4(0u, 0u, 0u, 0u);
+      if (t >= 1) {   // PV(t - 1)
+        const int u = t - 1, bb = u & 1;
+        ok = wait_phase(p_full + 8 * bb, (u >> 1) & 1, abort_flag);
+        if (ok) {
+          if constexpr (C::VQ) ok = wait_phase(vc_full + 8 * bb, (u >> 1) & 1, abort_flag);
+          else ok = wait_phase(bar_full + 8 * (u % C::NST), (u / C::NST) & 1, abort_flag);
+        }
+        if (!ok) break;
+        tc::fence_after_sync();
+        if (lane == 0) {
+          const uint32_t vb = C::VQ ? sbase + C::VC_OFF + bb * 2 * kTile16 : sbase + (u % C::NST) * C::STAGE + C::V_OFF;
+          const uint32_t ph = tmem + kColP + 64 * bb, pl = ph + 32;
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk) {
+            const uint64_t bh = tc::sdesc_sw128(vb + kk * 2048, kT * 128, 1024);
+            tc::mma_f16_ta(tmem + kColO, ph + 8 * kk, bh, idO, u > 0 || kk > 0);
+            tc::mma_f16_ta(tmem + kColO, pl + 8 * kk, bh, idO, true);
+            if constexpr (C::VQ) {
+              const uint64_t bl = tc::sdesc_sw128(vb + kTile16 + kk * 2048, kT * 128, 1024);
+              tc::mma_f16_ta(tmem + kColO, ph + 8 * kk, bl, idO, true);
+            }
+          }
+          tc::mma_commit(p_empty + 8 * bb);
+          if constexpr (C::VQ) tc::mma_commit(vc_empty + 8 * bb);
+          if constexpr (!(C::KQ && C::VQ)) tc::mma_commit(bar_empty + 8 * (u % C::NST));
+        }
+        __syncwarp();
       }
     }
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    // ---------------------------------------------------------------- S = Q K^T
-    if (tid == 0) {
-#pragma unroll
-      for (int ks = 0; ks < kD / 16; ++ks) {
-        const uint64_t ad = tc::sdesc_sw128(sQ + (ks >> 2) * (kRows * 128) + (ks & 3) * 32, 16, 1024);
-        const uint64_t bd = tc::sdesc_sw128(kb + (ks >> 2) * (kT * 128) + (ks & 3) * 32, 16, 1024);
-        tc::mma_f16(t_s, ad, bd, idS, ks > 0);
+    // every MMA issued is complete before the CTA leaves
+    if (lane == 0) tc::mma_commit(bar_drain);
+    mbar_wait_warp(bar_drain, 0, 1 << 20);
+  } else if (warp >= kConvWarp0) {
+    // ---------------------------------------------------------------- q8_0 tile conversion
+    if constexpr (C::CONV) {
+      const int ct = tid - 32 * kConvWarp0, nct = 32 * kConvWarps;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % C::NST, bb = t & 1;
+        if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag)) break;
+        const int nv = nv_of(t);
+        const uint8_t* st = smem + s * C::STAGE;
         if constexpr (C::KQ) {
-          const uint64_t bl = tc::sdesc_sw128(kb + kTile16 + (ks >> 2) * (kT * 128) + (ks & 3) * 32, 16, 1024);
-          tc::mma_f16(t_s, ad, bl, idS, true);
+          if (t >= 2 && !wait_phase(kc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag)) break;
+          convert_q8(st, st + C::KSC_OFF, smem + C::KC_OFF + bb * 2 * kTile16, ct, nct, nv,
+                     tile_sigma(st + C::KSC_OFF, lane, nv));
+          tc::fence_smem_to_async();
+          warp_arrive(kc_full + 8 * bb, lane);
         }
-      }
-      tc::mma_commit(bar_s);
-    }
-    ++n_s;
-    if (__syncthreads_or(!mbar_wait_warp(bar_s, (n_s - 1) & 1))) {
-      timed_out = true;
-      break;
-    }
-    tc::fence_after_sync();
-
-    // ---------------------------------------------------------------- softmax of this row
-    float x[kT];
-    tc::tmem_ld32(t_s + lane_off, x);
-    tc::tmem_ld32(t_s + lane_off + 32, x + 32);
-    const float mul = a.qk_scale_log2 * __uint_as_float((uint32_t)(127 + sk) << 23);
-    float mx = -INFINITY;
-    if (pos0 + kT - 1 <= lim) {
-#pragma unroll
-      for (int j = 0; j < kT; ++j) {
-        x[j] *= mul;
-        mx = fmaxf(mx, x[j]);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kT; ++j) {
-        x[j] = pos0 + j <= lim ? x[j] * mul : -INFINITY;
-        mx = fmaxf(mx, x[j]);
-      }
-    }
-    const int sv_new = C::VQ ? max(sv_run, svt) : 0;
-    float fo = 1.0f;   // this row's O rescale factor
-    if (mx > m + kLazy || sv_new != sv_run) {
-      const float nm = mx > m + kLazy ? mx : m;
-      const float fm = m == -INFINITY ? 1.0f : fast_exp2(m - nm);
-      // l is a sum of true p; O also carries the V tiles' unit 2^-sv_run
-      l *= fm;
-      m = nm;
-      fo = fm * (C::VQ && sv_run > -1000 ? __uint_as_float((uint32_t)(127 + sv_run - sv_new) << 23) : 1.0f);
-    }
-    sv_run = sv_new;
-    // tensor-memory loads and stores are warp-wide (.sync.aligned): a warp rescales its 32
-    // rows together, each by its own factor (1 where nothing moved)
-    if (__any_sync(0xffffffffu, n_o > 0 && fo != 1.0f)) {
-#pragma unroll 1
-      for (int c = 0; c < kD / 32; ++c) {
-        float ov[32];
-        tc::tmem_ld32(t_o + lane_off + 32 * c, ov);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] *= fo;
-        tc::tmem_st32(t_o + lane_off + 32 * c, ov);
-      }
-    }
-    // p = 2^(x - m) (0 for masked entries and rows that saw nothing); the MMA takes p 2^(svt - sv_run)
-    const float base = m == -INFINITY ? 0.0f : m;
-    const float vsc = C::VQ ? __uint_as_float((uint32_t)(127 + svt - sv_run) << 23) : 1.0f;
-    float lsum = 0.0f;
-#pragma unroll
-    for (int c = 0; c < kT / 8; ++c) {
-      uint32_t h[4], lo4[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float p0 = fast_exp2(x[8 * c + 2 * k] - base), p1 = fast_exp2(x[8 * c + 2 * k + 1] - base);
-        lsum += p0 + p1;
-        split2<false>(p0 * vsc, p1 * vsc, h[k], lo4[k]);
-      }
-      const uint32_t co = (uint32_t)(((c ^ (tid & 7)) << 4));
-      *reinterpret_cast<uint4*>(ph_row + co) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(pl_row + co) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
-    }
-    l += lsum;
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    // ---------------------------------------------------------------- O += P V
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk) {
-        const uint64_t ah = tc::sdesc_sw128(sPh + kk * 32, 16, 1024);
-        const uint64_t al = tc::sdesc_sw128(sPl + kk * 32, 16, 1024);
-        const uint64_t bh = tc::sdesc_sw128(vb + kk * 2048, kT * 128, 1024);
-        tc::mma_f16(t_o, ah, bh, idO, n_o > 0 || kk > 0);
-        tc::mma_f16(t_o, al, bh, idO, true);
         if constexpr (C::VQ) {
-          const uint64_t bl = tc::sdesc_sw128(vb + kTile16 + kk * 2048, kT * 128, 1024);
-          tc::mma_f16(t_o, ah, bl, idO, true);
+          if (t >= 2 && !wait_phase(vc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag)) break;
+          convert_q8(st + C::V_OFF, st + C::VSC_OFF, smem + C::VC_OFF + bb * 2 * kTile16, ct, nct, nv,
+                     tile_sigma(st + C::VSC_OFF, lane, nv));
+          tc::fence_smem_to_async();
+          warp_arrive(vc_full + 8 * bb, lane);
+        }
+        warp_arrive(bar_empty + 8 * s, lane);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax (warps 0-3)
+    const int r = row0 + tid;
+    const int lim = r < rows_total ? (int)(L - T + r / G) : -1;   // last position row r sees
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Q row -> f16 pairs in tensor-memory columns kColQ .. + 63
+    {
+      const bool qv = r < rows_total;
+      const __nv_bfloat16* qrow =
+          a.q + (((long long)b * T + (qv ? r / G : 0)) * a.num_q_heads + (long long)kvh * G + (qv ? r % G : 0)) * kD;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 x = make_uint4(0u, 0u, 0u, 0u);
+          if (qv) x = *reinterpret_cast<const uint4*>(qrow + 64 * h + 8 * c);
+          const float2 f0 = unpack2<true>(x.x), f1 = unpack2<true>(x.y), f2 = unpack2<true>(x.z),
+                       f3 = unpack2<true>(x.w);
+          w[4 * c + 0] = __uint_as_float(pack2<false>(f0.x, f0.y));
+          w[4 * c + 1] = __uint_as_float(pack2<false>(f1.x, f1.y));
+          w[4 * c + 2] = __uint_as_float(pack2<false>(f2.x, f2.y));
+          w[4 * c + 3] = __uint_as_float(pack2<false>(f3.x, f3.y));
+        }
+        tc::tmem_st32(tmem + lane_off + kColQ + 32 * h, w);
+      }
+      tc::fence_before_sync();
+      warp_arrive(q_full, lane);
+    }
+
+    float m = -INFINITY, l = 0.0f;
+    int sv_run = -1000;   // exponent of O's unit 2^-sv_run (q8_0 V)
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int s = t % C::NST, bb = t & 1, pos0 = t * kT;
+      // the tile's flags and prescale exponents, then the stage is this role's no more
+      if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag)) { ok = false; break; }
+      const int nv = nv_of(t);
+      const int sk = C::KQ ? tile_sigma(smem + s * C::STAGE + C::KSC_OFF, lane, nv) : 0;
+      const int svt = C::VQ ? tile_sigma(smem + s * C::STAGE + C::VSC_OFF, lane, nv) : 0;
+      if constexpr (!C::VQ) {
+        // V rows past the length (or of a bad page) hold whatever the stage holds: zero them
+        // before PV reads them (0 x NaN would reach O)
+        if (nv < kT) {
+          uint8_t* vt = smem + s * C::STAGE + C::V_OFF;
+          for (int i = tid; i < (kT - nv) * 16; i += 32 * kSoftmaxWarps) {
+            const int tt = nv + (i >> 4), c = i & 15;
+            *reinterpret_cast<uint4*>(vt + tile_chunk(tt, c)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          tc::fence_smem_to_async();
         }
       }
-      tc::mma_commit(bar_o);
-    }
-    ++n_o;
-    o_pending = true;
-  }
+      warp_arrive(bar_empty + 8 * s, lane);
 
-  // ---------------------------------------------------------------- drain, normalize, write
-  if (o_pending && !mbar_wait_warp(bar_o, (n_o - 1) & 1)) timed_out = true;
-  if (__syncthreads_or(timed_out)) {
-    // stages still being filled: wait (bounded) so that no copy lands after the CTA leaves
-    for (int t = tile; t < issued; ++t) mbar_wait_warp(bar_full + 8 * (t % kStages), (t / kStages) & 1, 1 << 16);
-    if (tid == 0) record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
-  }
-  tc::fence_after_sync();
-  {
-    // every lane takes part in the (warp-wide) tensor-memory loads; rows past the chunk store nothing
+      // scores of tile t
+      if (!wait_phase(s_full + 8 * bb, (t >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc::fence_after_sync();
+      float x[kT];
+      tc::tmem_ld32(tmem + lane_off + 64 * bb, x);
+      tc::tmem_ld32(tmem + lane_off + 64 * bb + 32, x + 32);
+      tc::fence_before_sync();
+      warp_arrive(s_empty + 8 * bb, lane);
+
+      const float mul = a.qk_scale_log2 * __uint_as_float((uint32_t)(127 + sk) << 23);
+      float mx = -INFINITY;
+      if (pos0 + kT - 1 <= lim && nv == kT) {
+#pragma unroll
+        for (int j = 0; j < kT; ++j) {
+          x[j] *= mul;
+          mx = fmaxf(mx, x[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kT; ++j) {
+          x[j] = (pos0 + j <= lim && j < nv) ? x[j] * mul : -INFINITY;
+          mx = fmaxf(mx, x[j]);
+        }
+      }
+      const int sv_new = C::VQ ? max(sv_run, svt) : 0;
+      float fo = 1.0f;   // this row's O rescale factor
+      if (mx > m + kLazy || sv_new != sv_run) {
+        const float nm = mx > m + kLazy ? mx : m;
+        const float fm = m == -INFINITY ? 1.0f : fast_exp2(m - nm);
+        // l is a sum of true p; O also carries the V tiles' unit 2^-sv_run
+        l *= fm;
+        m = nm;
+        fo = fm * (C::VQ && sv_run > -1000 ? __uint_as_float((uint32_t)(127 + sv_run - sv_new) << 23) : 1.0f);
+      }
+      sv_run = sv_new;
+      // O rescale (tensor-memory loads and stores are warp-wide: the warp's 32 rows together,
+      // each by its own factor) once PV(t - 1) is done
+      if (__any_sync(0xffffffffu, t > 0 && fo != 1.0f)) {
+        if (!wait_phase(p_empty + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          float ov[32];
+          tc::tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] *= fo;
+          tc::tmem_st32(tmem + lane_off + kColO + 32 * c, ov);
+        }
+      }
+      // p = 2^(x - m) (0 for masked entries and rows that saw nothing); PV takes p 2^(svt - sv_run)
+      const float base = m == -INFINITY ? 0.0f : m;
+      const float vsc = C::VQ ? __uint_as_float((uint32_t)(127 + svt - sv_run) << 23) : 1.0f;
+      float ph[32], pl[32];
+      float lsum = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float p0 = fast_exp2(x[2 * k] - base), p1 = fast_exp2(x[2 * k + 1] - base);
+        lsum += p0 + p1;
+        uint32_t h, lo;
+        split2<false>(p0 * vsc, p1 * vsc, h, lo);
+        ph[k] = __uint_as_float(h);
+        pl[k] = __uint_as_float(lo);
+      }
+      l += lsum;
+      // P buffer bb is free once PV(t - 2) is done
+      if (t >= 2 && !wait_phase(p_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+      tc::fence_after_sync();
+      tc::tmem_st32(tmem + lane_off + kColP + 64 * bb, ph);
+      tc::tmem_st32(tmem + lane_off + kColP + 64 * bb + 32, pl);
+      tc::fence_before_sync();
+      warp_arrive(p_full + 8 * bb, lane);
+    }
+    // O after the last PV
+    if (ok && n_tiles > 0) ok = wait_phase(p_empty + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort_flag);
+    tc::fence_after_sync();
     float* orow = r < rows_total
                       ? a.out + (((long long)b * T + r / G) * a.num_q_heads + (long long)kvh * G + r % G) * kD
                       : nullptr;
-    const float inv = (l > 0.0f && n_o > 0)
+    const float inv = (ok && l > 0.0f && n_tiles > 0)
                           ? (C::VQ ? __uint_as_float((uint32_t)(127 + sv_run) << 23) : 1.0f) / l
                           : 0.0f;
 #pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       float ov[32];
-      tc::tmem_ld32(t_o + lane_off + 32 * c, ov);
+      tc::tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);   // every lane: the load is warp-wide
       if (orow) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -439,9 +503,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
     }
   }
+
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0 && *abort_flag) record_fault(a.k.status, KVQ_DEVICE_TIMEOUT);
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 template <int KC, int VC>
@@ -460,7 +529,7 @@ cudaError_t launch(const PrefillArgs& a, int batch, const CUtensorMap& tmk, cons
   }
   const int rows = a.tokens * a.group;
   const dim3 grid((unsigned)((rows + kRows - 1) / kRows), a.k.num_kv_heads, batch);
-  e = launch_pdl(kern, grid, dim3(kThreads), C::SMEM, stream, tmk, tmv, a);
+  e = launch_pdl(kern, grid, dim3(C::THREADS), C::SMEM, stream, tmk, tmv, a);
   count_launch();
   return e;
 }
