@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -83,14 +84,22 @@ def hbm_peak():
 
 
 def kernel_sources_sha() -> str:
-    """Hash of the device-code sources the decode kernels are built from (every header of
-    the CUDA path and the tensor-core instantiation units; host-only files excluded)."""
-    h = hashlib.sha256()
+    """Hash of the device-code sources the decode kernels are built from: the tensor-core
+    decode instantiation units and every header they include, directly or not (the prefill
+    kernels' own headers are not among them)."""
     csrc = os.path.join(ROOT, "flash_decode_quantized_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith(".cuh") or (name.startswith("mma_") and name.endswith(".cu")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    files = sorted(n for n in os.listdir(csrc) if n.startswith("mma_") and n.endswith(".cu"))
+    todo, seen = list(files), set(files)
+    while todo:
+        for line in open(os.path.join(csrc, todo.pop())):
+            m = re.match(r'\s*#include\s+"([^"]+)"', line)
+            if m and m.group(1) not in seen and os.path.exists(os.path.join(csrc, m.group(1))):
+                seen.add(m.group(1))
+                todo.append(m.group(1))
+    h = hashlib.sha256()
+    for name in sorted(seen):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

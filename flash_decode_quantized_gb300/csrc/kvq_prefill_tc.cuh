@@ -12,18 +12,20 @@
 //    tile's largest scale) that keeps every hi below 2^15;
 //  * S = Q K^T: M 128 x N 64 x K 128, Q in tensor memory, two MMAs per K step for a q8_0 K
 //    (hi and lo), into one of two 64-column score buffers;
-//  * softmax by row (one thread per row; base 2, lazy running maximum as in the decode
-//    kernels); P goes to tensor memory as f16 hi + lo (P = P_h + P_l to ~22 bits);
+//  * softmax by row (two threads per row, one per 32-score half, the row maximum traded
+//    through shared memory; base 2, lazy running maximum as in the decode kernels); P goes
+//    to tensor memory as f16 hi + lo (P = P_h + P_l to ~22 bits);
 //  * O += P V: M 128 x N 128 x K 64, V as an MN-major operand straight from the tile layout;
 //    P_h V_h + P_l V_h (+ P_h V_l for a q8_0 V), O in 128 tensor-memory columns.  A q8_0 V
 //    tile carries its own 2^-sigma; O is kept in units of the largest sigma so far and
 //    rescaled (with the lazy maximum's rescale) when it grows.
 // Warp roles, linked by mbarriers only (no CTA-wide barrier inside the tile loop):
-//  warps 0-3 softmax (rows 32 w .. 32 w + 31, their tensor-memory lanes), warp 4 issues the
-//  MMAs (S of tile t, then PV of tile t - 1, so the tensor cores compute S(t) during the
-//  softmax of tile t - 1), warp 5 loads tiles, warps 6-9 convert q8_0 tiles (double
-//  buffered).  Every wait is bounded; a wait that runs out raises a CTA-wide abort flag that
-//  the other waits watch, and the timeout is reported in the K store's status word.
+//  warps 0-7 softmax (warp w: rows 32 (w % 4) .. + 31, its tensor-memory lanes, score half
+//  w / 4), warp 8 issues the MMAs (S of tile t, then PV of tile t - 1, so the tensor cores
+//  compute S(t) during the softmax of tile t - 1), warp 9 loads tiles, warps 10-17 convert
+//  q8_0 tiles (double buffered).  Every wait is bounded; a wait that runs out raises a
+//  CTA-wide abort flag that the other waits watch, and the timeout is reported in the K
+//  store's status word.
 #pragma once
 
 #include "kvq_decode_mma.cuh"
@@ -40,7 +42,7 @@ constexpr int kTile16 = kT * kD * 2;    // one 64 x 128 f16 operand tile (16 KB)
 constexpr int kTmemCols = 512;
 // tensor-memory columns: S buffers 0 and 64, O 128, P buffers (hi 32, lo 32) 256 and 320, Q 384
 constexpr uint32_t kColO = 128, kColP = 256, kColQ = 384;
-constexpr int kSoftmaxWarps = 4, kMmaWarp = 4, kLoadWarp = 5, kConvWarp0 = 6, kConvWarps = 4;
+constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kLoadWarp = 9, kConvWarp0 = 10, kConvWarps = 8;
 
 template <int KC, int VC>
 struct TCfg {
@@ -53,7 +55,7 @@ struct TCfg {
   static constexpr int V_OFF = KROWS, KSC_OFF = KROWS + VROWS, VSC_OFF = KSC_OFF + KSC;
   static constexpr int al1k(int x) { return (x + 1023) / 1024 * 1024; }
   static constexpr int STAGE = al1k(KROWS + VROWS + KSC + VSC);
-  static constexpr int FIXED = (KQ ? 4 * kTile16 : 0) + (VQ ? 4 * kTile16 : 0) + 2048;
+  static constexpr int FIXED = (KQ ? 4 * kTile16 : 0) + (VQ ? 4 * kTile16 : 0) + 2048 + 3 * 2 * kRows * 4;
   static constexpr int NST0 = (227 * 1024 - 1024 - FIXED) / STAGE;
   static constexpr int NST = NST0 > 6 ? 6 : NST0;                 // TMA stages
   static constexpr int KC_OFF = NST * STAGE;                       // converted K: 2 x (hi, lo)
@@ -63,7 +65,8 @@ struct TCfg {
   // s_empty, p_full, p_empty, then q_full, drain
   static constexpr int NBAR = 2 * NST + 16 + 2;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBAR;              // tensor-memory base, abort, stage flags
-  static constexpr int SMEM = MISC_OFF + 64 + 1024;
+  static constexpr int RED_OFF = MISC_OFF + 64;                    // row maxima [2 tiles][2 halves][rows], sums
+  static constexpr int SMEM = RED_OFF + 3 * 2 * kRows * 4 + 1024;
   static constexpr uint32_t TX = KROWS + VROWS + KSC + VSC;
   // arrivals that release a stage: softmax warps (flags, scales), converter warps, and the
   // MMA warp's commit when an MMA reads the stage itself
@@ -356,35 +359,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
     }
   } else {
-    // ---------------------------------------------------------------- softmax (warps 0-3)
-    const int r = row0 + tid;
+    // ---------------------------------------------------------------- softmax (warps 0-7)
+    const int row = tid & (kRows - 1), half = warp >> 2;   // tensor-memory lane, score half
+    const int r = row0 + row;
     const int lim = r < rows_total ? (int)(L - T + r / G) : -1;   // last position row r sees
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    // Q row -> f16 pairs in tensor-memory columns kColQ .. + 63
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    float* const red = reinterpret_cast<float*>(smem + C::RED_OFF);   // [tile & 1][half][row], sums
+    const int pair_bar = 1 + (warp & 3);   // named barrier of the two warps that share these rows
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(pair_bar), "r"(64) : "memory"); };
+    // Q row, dims 64 half .. + 63 -> f16 pairs in tensor-memory columns kColQ + 32 half ..
     {
       const bool qv = r < rows_total;
       const __nv_bfloat16* qrow =
-          a.q + (((long long)b * T + (qv ? r / G : 0)) * a.num_q_heads + (long long)kvh * G + (qv ? r % G : 0)) * kD;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        float w[32];
+          a.q + (((long long)b * T + (qv ? r / G : 0)) * a.num_q_heads + (long long)kvh * G + (qv ? r % G : 0)) * kD +
+          64 * half;
+      float w[32];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 x = make_uint4(0u, 0u, 0u, 0u);
-          if (qv) x = *reinterpret_cast<const uint4*>(qrow + 64 * h + 8 * c);
-          const float2 f0 = unpack2<true>(x.x), f1 = unpack2<true>(x.y), f2 = unpack2<true>(x.z),
-                       f3 = unpack2<true>(x.w);
-          w[4 * c + 0] = __uint_as_float(pack2<false>(f0.x, f0.y));
-          w[4 * c + 1] = __uint_as_float(pack2<false>(f1.x, f1.y));
-          w[4 * c + 2] = __uint_as_float(pack2<false>(f2.x, f2.y));
-          w[4 * c + 3] = __uint_as_float(pack2<false>(f3.x, f3.y));
-        }
-        tc::tmem_st32(tmem + lane_off + kColQ + 32 * h, w);
+      for (int c = 0; c < 8; ++c) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (qv) x = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+        const float2 f0 = unpack2<true>(x.x), f1 = unpack2<true>(x.y), f2 = unpack2<true>(x.z),
+                     f3 = unpack2<true>(x.w);
+        w[4 * c + 0] = __uint_as_float(pack2<false>(f0.x, f0.y));
+        w[4 * c + 1] = __uint_as_float(pack2<false>(f1.x, f1.y));
+        w[4 * c + 2] = __uint_as_float(pack2<false>(f2.x, f2.y));
+        w[4 * c + 3] = __uint_as_float(pack2<false>(f3.x, f3.y));
       }
+      tc::tmem_st32(tmem + lane_off + kColQ + 32 * half, w);
       tc::fence_before_sync();
       warp_arrive(q_full, lane);
     }
 
+    const int c0 = 32 * half;   // this thread's scores of a tile: columns c0 .. c0 + 31
     float m = -INFINITY, l = 0.0f;
     int sv_run = -1000;   // exponent of O's unit 2^-sv_run (q8_0 V)
     bool ok = true;
@@ -409,30 +415,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
       warp_arrive(bar_empty + 8 * s, lane);
 
-      // scores of tile t
+      // scores of tile t (this thread's half)
       if (!wait_phase(s_full + 8 * bb, (t >> 1) & 1, abort_flag)) { ok = false; break; }
       tc::fence_after_sync();
-      float x[kT];
-      tc::tmem_ld32(tmem + lane_off + 64 * bb, x);
-      tc::tmem_ld32(tmem + lane_off + 64 * bb + 32, x + 32);
+      float x[32];
+      tc::tmem_ld32(tmem + lane_off + 64 * bb + c0, x);
       tc::fence_before_sync();
       warp_arrive(s_empty + 8 * bb, lane);
 
-      const float mul = a.qk_scale_log2 * __uint_as_float((uint32_t)(127 + sk) << 23);
-      float mx = -INFINITY;
-      if (pos0 + kT - 1 <= lim && nv == kT) {
+      // row maximum of the raw scores (mul > 0), masked entries -inf; four independent chains
+      if (!(pos0 + c0 + 31 <= lim && c0 + 32 <= nv)) {
 #pragma unroll
-        for (int j = 0; j < kT; ++j) {
-          x[j] *= mul;
-          mx = fmaxf(mx, x[j]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < kT; ++j) {
-          x[j] = (pos0 + j <= lim && j < nv) ? x[j] * mul : -INFINITY;
-          mx = fmaxf(mx, x[j]);
-        }
+        for (int j = 0; j < 32; ++j)
+          if (!(pos0 + c0 + j <= lim && c0 + j < nv)) x[j] = -INFINITY;
       }
+      float mq[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+      for (int j = 4; j < 32; ++j) mq[j & 3] = fmaxf(mq[j & 3], x[j]);
+      float mr = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      red[(bb * 2 + half) * kRows + row] = mr;
+      pair_sync();
+      mr = fmaxf(mr, red[(bb * 2 + (half ^ 1)) * kRows + row]);
+      const float mul = a.qk_scale_log2 * __uint_as_float((uint32_t)(127 + sk) << 23);
+      const float mx = mr * mul;
+
       const int sv_new = C::VQ ? max(sv_run, svt) : 0;
       float fo = 1.0f;   // this row's O rescale factor
       if (mx > m + kLazy || sv_new != sv_run) {
@@ -445,45 +451,49 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
       sv_run = sv_new;
       // O rescale (tensor-memory loads and stores are warp-wide: the warp's 32 rows together,
-      // each by its own factor) once PV(t - 1) is done
+      // each by its own factor; this thread's 64 of the 128 columns) once PV(t - 1) is done
       if (__any_sync(0xffffffffu, t > 0 && fo != 1.0f)) {
         if (!wait_phase(p_empty + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
 #pragma unroll 1
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           float ov[32];
-          tc::tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);
+          tc::tmem_ld32(tmem + lane_off + kColO + 64 * half + 32 * c, ov);
 #pragma unroll
           for (int j = 0; j < 32; ++j) ov[j] *= fo;
-          tc::tmem_st32(tmem + lane_off + kColO + 32 * c, ov);
+          tc::tmem_st32(tmem + lane_off + kColO + 64 * half + 32 * c, ov);
         }
       }
-      // p = 2^(x - m) (0 for masked entries and rows that saw nothing); PV takes p 2^(svt - sv_run)
-      const float base = m == -INFINITY ? 0.0f : m;
+      // p = 2^(s mul - m) (0 for masked entries and rows that saw nothing); PV takes p 2^(svt - sv_run)
+      const float nb = m == -INFINITY ? 0.0f : -m;
       const float vsc = C::VQ ? __uint_as_float((uint32_t)(127 + svt - sv_run) << 23) : 1.0f;
-      float ph[32], pl[32];
-      float lsum = 0.0f;
+      float ph[16], pl[16];
+      float2 ls[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = fast_exp2(x[2 * k] - base), p1 = fast_exp2(x[2 * k + 1] - base);
-        lsum += p0 + p1;
+      for (int k = 0; k < 16; ++k) {
+        const float2 e = __ffma2_rn(make_float2(x[2 * k], x[2 * k + 1]), make_float2(mul, mul), make_float2(nb, nb));
+        const float2 p = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+        ls[k & 1] = __fadd2_rn(ls[k & 1], p);
         uint32_t h, lo;
-        split2<false>(p0 * vsc, p1 * vsc, h, lo);
+        split2<false>(p.x * vsc, p.y * vsc, h, lo);
         ph[k] = __uint_as_float(h);
         pl[k] = __uint_as_float(lo);
       }
-      l += lsum;
+      l += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
       // P buffer bb is free once PV(t - 2) is done
       if (t >= 2 && !wait_phase(p_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
       tc::fence_after_sync();
-      tc::tmem_st32(tmem + lane_off + kColP + 64 * bb, ph);
-      tc::tmem_st32(tmem + lane_off + kColP + 64 * bb + 32, pl);
+      tc::tmem_st16(tmem + lane_off + kColP + 64 * bb + 16 * half, ph);
+      tc::tmem_st16(tmem + lane_off + kColP + 64 * bb + 32 + 16 * half, pl);
       tc::fence_before_sync();
       warp_arrive(p_full + 8 * bb, lane);
     }
-    // O after the last PV
+    // O after the last PV; the row sum from both halves
     if (ok && n_tiles > 0) ok = wait_phase(p_empty + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort_flag);
     tc::fence_after_sync();
+    red[(4 + half) * kRows + row] = l;
+    pair_sync();
+    l += red[(4 + (half ^ 1)) * kRows + row];
     float* orow = r < rows_total
                       ? a.out + (((long long)b * T + r / G) * a.num_q_heads + (long long)kvh * G + r % G) * kD
                       : nullptr;
@@ -491,7 +501,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                           ? (C::VQ ? __uint_as_float((uint32_t)(127 + sv_run) << 23) : 1.0f) / l
                           : 0.0f;
 #pragma unroll 1
-    for (int c = 0; c < kD / 32; ++c) {
+    for (int c = 2 * half; c < 2 * half + 2; ++c) {
       float ov[32];
       tc::tmem_ld32(tmem + lane_off + kColO + 32 * c, ov);   // every lane: the load is warp-wide
       if (orow) {
