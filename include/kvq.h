@@ -257,11 +257,15 @@ kvq_status kvq_flash_decode_multi(const void* q, const kvq_store* k_store, const
  * [0, seq_lens[b] - num_tokens + i] (causal inside the chunk, everything before it).
  *   q    device bf16 [batch][num_tokens][num_q_heads][head_dim] (16-byte aligned)
  *   out  device fp32 [batch][num_tokens][num_q_heads][head_dim]
- * One launch, no workspace: a CTA owns 64 (token, head) query rows of one KV head and
- * streams the KV prefix once.  Built for head_dim 64, 128 and 256 and the pairs of
+ * One launch, no workspace; each CTA streams the KV prefix of one KV head once.  At
+ * head_dim 128 with K and V each q8_0 or f16 (four pairs) a CTA owns 128 (token, head)
+ * query rows on the 5th-generation tensor cores (scores, P and O in tensor memory, q8_0
+ * tiles turned once per CTA into exact f16 hi + lo operands); otherwise 64 rows on the
+ * warp-level MMA path, built for head_dim 64, 128 and 256 and the pairs of
  * kvq_flash_decode's tensor-core kernel (bf16/bf16, f16/f16, q8_0/bf16, q8_0/q8_0, q4s/q4s,
- * q8_0/q4s, q4s/q8_0, q4s/bf16); others give KVQ_ERR_UNSUPPORTED.  softmax_scale <= 0
- * selects 1/sqrt(head_dim).  Device faults as for kvq_flash_decode. */
+ * q8_0/q4s, q4s/q8_0, q4s/bf16).  Other pairs give KVQ_ERR_UNSUPPORTED.  Q must lie in the
+ * f16 range on both paths (it is rounded to f16 once).  softmax_scale <= 0 selects
+ * 1/sqrt(head_dim).  Device faults as for kvq_flash_decode. */
 kvq_status kvq_prefill_attention(const void* q, const kvq_store* k_store, const kvq_store* v_store,
                                  const int32_t* seq_lens, const int32_t* page_table, int max_pages,
                                  kvq_codec codec, float* out, int batch, int num_q_heads,
