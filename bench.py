@@ -703,6 +703,47 @@ def measure_e2e(torch, kvq, layer, flush, iters):
                           "timing": "one step at a time: the zero-copy step + synchronize, L2 evicted before, median"}}
 
 
+def prefill_cells(torch, kvq, flush):
+    """Chunked prefill attention at the 8B-class layer shape (pp512 at depth 32768): the f16
+    control, q8_0 K+V fused, and a separate dequantize pass + the f16 kernel; one row each
+    (medians of 6 event-timed launches, L2 evicted before each)."""
+    out = []
+    # the 512 chunk tokens are appended, then attend causally over the 33280-token store
+    depth, T = 32768, 512
+    times = {}
+    for arm in ("f16/f16", "q8_0/q8_0"):
+        layer = Layer(kvq, torch, WORKLOADS["layer8b"], arm, [depth + T], 0, seed=92)
+        qp = torch.randn((1, T, layer.hq, layer.d), device="cuda").to(torch.bfloat16)
+        outp = torch.empty((1, T, layer.hq, layer.d), dtype=torch.float32, device="cuda")
+
+        def pf(layer=layer, qp=qp, outp=outp):
+            kvq.kvq_prefill_attention(qp, layer.k_store, layer.v_store, layer.seq_lens, layer.page_table, out=outp)
+        time_decode_only(torch, layer, flush, 2, pf)
+        ms = statistics.median(time_decode_only(torch, layer, flush, 6, pf))
+        times[arm] = ms
+        flops = 4.0 * layer.d * layer.hq * sum(depth + i + 1 for i in range(T))
+        row = {"workload": "prefill_attention", "depth": depth, "chunk_tokens": T, "codec": arm,
+               "us": round(ms * 1e3, 1), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+        if arm == "q8_0/q8_0":
+            row["vs_f16_time"] = round(ms / times["f16/f16"], 3)
+            # unfused arm: the quantized store dequantized to f16 first, then the f16 kernel
+            kd = kvq.kvq_store_create("f16", layer.hkv, layer.d, layer.page_size, layer.k_store.num_pages)
+            vd = kvq.kvq_store_create("f16", layer.hkv, layer.d, layer.page_size, layer.k_store.num_pages)
+
+            def unf(layer=layer, qp=qp, outp=outp, kd=kd, vd=vd):
+                kvq.kvq_dequantize(layer.k_store, kd, layer.seq_lens, layer.page_table)
+                kvq.kvq_dequantize(layer.v_store, vd, layer.seq_lens, layer.page_table)
+                kvq.kvq_prefill_attention(qp, kd, vd, layer.seq_lens, layer.page_table, out=outp)
+            time_decode_only(torch, layer, flush, 2, unf)
+            um = statistics.median(time_decode_only(torch, layer, flush, 6, unf))
+            row["unfused_f16_us"] = round(um * 1e3, 1)
+            del kd, vd
+        out.append(row)
+        del layer
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_extras(torch, kvq, args, flush, peak):
     """The other workloads at full size: the long-context depth sweep (f16 control vs
     q8_0 K+V, GQA 16:1, D=256), the 64-sequence ragged paged batch, and the resident
@@ -758,41 +799,7 @@ def run_extras(torch, kvq, args, flush, peak):
                     "note": "bf16 K and V rows read, codes and scales written, one launch"})
         del ks, vs, rows_k, rows_v
         torch.cuda.empty_cache()
-    # chunked prefill attention (pp512 at depth 32768, 8B-class layer shape): the 512 chunk
-    # tokens are appended, then attend causally over the 33280-token store; q8_0 against
-    # the f16 control and against a separate dequantize pass + f16 prefill
-    depth, T = 32768, 512
-    times = {}
-    for arm in ("f16/f16", "q8_0/q8_0"):
-        layer = Layer(kvq, torch, WORKLOADS["layer8b"], arm, [depth + T], 0, seed=92)
-        qp = torch.randn((1, T, layer.hq, layer.d), device="cuda").to(torch.bfloat16)
-        outp = torch.empty((1, T, layer.hq, layer.d), dtype=torch.float32, device="cuda")
-
-        def pf(layer=layer, qp=qp, outp=outp):
-            kvq.kvq_prefill_attention(qp, layer.k_store, layer.v_store, layer.seq_lens, layer.page_table, out=outp)
-        time_decode_only(torch, layer, flush, 2, pf)
-        ms = statistics.median(time_decode_only(torch, layer, flush, 6, pf))
-        times[arm] = ms
-        flops = 4.0 * layer.d * layer.hq * sum(depth + i + 1 for i in range(T))
-        row = {"workload": "prefill_attention", "depth": depth, "chunk_tokens": T, "codec": arm,
-               "us": round(ms * 1e3, 1), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
-        if arm == "q8_0/q8_0":
-            row["vs_f16_time"] = round(ms / times["f16/f16"], 3)
-            # unfused arm: the quantized store dequantized to f16 first, then the f16 kernel
-            kd = kvq.kvq_store_create("f16", layer.hkv, layer.d, layer.page_size, layer.k_store.num_pages)
-            vd = kvq.kvq_store_create("f16", layer.hkv, layer.d, layer.page_size, layer.k_store.num_pages)
-
-            def unf(layer=layer, qp=qp, outp=outp, kd=kd, vd=vd):
-                kvq.kvq_dequantize(layer.k_store, kd, layer.seq_lens, layer.page_table)
-                kvq.kvq_dequantize(layer.v_store, vd, layer.seq_lens, layer.page_table)
-                kvq.kvq_prefill_attention(qp, kd, vd, layer.seq_lens, layer.page_table, out=outp)
-            time_decode_only(torch, layer, flush, 2, unf)
-            um = statistics.median(time_decode_only(torch, layer, flush, 6, unf))
-            row["unfused_f16_us"] = round(um * 1e3, 1)
-            del kd, vd
-        out.append(row)
-        del layer
-        torch.cuda.empty_cache()
+    out.extend(prefill_cells(torch, kvq, flush))
     # the same chunk at the long-context shape (GQA 16:1, head_dim 256)
     ptimes = {}
     for arm in ("f16/f16", "q8_0/q8_0"):
@@ -1018,6 +1025,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads' cells")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the chunked prefill cells (pp512 at depth 32768) and print them")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -1026,6 +1035,15 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, world)))
+        return
+    if args.prefill_only:
+        if rank == 0:
+            import torch
+            from flash_decode_quantized_gb300 import kvq
+            cells = prefill_cells(torch, kvq, l2_flusher(torch))
+            print(json.dumps({"metric": "chunked prefill attention us (pp512 at depth 32768, 8B-class layer)",
+                              "unit": "us", "higher_is_better": False, "cells": cells,
+                              "gpu_launches": kvq.kvq_launch_count()}))
         return
     if world > 1:
         import torch
