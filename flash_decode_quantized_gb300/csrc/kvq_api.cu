@@ -605,6 +605,7 @@ kvq_status kvq_prefill_attention(const void* q, const kvq_store* k_store, const 
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt((float)kd.head_dim);
   a.qk_scale_log2 = scale * 1.4426950408889634f;
   a.out = out;
+  fault_injection(&a.wait_limit, &a.skip_tile);
   const cudaError_t e = prefill_launch(kd.codec, vd.codec, a, batch, kd.head_dim, k_store->rows_map,
                                        v_store->rows_map, static_cast<cudaStream_t>(stream));
   return e == cudaErrorNotSupported ? KVQ_ERR_UNSUPPORTED : from_cuda(e);

@@ -125,6 +125,8 @@ struct PrefillArgs {
   int tokens;                 // T
   float qk_scale_log2;
   float* out;                 // [B][T][Hq][D]
+  int wait_limit;             // tries of each bounded mbarrier wait (tensor-core kernel)
+  int skip_tile;              // fault injection: tile the producer never issues (-1: none)
 };
 
 // Launchers implemented in the kernel translation units.  Each returns a CUDA error.

@@ -62,8 +62,9 @@ struct TCfg {
   static constexpr int VC_OFF = KC_OFF + (KQ ? 4 * kTile16 : 0);   // converted V: 2 x (hi, lo)
   static constexpr int BAR_OFF = VC_OFF + (VQ ? 4 * kTile16 : 0);
   // barriers: full[NST], empty[NST], then pairs kc_full, kc_empty, vc_full, vc_empty, s_full,
-  // s_empty, p_full, p_empty, then q_full, drain
-  static constexpr int NBAR = 2 * NST + 16 + 2;
+  // s_empty, p_full, p_empty, then q_full, drain, then the softmax row pairs' exchanges
+  // (per pair of warps: two tile parities and the final sums)
+  static constexpr int NBAR = 2 * NST + 16 + 2 + 12;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBAR;              // tensor-memory base, abort, stage flags
   static constexpr int RED_OFF = MISC_OFF + 64;                    // row maxima [2 tiles][2 halves][rows], sums
   static constexpr int SMEM = RED_OFF + 3 * 2 * kRows * 4 + 1024;
@@ -129,8 +130,8 @@ __device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* s
 
 // Bounded wait of a whole warp for the phase of parity `parity`; gives up (false) at the
 // limit, raising the abort flag, or as soon as another role has raised it.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  for (int it = 0; it < kTimeoutIters; ++it) {
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int limit) {
+  for (int it = 0; it < limit; ++it) {
     if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
     if (*abort_flag) return false;
   }
@@ -156,7 +157,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   const uint32_t pairs = bar_empty + 8 * C::NST;   // each pair: buffer 0, buffer 1
   const uint32_t kc_full = pairs, kc_empty = pairs + 16, vc_full = pairs + 32, vc_empty = pairs + 48;
   const uint32_t s_full = pairs + 64, s_empty = pairs + 80, p_full = pairs + 96, p_empty = pairs + 112;
-  const uint32_t q_full = pairs + 128, bar_drain = pairs + 136;
+  const uint32_t q_full = pairs + 128, bar_drain = pairs + 136, xch = pairs + 144;   // xch: [4][3]
+  const int wl = a.wait_limit;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile int* stage_ok = reinterpret_cast<volatile int*>(misc + 4);
@@ -206,6 +208,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     mbar_init(q_full, kSoftmaxWarps);
     mbar_init(bar_drain, 1);
+    for (int i = 0; i < 12; ++i) mbar_init(xch + 8 * i, 2);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -229,7 +232,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     int issued = 0;
     for (; issued < n_tiles; ++issued) {
       const int t = issued, s = t % C::NST;
-      if (t >= C::NST && !wait_phase(bar_empty + 8 * s, ((t / C::NST) - 1) & 1, abort_flag)) break;
+      if (t >= C::NST && !wait_phase(bar_empty + 8 * s, ((t / C::NST) - 1) & 1, abort_flag, wl)) break;
+      if (t == a.skip_tile) continue;   // fault injection: never issued (no copy, no arrival)
       while (t >= pb + 32) {
         pg_lo = pg_hi;
         pb += 32;
@@ -274,14 +278,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issue
     const uint32_t idS = tc::idesc_f16(kRows, kT, false), idO = tc::idesc_f16(kRows, kD, true);
-    bool ok = wait_phase(q_full, 0, abort_flag);
+    bool ok = wait_phase(q_full, 0, abort_flag, wl);
     tc::fence_after_sync();
     for (int t = 0; ok && t <= n_tiles; ++t) {
       if (t < n_tiles) {   // S(t) into score buffer t & 1
         const int bb = t & 1;
-        ok = C::KQ ? wait_phase(kc_full + 8 * bb, (t >> 1) & 1, abort_flag)
-                   : wait_phase(bar_full + 8 * (t % C::NST), (t / C::NST) & 1, abort_flag);
-        if (ok && t >= 2) ok = wait_phase(s_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag);
+        ok = C::KQ ? wait_phase(kc_full + 8 * bb, (t >> 1) & 1, abort_flag, wl)
+                   : wait_phase(bar_full + 8 * (t % C::NST), (t / C::NST) & 1, abort_flag, wl);
+        if (ok && t >= 2) ok = wait_phase(s_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl);
         if (!ok) break;
         tc::fence_after_sync();
         if (lane == 0) {
@@ -302,10 +306,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
       if (t >= 1) {   // PV(t - 1)
         const int u = t - 1, bb = u & 1;
-        ok = wait_phase(p_full + 8 * bb, (u >> 1) & 1, abort_flag);
+        ok = wait_phase(p_full + 8 * bb, (u >> 1) & 1, abort_flag, wl);
         if (ok) {
-          if constexpr (C::VQ) ok = wait_phase(vc_full + 8 * bb, (u >> 1) & 1, abort_flag);
-          else ok = wait_phase(bar_full + 8 * (u % C::NST), (u / C::NST) & 1, abort_flag);
+          if constexpr (C::VQ) ok = wait_phase(vc_full + 8 * bb, (u >> 1) & 1, abort_flag, wl);
+          else ok = wait_phase(bar_full + 8 * (u % C::NST), (u / C::NST) & 1, abort_flag, wl);
         }
         if (!ok) break;
         tc::fence_after_sync();
@@ -338,18 +342,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       const int ct = tid - 32 * kConvWarp0, nct = 32 * kConvWarps;
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % C::NST, bb = t & 1;
-        if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag)) break;
+        if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag, wl)) break;
         const int nv = nv_of(t);
         const uint8_t* st = smem + s * C::STAGE;
         if constexpr (C::KQ) {
-          if (t >= 2 && !wait_phase(kc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag)) break;
+          if (t >= 2 && !wait_phase(kc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) break;
           convert_q8(st, st + C::KSC_OFF, smem + C::KC_OFF + bb * 2 * kTile16, ct, nct, nv,
                      tile_sigma(st + C::KSC_OFF, lane, nv));
           tc::fence_smem_to_async();
           warp_arrive(kc_full + 8 * bb, lane);
         }
         if constexpr (C::VQ) {
-          if (t >= 2 && !wait_phase(vc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag)) break;
+          if (t >= 2 && !wait_phase(vc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) break;
           convert_q8(st + C::V_OFF, st + C::VSC_OFF, smem + C::VC_OFF + bb * 2 * kTile16, ct, nct, nv,
                      tile_sigma(st + C::VSC_OFF, lane, nv));
           tc::fence_smem_to_async();
@@ -365,8 +369,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int lim = r < rows_total ? (int)(L - T + r / G) : -1;   // last position row r sees
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float* const red = reinterpret_cast<float*>(smem + C::RED_OFF);   // [tile & 1][half][row], sums
-    const int pair_bar = 1 + (warp & 3);   // named barrier of the two warps that share these rows
-    auto pair_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(pair_bar), "r"(64) : "memory"); };
+    // exchanges with the other warp of these rows: bounded mbarrier waits (an abort cannot
+    // leave one of the two waiting for good)
+    const uint32_t my_xch = xch + 24 * (warp & 3);
     // Q row, dims 64 half .. + 63 -> f16 pairs in tensor-memory columns kColQ + 32 half ..
     {
       const bool qv = r < rows_total;
@@ -397,7 +402,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     for (int t = 0; t < n_tiles; ++t) {
       const int s = t % C::NST, bb = t & 1, pos0 = t * kT;
       // the tile's flags and prescale exponents, then the stage is this role's no more
-      if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag)) { ok = false; break; }
+      if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag, wl)) { ok = false; break; }
       const int nv = nv_of(t);
       const int sk = C::KQ ? tile_sigma(smem + s * C::STAGE + C::KSC_OFF, lane, nv) : 0;
       const int svt = C::VQ ? tile_sigma(smem + s * C::STAGE + C::VSC_OFF, lane, nv) : 0;
@@ -416,7 +421,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       warp_arrive(bar_empty + 8 * s, lane);
 
       // scores of tile t (this thread's half)
-      if (!wait_phase(s_full + 8 * bb, (t >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!wait_phase(s_full + 8 * bb, (t >> 1) & 1, abort_flag, wl)) { ok = false; break; }
       tc::fence_after_sync();
       float x[32];
       tc::tmem_ld32(tmem + lane_off + 64 * bb + c0, x);
@@ -434,7 +439,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       for (int j = 4; j < 32; ++j) mq[j & 3] = fmaxf(mq[j & 3], x[j]);
       float mr = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       red[(bb * 2 + half) * kRows + row] = mr;
-      pair_sync();
+      warp_arrive(my_xch + 8 * bb, lane);
+      if (!wait_phase(my_xch + 8 * bb, (t >> 1) & 1, abort_flag, wl)) { ok = false; break; }
       mr = fmaxf(mr, red[(bb * 2 + (half ^ 1)) * kRows + row]);
       const float mul = a.qk_scale_log2 * __uint_as_float((uint32_t)(127 + sk) << 23);
       const float mx = mr * mul;
@@ -453,7 +459,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       // O rescale (tensor-memory loads and stores are warp-wide: the warp's 32 rows together,
       // each by its own factor; this thread's 64 of the 128 columns) once PV(t - 1) is done
       if (__any_sync(0xffffffffu, t > 0 && fo != 1.0f)) {
-        if (!wait_phase(p_empty + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!wait_phase(p_empty + 8 * ((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, wl)) { ok = false; break; }
         tc::fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
@@ -481,7 +487,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
       l += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
       // P buffer bb is free once PV(t - 2) is done
-      if (t >= 2 && !wait_phase(p_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+      if (t >= 2 && !wait_phase(p_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) { ok = false; break; }
       tc::fence_after_sync();
       tc::tmem_st16(tmem + lane_off + kColP + 64 * bb + 16 * half, ph);
       tc::tmem_st16(tmem + lane_off + kColP + 64 * bb + 32 + 16 * half, pl);
@@ -489,10 +495,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       warp_arrive(p_full + 8 * bb, lane);
     }
     // O after the last PV; the row sum from both halves
-    if (ok && n_tiles > 0) ok = wait_phase(p_empty + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort_flag);
+    if (ok && n_tiles > 0) ok = wait_phase(p_empty + 8 * ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, abort_flag, wl);
     tc::fence_after_sync();
     red[(4 + half) * kRows + row] = l;
-    pair_sync();
+    warp_arrive(my_xch + 16, lane);
+    if (!wait_phase(my_xch + 16, 0, abort_flag, wl)) ok = false;
     l += red[(4 + (half ^ 1)) * kRows + row];
     float* orow = r < rows_total
                       ? a.out + (((long long)b * T + r / G) * a.num_q_heads + (long long)kvh * G + r % G) * kD

@@ -328,7 +328,7 @@ kvq_status kvq_flash_decode_static_ws(const void* q, const kvq_store* k_store,
  * no counterpart: it is how kernels that never trap report bad device data. */
 kvq_status kvq_store_get_error(kvq_store* store, int32_t* device_code);
 
-/* Number of decode/append/combine kernels this library has launched in this process
+/* Number of kernels (decode, append, combine, prefill, dequantize) this library has launched in this process
  * (a dispatch counter for benchmarks and tests: the pages prove their kernels ran by
  * counting dispatches, rMLX issue #295 "Finding" table and rMLX issue #292 "Symptom"). */
 uint64_t kvq_launch_count(void);

@@ -143,3 +143,30 @@ def test_device_timeout_is_recorded_and_the_next_call_runs(hq, hkv, d, kc, skip)
     assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
     assert torch.equal(got, want)
 
+
+
+@pytest.mark.parametrize("kc,vc,skip", [("q8_0", "q8_0", 2), ("f16", "f16", 0), ("q8_0", "f16", 1)])
+def test_prefill_device_timeout_is_recorded_and_the_next_call_runs(kc, vc, skip):
+    # The tensor-core prefill (head_dim 128): a tile that the producer never issues (no copy,
+    # no arrival) leaves the waits on it to run out; the CTA raises its abort flag, every
+    # role leaves its loop (the row-pair exchanges are bounded waits too), the copies it did
+    # issue are waited for, KVQ_DEVICE_TIMEOUT is recorded, and the next call is exact.
+    inp = make_inputs([1500, 300], 16, 4, 128, seed=47)
+    k = kvq()
+    ks = build_store(inp, kc, "k")
+    vs = build_store(inp, vc, "v")
+    _, sl, pt = device_inputs(inp)
+    T = 100
+    rng = np.random.default_rng(48)
+    q = torch.from_numpy(rng.standard_normal((inp.batch, T, 16, 128), dtype=np.float32)).cuda().to(torch.bfloat16)
+    want = k.kvq_prefill_attention(q, ks, vs, sl, pt)
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+    try:
+        k.kvq_set_fault_injection(4096, skip)
+        k.kvq_prefill_attention(q, ks, vs, sl, pt)
+        assert k.kvq_store_get_error(ks) == 4   # KVQ_DEVICE_TIMEOUT
+    finally:
+        k.kvq_set_fault_injection(0, -1)
+    got = k.kvq_prefill_attention(q, ks, vs, sl, pt)
+    assert k.kvq_store_get_error(ks) == 0 and k.kvq_store_get_error(vs) == 0
+    assert torch.equal(got, want)
