@@ -6,10 +6,11 @@
 // A CTA owns 128 query rows of one (sequence, KV head), row = token * G + head-in-group,
 // one per tensor-memory lane.  Per 64-token KV tile:
 //  * the tile arrives by TMA in the 128-byte swizzled layout that the MMA reads; a q8_0 tile
-//    is turned, once for all 128 rows, into two f16 tiles of the same layout whose sum is
-//    d q exactly (hi = d q rounded, lo = the rounding error, exact in f16: d has 11
-//    significant bits and q 7), with a power of two 2^-sigma folded in per tile (from the
-//    tile's largest scale) that keeps every hi below 2^15;
+//    is turned, once for all 128 rows, into two f16 tiles of the same layout that give d q
+//    exactly (hi = d q rounded, lo = its rounding error, exact in f16: d has 11 significant
+//    bits and q 7; lo is stored negated and read with the MMA's negate-B bit), with a power
+//    of two 2^-sigma folded in per tile (from the tile's largest scale) that keeps every hi
+//    below 2^15;
 //  * S = Q K^T: M 128 x N 64 x K 128, Q in tensor memory, two MMAs per K step for a q8_0 K
 //    (hi and lo), into one of two 64-column score buffers;
 //  * softmax by row (two threads per row, one per 32-score half, the row maximum traded
@@ -94,37 +95,49 @@ __device__ __forceinline__ int tile_sigma(const uint8_t* sc, int lane, int n_val
   return (int)(m >> 10) - 22;
 }
 
-// q8_0 tile (TMA layout, one 128-byte line per row) + its scales -> f16 hi and lo tiles of
-// the two-region layout, d q 2^-sigma = hi + lo exactly; rows >= n_valid become zeros.
-// Thread ct of nct converts 16-code chunks ct, ct + nct, ...
-__device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* sc, uint8_t* dst, int ct, int nct,
+// Shared-memory offsets of one 16-code chunk a converter thread handles in every tile: the
+// codes (TMA layout), its scale, and its two 16-byte destinations (the two-region layout).
+struct ConvItem {
+  uint32_t src, scale, dst0, dst1;
+  int row;
+};
+__device__ __forceinline__ ConvItem conv_item(int i) {
+  const int t = i >> 3, c = i & 7;   // row, 16-code chunk
+  return {(uint32_t)(t * 128 + ((c ^ (t & 7)) << 4)), (uint32_t)((t * 4 + (c >> 1)) * 2), tile_chunk(t, 2 * c),
+          tile_chunk(t, 2 * c + 1), t};
+}
+
+// q8_0 tile (TMA layout, one 128-byte line per row) + its scales -> f16 hi and negated lo
+// tiles of the two-region layout, d q 2^-sigma = hi - nlo exactly (nlo = hi - d q 2^-sigma,
+// the product's rounding error with its sign flipped: the MMAs that read it negate B);
+// rows >= n_valid become zeros.
+template <int NI>
+__device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* sc, uint8_t* dst, const ConvItem* it,
                                            int n_valid, int sigma) {
   const float f = __uint_as_float((uint32_t)(127 - sigma) << 23);
-#pragma unroll 2
-  for (int i = ct; i < kT * 8; i += nct) {
-    const int t = i >> 3, c = i & 7;   // row, 16-code chunk
+#pragma unroll
+  for (int u = 0; u < NI; ++u) {
     uint32_t hi[8], lo[8];
-    if (t < n_valid) {
-      const uint4 w = *reinterpret_cast<const uint4*>(rows + t * 128 + (((c ^ (t & 7)) << 4)));
-      const float d = __half2float(*reinterpret_cast<const __half*>(sc + (t * 4 + (c >> 1)) * 2)) * f;
-      const uint32_t d2 = pack2<false>(d, d);
+    if (it[u].row < n_valid) {
+      const uint4 w = *reinterpret_cast<const uint4*>(rows + it[u].src);
+      const float d = __half2float(*reinterpret_cast<const __half*>(sc + it[u].scale)) * f;
+      const uint32_t d2 = pack2<false>(d, d), nd2 = d2 ^ 0x80008000u;
       const uint32_t ws[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t q2 = hsub2_u32(i8pair_raw(ws[k >> 1], (k & 1) ? 0x4342 : 0x4140), 0x64806480u);
         __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&q2), *reinterpret_cast<const __half2*>(&d2));
         hi[k] = *reinterpret_cast<uint32_t*>(&h);
-        lo[k] = hfma2_u32(q2, d2, hi[k] ^ 0x80008000u);   // the product's rounding error, exact
+        lo[k] = hfma2_u32(q2, nd2, hi[k]);   // hi - d q, exact
       }
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) hi[k] = lo[k] = 0u;
     }
-    const int oc = 2 * c;   // f16 chunks 2c, 2c + 1 of the row (dims 16 c .. 16 c + 15)
-    *reinterpret_cast<uint4*>(dst + tile_chunk(t, oc)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(dst + tile_chunk(t, oc + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-    *reinterpret_cast<uint4*>(dst + kTile16 + tile_chunk(t, oc)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4*>(dst + kTile16 + tile_chunk(t, oc + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    *reinterpret_cast<uint4*>(dst + it[u].dst0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(dst + it[u].dst1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    *reinterpret_cast<uint4*>(dst + kTile16 + it[u].dst0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(dst + kTile16 + it[u].dst1) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
   }
 }
 
@@ -296,7 +309,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             tc::mma_f16_ta(tmem + 64 * bb, tmem + kColQ + 8 * ks, bd, idS, ks > 0);
             if constexpr (C::KQ) {
               const uint64_t bl = tc::sdesc_sw128(kb + kTile16 + (ks >> 2) * (kT * 128) + (ks & 3) * 32, 16, 1024);
-              tc::mma_f16_ta(tmem + 64 * bb, tmem + kColQ + 8 * ks, bl, idS, true);
+              tc::mma_f16_ta(tmem + 64 * bb, tmem + kColQ + 8 * ks, bl, idS | tc::kNegateB, true);   // negated lo
             }
           }
           tc::mma_commit(s_full + 8 * bb);
@@ -323,7 +336,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             tc::mma_f16_ta(tmem + kColO, pl + 8 * kk, bh, idO, true);
             if constexpr (C::VQ) {
               const uint64_t bl = tc::sdesc_sw128(vb + kTile16 + kk * 2048, kT * 128, 1024);
-              tc::mma_f16_ta(tmem + kColO, ph + 8 * kk, bl, idO, true);
+              tc::mma_f16_ta(tmem + kColO, ph + 8 * kk, bl, idO | tc::kNegateB, true);   // negated lo
             }
           }
           tc::mma_commit(p_empty + 8 * bb);
@@ -339,7 +352,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   } else if (warp >= kConvWarp0) {
     // ---------------------------------------------------------------- q8_0 tile conversion
     if constexpr (C::CONV) {
+      constexpr int kItems = kT * 8 / (32 * kConvWarps);   // 16-code chunks per thread and tile
+      static_assert(kItems * 32 * kConvWarps == kT * 8, "converter items");
       const int ct = tid - 32 * kConvWarp0, nct = 32 * kConvWarps;
+      ConvItem items[kItems];
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) items[u] = conv_item(ct + nct * u);
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % C::NST, bb = t & 1;
         if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag, wl)) break;
@@ -347,14 +365,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const uint8_t* st = smem + s * C::STAGE;
         if constexpr (C::KQ) {
           if (t >= 2 && !wait_phase(kc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) break;
-          convert_q8(st, st + C::KSC_OFF, smem + C::KC_OFF + bb * 2 * kTile16, ct, nct, nv,
+          convert_q8<kItems>(st, st + C::KSC_OFF, smem + C::KC_OFF + bb * 2 * kTile16, items, nv,
                      tile_sigma(st + C::KSC_OFF, lane, nv));
           tc::fence_smem_to_async();
           warp_arrive(kc_full + 8 * bb, lane);
         }
         if constexpr (C::VQ) {
           if (t >= 2 && !wait_phase(vc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) break;
-          convert_q8(st + C::V_OFF, st + C::VSC_OFF, smem + C::VC_OFF + bb * 2 * kTile16, ct, nct, nv,
+          convert_q8<kItems>(st + C::V_OFF, st + C::VSC_OFF, smem + C::VC_OFF + bb * 2 * kTile16, items, nv,
                      tile_sigma(st + C::VSC_OFF, lane, nv));
           tc::fence_smem_to_async();
           warp_arrive(vc_full + 8 * bb, lane);

@@ -30,6 +30,9 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) 
   return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction-descriptor bit that negates B (bit 14; bit 13 negates A).
+constexpr uint32_t kNegateB = 1u << 14;
+
 // Tensor-memory allocation of `ncols` columns (a power of two >= 32) by one whole warp; the
 // base address is written to shared memory at `dst`.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
