@@ -800,6 +800,7 @@ def run_extras(torch, kvq, args, flush, peak):
         del ks, vs, rows_k, rows_v
         torch.cuda.empty_cache()
     out.extend(prefill_cells(torch, kvq, flush))
+    depth, T = 32768, 512
     # the same chunk at the long-context shape (GQA 16:1, head_dim 256)
     ptimes = {}
     for arm in ("f16/f16", "q8_0/q8_0"):

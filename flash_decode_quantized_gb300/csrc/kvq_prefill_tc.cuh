@@ -488,9 +488,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           tc::tmem_st32(tmem + lane_off + kColO + 64 * half + 32 * c, ov);
         }
       }
-      // p = 2^(s mul - m) (0 for masked entries and rows that saw nothing); PV takes p 2^(svt - sv_run)
-      const float nb = m == -INFINITY ? 0.0f : -m;
-      const float vsc = C::VQ ? __uint_as_float((uint32_t)(127 + svt - sv_run) << 23) : 1.0f;
+      // PV takes p 2^(svt - sv_run) with p = 2^(s mul - m) (0 for masked entries and rows
+      // that saw nothing): the power of two rides in the exponent, and l, a sum of true p,
+      // takes the tile's sum times 2^(sv_run - svt) (exact)
+      const float nb = (m == -INFINITY ? 0.0f : -m) + (C::VQ ? (float)(svt - sv_run) : 0.0f);
       float ph[16], pl[16];
       float2 ls[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
@@ -499,11 +500,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const float2 p = make_float2(fast_exp2(e.x), fast_exp2(e.y));
         ls[k & 1] = __fadd2_rn(ls[k & 1], p);
         uint32_t h, lo;
-        split2<false>(p.x * vsc, p.y * vsc, h, lo);
+        split2<false>(p.x, p.y, h, lo);
         ph[k] = __uint_as_float(h);
         pl[k] = __uint_as_float(lo);
       }
-      l += (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
+      const float lt = (ls[0].x + ls[1].x) + (ls[0].y + ls[1].y);
+      l += C::VQ ? lt * __uint_as_float((uint32_t)(127 + sv_run - svt) << 23) : lt;
       // P buffer bb is free once PV(t - 2) is done
       if (t >= 2 && !wait_phase(p_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) { ok = false; break; }
       tc::fence_after_sync();
