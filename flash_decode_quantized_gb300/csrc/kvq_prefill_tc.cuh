@@ -1,5 +1,6 @@
 // Chunked prefill attention on the 5th-generation tensor cores (tcgen05, operands and
-// accumulators in tensor memory), head_dim 128, K and V each q8_0 or f16: the
+// accumulators in tensor memory), head_dim 128, K and V each q8_0 or f16, or bf16 / bf16 and
+// q8_0 / bf16 (a bf16 side takes bf16 operands: Q for a bf16 K, P for a bf16 V): the
 // prompt-processing arm of halobench record clm-0022's depth tables (pp512 at depth), with
 // the dequantization fused into the load of each KV tile.
 //
@@ -48,6 +49,9 @@ constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kLoadWarp = 9, kConvWarp0 = 10, k
 template <int KC, int VC>
 struct TCfg {
   static constexpr bool KQ = KC == KVQ_CODEC_Q8_0, VQ = VC == KVQ_CODEC_Q8_0, CONV = KQ || VQ;
+  // 16-bit types of the two products: bf16 when that side's 16-bit operand is bf16 (Q and
+  // a bf16 K; P and a bf16 V), f16 otherwise
+  static constexpr bool SBF = KC == KVQ_CODEC_BF16, PBF = VC == KVQ_CODEC_BF16;
   static constexpr int THREADS = 32 * (CONV ? kConvWarp0 + kConvWarps : kConvWarp0);
   static constexpr int NB = kD / kBlock;
   static constexpr int KRB = KQ ? kD : 2 * kD, VRB = VQ ? kD : 2 * kD;
@@ -290,7 +294,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issue
-    const uint32_t idS = tc::idesc_f16(kRows, kT, false), idO = tc::idesc_f16(kRows, kD, true);
+    const uint32_t idS = tc::idesc_f16(kRows, kT, false, C::SBF), idO = tc::idesc_f16(kRows, kD, true, C::PBF);
     bool ok = wait_phase(q_full, 0, abort_flag, wl);
     tc::fence_after_sync();
     for (int t = 0; ok && t <= n_tiles; ++t) {
@@ -403,10 +407,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (qv) x = *reinterpret_cast<const uint4*>(qrow + 8 * c);
         const float2 f0 = unpack2<true>(x.x), f1 = unpack2<true>(x.y), f2 = unpack2<true>(x.z),
                      f3 = unpack2<true>(x.w);
-        w[4 * c + 0] = __uint_as_float(pack2<false>(f0.x, f0.y));
-        w[4 * c + 1] = __uint_as_float(pack2<false>(f1.x, f1.y));
-        w[4 * c + 2] = __uint_as_float(pack2<false>(f2.x, f2.y));
-        w[4 * c + 3] = __uint_as_float(pack2<false>(f3.x, f3.y));
+        w[4 * c + 0] = __uint_as_float(pack2<C::SBF>(f0.x, f0.y));   // bf16 Q for a bf16 K: as given
+        w[4 * c + 1] = __uint_as_float(pack2<C::SBF>(f1.x, f1.y));
+        w[4 * c + 2] = __uint_as_float(pack2<C::SBF>(f2.x, f2.y));
+        w[4 * c + 3] = __uint_as_float(pack2<C::SBF>(f3.x, f3.y));
       }
       tc::tmem_st32(tmem + lane_off + kColQ + 32 * half, w);
       tc::fence_before_sync();
@@ -500,7 +504,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const float2 p = make_float2(fast_exp2(e.x), fast_exp2(e.y));
         ls[k & 1] = __fadd2_rn(ls[k & 1], p);
         uint32_t h, lo;
-        split2<false>(p.x, p.y, h, lo);
+        split2<C::PBF>(p.x, p.y, h, lo);
         ph[k] = __uint_as_float(h);
         pl[k] = __uint_as_float(lo);
       }

@@ -23,11 +23,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: f32 accumulator (bits 4-5 = 1), A and B f16 (bits
-// 7-9, 10-12 = 0), A K-major (bit 15 = 0), B K-major or MN-major (bit 16), N >> 3 (bits
-// 17-22), M >> 4 (bits 24-28); dense, no negation, no saturation.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
-  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: f32 accumulator (bits 4-5 = 1), A and B both f16 (0)
+// or both bf16 (1) (bits 7-9, 10-12), A K-major (bit 15 = 0), B K-major or MN-major (bit
+// 16), N >> 3 (bits 17-22), M >> 4 (bits 24-28); dense, no negation, no saturation.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major, bool bf16 = false) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction-descriptor bit that negates B (bit 14; bit 13 negates A).
