@@ -15,8 +15,9 @@
 //  * S = Q K^T: M 128 x N 64 x K 128, Q in tensor memory, two MMAs per K step for a q8_0 K
 //    (hi and lo), into one of two 64-column score buffers;
 //  * softmax by row (two threads per row, one per 32-score half, the row maximum traded
-//    through shared memory; base 2, lazy running maximum as in the decode kernels); P goes
-//    to tensor memory as f16 hi + lo (P = P_h + P_l to ~22 bits);
+//    through shared memory under an mbarrier of the warp pair; base 2, lazy running maximum
+//    as in the decode kernels); P goes to tensor memory as 16-bit hi + lo (P = P_h + P_l to
+//    ~22 bits in f16, ~16 in bf16);
 //  * O += P V: M 128 x N 128 x K 64, V as an MN-major operand straight from the tile layout;
 //    P_h V_h + P_l V_h (+ P_h V_l for a q8_0 V), O in 128 tensor-memory columns.  A q8_0 V
 //    tile carries its own 2^-sigma; O is kept in units of the largest sigma so far and
