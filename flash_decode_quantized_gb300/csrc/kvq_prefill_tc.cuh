@@ -1,32 +1,32 @@
 // Chunked prefill attention on the 5th-generation tensor cores (tcgen05, operands and
-// accumulators in tensor memory), head_dim 128, K and V each q8_0 or f16, or bf16 / bf16 and
-// q8_0 / bf16 (a bf16 side takes bf16 operands: Q for a bf16 K, P for a bf16 V): the
-// prompt-processing arm of halobench record clm-0022's depth tables (pp512 at depth), with
-// the dequantization fused into the load of each KV tile.
+// accumulators in tensor memory), head_dim 128, K and V each q8_0, q4s or f16, or bf16 /
+// bf16, q8_0 / bf16 and q4s / bf16 (a bf16 side takes bf16 operands: Q for a bf16 K, P for
+// a bf16 V): the prompt-processing arm of halobench record clm-0022's depth tables (pp512 at
+// depth), with the dequantization fused into the load of each KV tile.
 //
 // A CTA owns 128 query rows of one (sequence, KV head), row = token * G + head-in-group,
 // one per tensor-memory lane.  Per 64-token KV tile:
-//  * the tile arrives by TMA in the 128-byte swizzled layout that the MMA reads; a q8_0 tile
-//    is turned, once for all 128 rows, into two f16 tiles of the same layout that give d q
-//    exactly (hi = d q rounded, lo = its rounding error, exact in f16: d has 11 significant
-//    bits and q 7; lo is stored negated and read with the MMA's negate-B bit), with a power
-//    of two 2^-sigma folded in per tile (from the tile's largest scale) that keeps every hi
-//    below 2^15;
-//  * S = Q K^T: M 128 x N 64 x K 128, Q in tensor memory, two MMAs per K step for a q8_0 K
-//    (hi and lo), into one of two 64-column score buffers;
+//  * the tile arrives by TMA in the swizzled layout that the MMA reads (16-bit codecs); a
+//    q8_0 or q4s tile is turned, once for all 128 rows, into two f16 tiles of that layout
+//    that give d q exactly (hi = d q rounded, lo = its rounding error, exact in f16: d has
+//    11 significant bits and q at most 7; lo is stored negated and read with the MMA's
+//    negate-B bit), with a power of two 2^-sigma folded in per tile (from the tile's largest
+//    scale) that keeps every hi below 2^15;
+//  * S = Q K^T: M 128 x N 64 x K 128, Q in tensor memory, two MMAs per K step for a quantized
+//    K (hi and lo), into one of two 64-column score buffers;
 //  * softmax by row (two threads per row, one per 32-score half, the row maximum traded
 //    through shared memory under an mbarrier of the warp pair; base 2, lazy running maximum
 //    as in the decode kernels); P goes to tensor memory as 16-bit hi + lo (P = P_h + P_l to
 //    ~22 bits in f16, ~16 in bf16);
 //  * O += P V: M 128 x N 128 x K 64, V as an MN-major operand straight from the tile layout;
-//    P_h V_h + P_l V_h (+ P_h V_l for a q8_0 V), O in 128 tensor-memory columns.  A q8_0 V
-//    tile carries its own 2^-sigma; O is kept in units of the largest sigma so far and
-//    rescaled (with the lazy maximum's rescale) when it grows.
+//    P_h V_h + P_l V_h (+ P_h V_l for a quantized V), O in 128 tensor-memory columns.  A
+//    quantized V tile carries its own 2^-sigma; O is kept in units of the largest sigma so
+//    far and rescaled (with the lazy maximum's rescale) when it grows.
 // Warp roles, linked by mbarriers only (no CTA-wide barrier inside the tile loop):
 //  warps 0-7 softmax (warp w: rows 32 (w % 4) .. + 31, its tensor-memory lanes, score half
 //  w / 4), warp 8 issues the MMAs (S of tile t, then PV of tile t - 1, so the tensor cores
 //  compute S(t) during the softmax of tile t - 1), warp 9 loads tiles, warps 10-17 convert
-//  q8_0 tiles (double buffered).  Every wait is bounded; a wait that runs out raises a
+//  q8_0 / q4s tiles (double buffered).  Every wait is bounded; a wait that runs out raises a
 //  CTA-wide abort flag that the other waits watch, and the timeout is reported in the K
 //  store's status word.
 #pragma once
@@ -49,13 +49,14 @@ constexpr int kSoftmaxWarps = 8, kMmaWarp = 8, kLoadWarp = 9, kConvWarp0 = 10, k
 
 template <int KC, int VC>
 struct TCfg {
-  static constexpr bool KQ = KC == KVQ_CODEC_Q8_0, VQ = VC == KVQ_CODEC_Q8_0, CONV = KQ || VQ;
+  static constexpr bool K4 = KC == KVQ_CODEC_Q4S, V4 = VC == KVQ_CODEC_Q4S;   // 4-bit codes
+  static constexpr bool KQ = KC == KVQ_CODEC_Q8_0 || K4, VQ = VC == KVQ_CODEC_Q8_0 || V4, CONV = KQ || VQ;
   // 16-bit types of the two products: bf16 when that side's 16-bit operand is bf16 (Q and
   // a bf16 K; P and a bf16 V), f16 otherwise
   static constexpr bool SBF = KC == KVQ_CODEC_BF16, PBF = VC == KVQ_CODEC_BF16;
   static constexpr int THREADS = 32 * (CONV ? kConvWarp0 + kConvWarps : kConvWarp0);
   static constexpr int NB = kD / kBlock;
-  static constexpr int KRB = KQ ? kD : 2 * kD, VRB = VQ ? kD : 2 * kD;
+  static constexpr int KRB = K4 ? kD / 2 : KQ ? kD : 2 * kD, VRB = V4 ? kD / 2 : VQ ? kD : 2 * kD;
   static constexpr int KROWS = kT * KRB, VROWS = kT * VRB;
   static constexpr int KSC = KQ ? kT * NB * 2 : 0, VSC = VQ ? kT * NB * 2 : 0;
   static constexpr int V_OFF = KROWS, KSC_OFF = KROWS + VROWS, VSC_OFF = KSC_OFF + KSC;
@@ -143,6 +144,59 @@ __device__ __forceinline__ void convert_q8(const uint8_t* rows, const uint8_t* s
     *reinterpret_cast<uint4*>(dst + it[u].dst1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
     *reinterpret_cast<uint4*>(dst + kTile16 + it[u].dst0) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     *reinterpret_cast<uint4*>(dst + kTile16 + it[u].dst1) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  }
+}
+
+// The same for a q4s tile: rows of 64 bytes (TMA's 64-byte swizzle: 16-byte chunk c of row t
+// at c ^ ((t >> 1) & 3)), chunk c = block c = dims 32 c .. 32 c + 31, byte j of it holding
+// dims 2 j (low nibble) and 2 j + 1 (high nibble) as q + 8.
+struct Conv4Item {
+  uint32_t src, scale, dst[4];
+  int row;
+};
+__device__ __forceinline__ Conv4Item conv4_item(int i) {
+  const int t = i >> 2, c = i & 3;   // row, 32-code block
+  Conv4Item it;
+  it.src = (uint32_t)(t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
+  it.scale = (uint32_t)((t * 4 + c) * 2);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) it.dst[j] = tile_chunk(t, 4 * c + j);
+  it.row = t;
+  return it;
+}
+constexpr uint32_t kQ4Mul = 0x2C003C00u;   // f16 pair (1, 1/16)
+constexpr uint32_t kQ4Add = 0xD480E408u;   // f16 pair (-1032, -72)
+template <int NI>
+__device__ __forceinline__ void convert_q4(const uint8_t* rows, const uint8_t* sc, uint8_t* dst, const Conv4Item* it,
+                                           int n_valid, int sigma) {
+  const float f = __uint_as_float((uint32_t)(127 - sigma) << 23);
+#pragma unroll
+  for (int u = 0; u < NI; ++u) {
+    uint32_t hi[16], lo[16];
+    if (it[u].row < n_valid) {
+      const uint4 w = *reinterpret_cast<const uint4*>(rows + it[u].src);
+      const float d = __half2float(*reinterpret_cast<const __half*>(sc + it[u].scale)) * f;
+      const uint32_t d2 = pack2<false>(d, d), nd2 = d2 ^ 0x80008000u;
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        // byte j twice, as (1024 + low nibble, 1024 + 16 high nibble), then both codes exactly
+        const uint32_t y = __byte_perm(ws[j >> 2], 0u, 0x4040u + 0x0101u * (uint32_t)(j & 3));
+        const uint32_t q2 = hfma2_u32(and_or(y, 0x00F0000Fu, 0x64006400u), kQ4Mul, kQ4Add);
+        __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&q2), *reinterpret_cast<const __half2*>(&d2));
+        hi[j] = *reinterpret_cast<uint32_t*>(&h);
+        lo[j] = hfma2_u32(q2, nd2, hi[j]);   // hi - d q, exact
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) hi[j] = lo[j] = 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      *reinterpret_cast<uint4*>(dst + it[u].dst[j]) = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+      *reinterpret_cast<uint4*>(dst + kTile16 + it[u].dst[j]) =
+          make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+    }
   }
 }
 
@@ -271,10 +325,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           mbar_expect_tx(full, C::TX);
           const uint32_t st = sbase + s * C::STAGE;
 #pragma unroll
-          for (int seg = 0; seg < C::KRB / 128; ++seg)
+          for (int seg = 0; seg < (C::KRB + 127) / 128; ++seg)
             tma_load_4d(st + seg * kT * 128, &tmk, seg * 128, rr0, kvh, page, full);
 #pragma unroll
-          for (int seg = 0; seg < C::VRB / 128; ++seg)
+          for (int seg = 0; seg < (C::VRB + 127) / 128; ++seg)
             tma_load_4d(st + C::V_OFF + seg * kT * 128, &tmv, seg * 128, rr0, kvh, page, full);
           if constexpr (C::KQ)
             bulk_load(st + C::KSC_OFF, a.k.buf + ((long long)page * a.k.num_kv_heads + kvh) * a.k.slab_bytes +
@@ -355,14 +409,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     if (lane == 0) tc::mma_commit(bar_drain);
     mbar_wait_warp(bar_drain, 0, 1 << 20);
   } else if (warp >= kConvWarp0) {
-    // ---------------------------------------------------------------- q8_0 tile conversion
+    // ---------------------------------------------------------------- q8_0 / q4s tile conversion
     if constexpr (C::CONV) {
-      constexpr int kItems = kT * 8 / (32 * kConvWarps);   // 16-code chunks per thread and tile
-      static_assert(kItems * 32 * kConvWarps == kT * 8, "converter items");
+      constexpr int kItems = kT * 8 / (32 * kConvWarps);    // q8_0: 16-code chunks per thread and tile
+      constexpr int kItems4 = kT * 4 / (32 * kConvWarps);   // q4s: 32-code blocks per thread and tile
+      static_assert(kItems * 32 * kConvWarps == kT * 8 && kItems4 * 32 * kConvWarps == kT * 4, "converter items");
       const int ct = tid - 32 * kConvWarp0, nct = 32 * kConvWarps;
       ConvItem items[kItems];
+      Conv4Item items4[kItems4];
 #pragma unroll
       for (int u = 0; u < kItems; ++u) items[u] = conv_item(ct + nct * u);
+#pragma unroll
+      for (int u = 0; u < kItems4; ++u) items4[u] = conv4_item(ct + nct * u);
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % C::NST, bb = t & 1;
         if (!wait_phase(bar_full + 8 * s, (t / C::NST) & 1, abort_flag, wl)) break;
@@ -370,15 +428,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const uint8_t* st = smem + s * C::STAGE;
         if constexpr (C::KQ) {
           if (t >= 2 && !wait_phase(kc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) break;
-          convert_q8<kItems>(st, st + C::KSC_OFF, smem + C::KC_OFF + bb * 2 * kTile16, items, nv,
-                     tile_sigma(st + C::KSC_OFF, lane, nv));
+          const int sg = tile_sigma(st + C::KSC_OFF, lane, nv);
+          if constexpr (C::K4) convert_q4<kItems4>(st, st + C::KSC_OFF, smem + C::KC_OFF + bb * 2 * kTile16, items4, nv, sg);
+          else convert_q8<kItems>(st, st + C::KSC_OFF, smem + C::KC_OFF + bb * 2 * kTile16, items, nv, sg);
           tc::fence_smem_to_async();
           warp_arrive(kc_full + 8 * bb, lane);
         }
         if constexpr (C::VQ) {
           if (t >= 2 && !wait_phase(vc_empty + 8 * bb, ((t >> 1) - 1) & 1, abort_flag, wl)) break;
-          convert_q8<kItems>(st + C::V_OFF, st + C::VSC_OFF, smem + C::VC_OFF + bb * 2 * kTile16, items, nv,
-                     tile_sigma(st + C::VSC_OFF, lane, nv));
+          const int sg = tile_sigma(st + C::VSC_OFF, lane, nv);
+          if constexpr (C::V4)
+            convert_q4<kItems4>(st + C::V_OFF, st + C::VSC_OFF, smem + C::VC_OFF + bb * 2 * kTile16, items4, nv, sg);
+          else convert_q8<kItems>(st + C::V_OFF, st + C::VSC_OFF, smem + C::VC_OFF + bb * 2 * kTile16, items, nv, sg);
           tc::fence_smem_to_async();
           warp_arrive(vc_full + 8 * bb, lane);
         }

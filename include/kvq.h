@@ -257,13 +257,13 @@ kvq_status kvq_flash_decode_multi(const void* q, const kvq_store* k_store, const
  * [0, seq_lens[b] - num_tokens + i] (causal inside the chunk, everything before it).
  *   q    device bf16 [batch][num_tokens][num_q_heads][head_dim] (16-byte aligned)
  *   out  device fp32 [batch][num_tokens][num_q_heads][head_dim]
- * One launch, no workspace; each CTA streams the KV prefix of one KV head once.  At
- * head_dim 128 with K and V each q8_0 or f16 (four pairs), bf16/bf16 or q8_0/bf16, a CTA
- * owns 128 (token, head) query rows on the 5th-generation tensor cores (scores, P and O in
- * tensor memory, q8_0 tiles turned once per CTA into exact f16 hi + lo operands); otherwise
- * 64 rows on the warp-level MMA path, built for head_dim 64, 128 and 256 and the pairs of
- * kvq_flash_decode's tensor-core kernel (bf16/bf16, f16/f16, q8_0/bf16, q8_0/q8_0, q4s/q4s,
- * q8_0/q4s, q4s/q8_0, q4s/bf16).  Other pairs give KVQ_ERR_UNSUPPORTED.  Unless K is bf16,
+ * One launch, no workspace; each CTA streams the KV prefix of one KV head once.  Built for
+ * the pairs of kvq_flash_decode's tensor-core kernel (bf16/bf16, f16/f16, q8_0/bf16,
+ * q8_0/q8_0, q4s/q4s, q8_0/q4s, q4s/q8_0, q4s/bf16) at head_dim 64, 128 and 256, and for
+ * q8_0/f16 and f16/q8_0 at 128.  At head_dim 128 a CTA owns 128 (token, head) query rows on
+ * the 5th-generation tensor cores (scores, P and O in tensor memory, quantized tiles turned
+ * once per CTA into exact f16 hi + lo operands); at 64 and 256, 64 rows on the warp-level
+ * MMA path.  Other pairs give KVQ_ERR_UNSUPPORTED.  Unless K is bf16,
  * Q must lie in the f16 range (it is rounded to f16 once).  softmax_scale <= 0 selects
  * 1/sqrt(head_dim).  Device faults as for kvq_flash_decode. */
 kvq_status kvq_prefill_attention(const void* q, const kvq_store* k_store, const kvq_store* v_store,

@@ -145,7 +145,8 @@ def test_device_timeout_is_recorded_and_the_next_call_runs(hq, hkv, d, kc, skip)
 
 
 
-@pytest.mark.parametrize("kc,vc,skip", [("q8_0", "q8_0", 2), ("f16", "f16", 0), ("q8_0", "f16", 1)])
+@pytest.mark.parametrize("kc,vc,skip", [("q8_0", "q8_0", 2), ("f16", "f16", 0), ("q8_0", "f16", 1),
+                                        ("q4s", "q4s", 1)])
 def test_prefill_device_timeout_is_recorded_and_the_next_call_runs(kc, vc, skip):
     # The tensor-core prefill (head_dim 128): a tile that the producer never issues (no copy,
     # no arrival) leaves the waits on it to run out; the CTA raises its abort flag, every
