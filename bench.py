@@ -83,10 +83,10 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_sha() -> str:
-    """Hash of the device-code sources the decode kernels are built from: the tensor-core
-    decode instantiation units and every header they include, directly or not (the prefill
-    kernels' own headers are not among them)."""
+def decode_source_files() -> list:
+    """The device-code sources the decode kernels are built from: the tensor-core decode
+    instantiation units and every header they include, directly or not (the prefill
+    kernels' own headers are not among them), sorted."""
     csrc = os.path.join(ROOT, "flash_decode_quantized_gb300", "csrc")
     files = sorted(n for n in os.listdir(csrc) if n.startswith("mma_") and n.endswith(".cu"))
     todo, seen = list(files), set(files)
@@ -96,8 +96,14 @@ def kernel_sources_sha() -> str:
             if m and m.group(1) not in seen and os.path.exists(os.path.join(csrc, m.group(1))):
                 seen.add(m.group(1))
                 todo.append(m.group(1))
+    return sorted(seen)
+
+
+def kernel_sources_sha() -> str:
+    """Hash of decode_source_files(), in order."""
+    csrc = os.path.join(ROOT, "flash_decode_quantized_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(seen):
+    for name in decode_source_files():
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -51,3 +51,15 @@ def test_single_process_is_unchanged():
     import bench
     assert bench.max_over_ranks(torch, 0.0123, 1, "cpu") == 0.0123
     assert bench.job_gbs(1e9, 1, 1.0) == pytest.approx(1000.0)
+
+
+def test_decode_source_hash_covers_the_decode_include_closure_only():
+    # the DRAM-traffic rows are keyed by a hash of the decode kernels' sources: every decode
+    # instantiation unit and header they include counts, the prefill kernels' headers do not
+    import bench
+    files = bench.decode_source_files()
+    for name in ("kvq_decode_mma.cuh", "kvq_decode_hm.cuh", "kvq_encode.cuh", "mma_q8_0_q8_0.cu"):
+        assert name in files
+    for name in ("kvq_prefill.cuh", "kvq_prefill_tc.cuh", "kvq_tc.cuh", "prefill_pairs.cu"):
+        assert name not in files
+    assert len(bench.kernel_sources_sha()) == 16
