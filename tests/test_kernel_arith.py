@@ -1,5 +1,15 @@
-"""The arithmetic the tensor-core prefill kernel relies on, checked exhaustively in float64 /
-float16 on the CPU (numpy only; no oracle, no CUDA):
+"""Bit-level arithmetic the CUDA kernels rely on, checked exhaustively in float64 / float16
+on the CPU (numpy only; no oracle, no CUDA).
+
+Decode (the magic-number conversions of integer codes to f16 in registers):
+
+* an 8-bit code q, its byte flipped to q + 128 and placed under the f16 exponent byte 0x64,
+  is the f16 value 1152 + q, and one f16 subtraction of 1152 gives q exactly;
+* a 4-bit code stored as u = q + 8: in mantissa bits 0-3 under 0x64 it is 1024 + u (less
+  1032 gives q); in bits 4-7 under 0x64 it is 1024 + 16 u, and one fma with (1/16, -72) gives
+  q; in bits 4-7 under 0x48 (the K form) it is 9 + q / 8.
+
+Tensor-core prefill:
 
 * a quantized tile becomes two f16 operands, hi = d q rounded and nlo = hi - d q (stored
   negated, read with the MMA's negate-B bit), with d the block scale times the tile's power
@@ -72,3 +82,22 @@ def test_q4s_byte_to_code_pair():
     q_hi = rn16(hi * mul_hi + add_hi)
     assert np.array_equal(q_lo, (b & 15).astype(np.float64) - 8)
     assert np.array_equal(q_hi, (b >> 4).astype(np.float64) - 8)
+
+
+def test_8bit_code_under_0x64_less_1152_is_the_code():
+    q = np.arange(-128, 128)
+    u = (q + 128) & 0xFF                          # the byte after the sign flip (xor 0x80)
+    x = f16(0x6400 | u)
+    assert np.array_equal(x, 1152.0 + q)
+    assert np.array_equal(rn16(x - f16(0x6480)), q.astype(np.float64))   # 0x6480 = 1152
+
+
+def test_4bit_code_forms():
+    q = np.arange(-8, 8)
+    u = q + 8
+    low = f16(0x6400 | u)                          # mantissa bits 0-3
+    assert np.array_equal(low, 1032.0 + q) and np.array_equal(rn16(low - f16(0x6408)), q.astype(np.float64))
+    high = f16(0x6400 | (u << 4))                  # mantissa bits 4-7
+    assert np.array_equal(rn16(high * f16(0x2C00) + f16(0xD480)), q.astype(np.float64))   # (x / 16) - 72
+    k_form = f16(0x4800 | (u << 4))                # the K codes: 8 + u / 8
+    assert np.array_equal(k_form, 9.0 + q / 8.0)
