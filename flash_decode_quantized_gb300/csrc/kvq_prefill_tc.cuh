@@ -456,7 +456,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // exchanges with the other warp of these rows: bounded mbarrier waits (an abort cannot
     // leave one of the two waiting for good)
     const uint32_t my_xch = xch + 24 * (warp & 3);
-    // Q row, dims 64 half .. + 63 -> f16 pairs in tensor-memory columns kColQ + 32 half ..
+    // Q row, dims 64 half .. + 63 -> 16-bit pairs (f16; bf16 for a bf16 K) in tensor-memory
+    // columns kColQ + 32 half ..
     {
       const bool qv = r < rows_total;
       const __nv_bfloat16* qrow =
